@@ -1,0 +1,545 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 grouped-query decode attention library.
+
+One step = one decode call over the configuration's whole synthetic KV cache
+(the dense path: split kernel + LSE combine; or the sparse paged FP8 path),
+with inputs resident in HBM and the L2 flushed (a memset larger than L2)
+before every step.  Prints one JSON line on rank 0.
+
+Metric: KV-cache HBM GB/s on K/V bytes read once, with the byte model of
+"Attention Kernel Portability Across GPU Architectures", section "Decode"
+(2 * B * Hkv * N * D * bytes per element), plus us per call.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config NAME] [--impl gqa|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this project
+has) on the host cores, on the same workload and metric.  Under torchrun
+(N > 1) each rank runs an independent replica of the workload (the path needs
+no collective); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gqa_inputs  # noqa: E402
+
+METRIC = "GQA decode µs/call and KV-cache HBM GB/s (% of measured GB300 peak)"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["gqa_dense_kernel.cuh", "gqa_paged_kernel.cuh", "gqa_common.cuh", "gqa_params.h",
+                  "gqa_dense_impl.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# host-side accounting (unit-tested on CPU)
+# ---------------------------------------------------------------------------
+def kv_bytes(B: int, Hkv: int, N: int, D: int, bytes_per_elem: int) -> int:
+    """K and V bytes of one decode step, each byte counted once."""
+    return 2 * B * Hkv * N * D * bytes_per_elem
+
+
+def dense_flops(B, Hq, Sq, Skv, D) -> int:
+    return 4 * B * Hq * Sq * Skv * D
+
+
+def paged_flops(B, Hq, topk, D) -> int:
+    return 4 * B * topk * Hq * D
+
+
+def workload_kv_bytes(cfg) -> int:
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        return kv_bytes(cfg.B, cfg.Hkv, cfg.Skv, cfg.D, 2)
+    return kv_bytes(cfg.B, cfg.Hkv, cfg.topk, cfg.D, 1)
+
+
+def workload_config(cfg) -> dict:
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        return {"workload": cfg.name, "B": cfg.B, "Sq": cfg.Sq, "Skv": cfg.Skv, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+                "D": cfg.D, "kv_dtype": "bf16", "mask": "bottom-right causal" if cfg.Sq > 1 else "none"}
+    return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
+            "page_size": cfg.page_size, "pages_per_req": cfg.pages_per_req, "num_pages": cfg.num_pages,
+            "topk": cfg.topk, "kv_dtype": "fp8_e4m3fn"}
+
+
+def gbs(nbytes: float, ms: float) -> float:
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def percentile(xs, p):
+    xs = sorted(xs)
+    if not xs:
+        return float("nan")
+    k = (len(xs) - 1) * p / 100.0
+    lo, hi = math.floor(k), math.ceil(k)
+    return xs[lo] + (xs[hi] - xs[lo]) * (k - lo)
+
+
+def parse_clocks(csv_text: str) -> dict | None:
+    """Summary of `nvidia-smi --query-gpu=... --format=csv -lms` samples."""
+    lines = [ln.strip() for ln in csv_text.strip().splitlines() if ln.strip()]
+    if len(lines) < 2:
+        return None
+    hdr = [h.strip() for h in lines[0].split(",")]
+    rows = [[c.strip() for c in ln.split(",")] for ln in lines[1:] if not ln.startswith("index")]
+    rows = [r for r in rows if len(r) == len(hdr)]
+    if not rows:
+        return None
+
+    def col(name):
+        for i, h in enumerate(hdr):
+            if h.startswith(name):
+                return i
+        return None
+
+    ism, imax, ipow = col("clocks.current.sm") or col("clocks.sm"), col("clocks.max.sm"), col("power.draw")
+
+    def num(s):
+        try:
+            return float(s.split()[0])
+        except (ValueError, IndexError):
+            return float("nan")
+
+    sm = [num(r[ism]) for r in rows] if ism is not None else []
+    mx = [num(r[imax]) for r in rows] if imax is not None else []
+    pw = [num(r[ipow]) for r in rows] if ipow is not None else []
+    # samples under load: power above the midpoint of the observed range
+    if pw and max(pw) > min(pw):
+        thr = 0.5 * (max(pw) + min(pw))
+        loaded = [s for s, p in zip(sm, pw) if p >= thr]
+    else:
+        loaded = sm
+    reasons = set()
+    for i, h in enumerate(hdr):
+        if h.startswith("clocks_event_reasons.") and h != "clocks_event_reasons.active":
+            if any(r[i].lower().startswith("active") for r in rows):
+                reasons.add(h.split(".", 1)[1].split(" ")[0])
+    return {"sm_mhz": statistics.median(loaded) if loaded else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+def measured_hbm_peak() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gqa_decode_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+def reduce_over_ranks(values: list[float], op: str = "max") -> list[float]:
+    """Element-wise reduction across torch.distributed ranks (identity at N=1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return t.cpu().tolist()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        with open(self.path) as f:
+            text = f.read()
+        os.unlink(self.path)
+        return parse_clocks(text)
+
+
+# ---------------------------------------------------------------------------
+# the library arm
+# ---------------------------------------------------------------------------
+def _dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def _barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def _make_call(gq, cfg, dev, seed_offset):
+    import torch
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        q, k, v = gqa_inputs.dense_inputs(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D,
+                                          cfg.seed + seed_offset, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((cfg.B, cfg.Hq, cfg.Sq), dtype=torch.float32, device=dev)
+
+        def call():
+            gq.gqa_decode(q, k, v, out=out, lse=lse)
+        splits = gq.gqa_decode_num_splits(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D)
+        return call, dict(q=q, k=k, v=v, out=out, lse=lse), (2 if splits > 1 else 1), splits
+    inp = gqa_inputs.paged_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
+                                  cfg.num_pages, cfg.topk, cfg.seed + seed_offset, device=dev)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty((cfg.B, cfg.Hq), dtype=torch.float32, device=dev)
+
+    def call():
+        gq.gqa_decode_paged_fp8(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["page_table"],
+                                inp["topk"], inp["k_scale"], inp["v_scale"], out=out, lse=lse)
+    return call, dict(inp, out=out, lse=lse), 1, 1
+
+
+def _copy_peak_gbs(dev) -> float:
+    """Device-to-device copy bandwidth (read + write bytes) of a 2 GiB copy,
+    best of 5, measured in this run."""
+    import torch
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = 0.0
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, gbs(2 * a.numel() * a.element_size(), e0.elapsed_time(e1)))
+    del a, b
+    torch.cuda.empty_cache()
+    return best
+
+
+def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
+    """The fp64 oracle, as it stands, on this host's cores: the full workload
+    repeated until min_seconds (or a row subset when one pass would exceed
+    max_seconds)."""
+    import oracle
+    orc = oracle.load()
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        q, k, v = (tensors[n].cpu() for n in ("q", "k", "v"))
+        nrows = cfg.B * cfg.Hq * cfg.Sq
+        t0 = time.perf_counter()
+        orc.gqa_decode(q, k, v, cfg.scale, rows=list(range(min(nrows, 8))))
+        per_row = (time.perf_counter() - t0) / min(nrows, 8)
+        rows = None if per_row * nrows <= max_seconds else list(range(max(1, int(max_seconds / 3 / per_row))))
+        frac = 1.0 if rows is None else len(rows) / nrows
+        reps, elapsed = 0, 0.0
+        while elapsed < min_seconds and reps < 1000:
+            t0 = time.perf_counter()
+            orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
+            elapsed += time.perf_counter() - t0
+            reps += 1
+        sample = (f"{'all' if rows is None else len(rows)} of {nrows} query rows "
+                  f"(the rows of whole KV-head groups), {reps} pass(es)")
+    else:
+        cpu = {n: (t.cpu() if hasattr(t, "cpu") else t) for n, t in tensors.items()}
+        nrows = cfg.B * cfg.Hq
+        t0 = time.perf_counter()
+        orc.gqa_decode_paged_fp8(cpu["q"], cpu["gate"], cpu["k_pool"], cpu["v_pool"], cpu["page_table"],
+                                 cpu["topk"], cpu["k_scale"], cpu["v_scale"], cfg.scale, rows=list(range(64)))
+        per_row = (time.perf_counter() - t0) / 64
+        rows = None if per_row * nrows <= max_seconds else list(range(int(max_seconds / 3 / per_row)))
+        frac = 1.0 if rows is None else len(rows) / nrows
+        reps, elapsed = 0, 0.0
+        while elapsed < min_seconds and reps < 1000:
+            t0 = time.perf_counter()
+            orc.gqa_decode_paged_fp8(cpu["q"], cpu["gate"], cpu["k_pool"], cpu["v_pool"], cpu["page_table"],
+                                     cpu["topk"], cpu["k_scale"], cpu["v_scale"], cfg.scale, rows=rows)
+            elapsed += time.perf_counter() - t0
+            reps += 1
+        sample = f"{'all' if rows is None else len(rows)} of {nrows} (request, head) rows, {reps} pass(es)"
+    per_pass = elapsed / reps
+    # KV bytes in proportion to the rows covered (every row reads its group's K/V)
+    return {"value": gbs(workload_kv_bytes(cfg) * frac, per_pass * 1e3), "unit": "GB/s",
+            "cores": orc.num_threads(), "kind": "oracle", "sample": sample,
+            "us_per_call_equiv": per_pass / frac * 1e6}
+
+
+def run_gqa(args) -> int:
+    import torch
+    world, rank, local = _dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from gqa_decode_attention_gb300 import build as gbuild
+    if rank == 0:
+        gbuild.build()
+    _barrier()
+    import gqa_decode_attention_gb300 as gq
+    gq.load_library()
+    cfg = gqa_inputs.CONFIGS[args.config]
+    nbytes = workload_kv_bytes(cfg)
+    peak, peak_kind = measured_hbm_peak()
+
+    copy_peak = _copy_peak_gbs(dev)
+    call, tensors, launches_per_call, splits = _make_call(gq, cfg, dev, seed_offset=rank)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(512 << 20, 4 * l2), dtype=torch.uint8, device=dev)
+
+    def step_events(n, hook=False):
+        times, ktimes = [], []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if hook:
+                k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                # record once from torch so it treats them as recorded; the
+                # library re-records both around its kernel (latest record wins)
+                k0.record()
+                k1.record()
+                gq.gqa_debug_set_kernel_events(k0, k1)
+            e0.record()
+            call()
+            e1.record()
+            if hook:
+                gq.gqa_debug_set_kernel_events(None, None)
+                ktimes.append((k0, k1))
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        return ([a.elapsed_time(b) for a, b in times], [a.elapsed_time(b) for a, b in ktimes])
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    if gq.gqa_device_status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: exactly K steps
+    _barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ms, _ = step_events(args.steps)
+    torch.cuda.synchronize()
+    _barrier()
+    clocks = clk.summary()
+    total_ms = sum(step_ms)
+    (max_total_ms,) = reduce_over_ranks([total_ms], "max")
+    if gq.gqa_device_status() != 0:
+        raise RuntimeError("device error in the timed region")
+
+    # ---- dominant kernel alone (split kernel / paged kernel), same workload
+    _, kern_ms = step_events(args.steps, hook=True)
+    kern_avg = statistics.mean(kern_ms)
+
+    # ---- end to end through the host-buffer entry point (dense path)
+    e2e = None
+    if not args.no_e2e and isinstance(cfg, gqa_inputs.DenseConfig):
+        qh = tensors["q"].cpu().pin_memory()
+        kh = tensors["k"].cpu().pin_memory()
+        vh = tensors["v"].cpu().pin_memory()
+        oh = torch.empty_like(qh).pin_memory()
+        lh = torch.empty(tuple(tensors["lse"].shape), dtype=torch.float32).pin_memory()
+        gq.gqa_decode_host(qh, kh, vh, oh, lh)  # warm-up
+        ts = []
+        for _ in range(max(1, args.e2e_steps)):
+            t0 = time.perf_counter()
+            gq.gqa_decode_host(qh, kh, vh, oh, lh)
+            ts.append((time.perf_counter() - t0) * 1e3)
+        (e2e_ms,) = reduce_over_ranks([statistics.mean(ts)], "max")
+        e2e = {"value": gbs(world * nbytes, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2,
+               "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+               "api": "gqa_decode_host (pinned host buffers, copies inside the timed call)"}
+        del qh, kh, vh, oh, lh
+
+    cpu_base = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        cpu_base = _cpu_baseline(cfg, tensors)
+
+    if rank == 0:
+        us = [t * 1e3 for t in step_ms]
+        value = gbs(world * args.steps * nbytes, max_total_ms)
+        achieved = gbs(nbytes, kern_avg)
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(max_total_ms / args.steps, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16" if isinstance(cfg, gqa_inputs.DenseConfig) else "fp8_e4m3fn kv, bf16 q/out, f16 mma",
+            "data": "synthetic (seeded N(0,1), generated on the device)",
+            "config": dict(workload_config(cfg), l2=f"flushed: {flush.numel() >> 20} MiB memset before every step",
+                           splits=splits, parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "us_per_call": {"median": round(statistics.median(us), 2), "p10": round(percentile(us, 10), 2),
+                            "p90": round(percentile(us, 90), 2)},
+            "kv_bytes_per_call": nbytes,
+            "frac_of_peak": round(value / world / peak, 4),
+            "peak_gbs": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback",
+            "copy_peak_gbs_this_run": round(copy_peak, 1),
+            "frac_of_copy_peak_this_run": round(value / world / copy_peak, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": recorded_traffic(cfg.name),
+                         "kernel": "gqa_dense_split_kernel" if isinstance(cfg, gqa_inputs.DenseConfig)
+                         else "gqa_paged_fp8_kernel",
+                         "kernel_us": round(kern_avg * 1e3, 2),
+                         "algorithmic_bytes_per_launch": nbytes},
+            "cpu_baseline": cpu_base,
+            "e2e": e2e,
+            "gpu_launches": args.steps * launches_per_call,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args) -> int:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    import oracle
+    orc = oracle.load()
+    cfg = gqa_inputs.CONFIGS[args.config]
+    nbytes = workload_kv_bytes(cfg)
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        q, k, v = gqa_inputs.dense_config_inputs(cfg, device="cpu")
+        nrows = cfg.B * cfg.Hq * cfg.Sq
+        t0 = time.perf_counter()
+        orc.gqa_decode(q, k, v, cfg.scale, rows=list(range(min(8, nrows))))
+        per_row = (time.perf_counter() - t0) / min(8, nrows)
+        budget_s = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+        rows = None if per_row * nrows <= budget_s else list(range(max(1, int(budget_s / per_row))))
+
+        def step():
+            orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
+    else:
+        inp = gqa_inputs.paged_config_inputs(cfg, device="cpu")
+        nrows = cfg.B * cfg.Hq
+        t0 = time.perf_counter()
+        orc.gqa_decode_paged_fp8(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["page_table"],
+                                 inp["topk"], inp["k_scale"], inp["v_scale"], cfg.scale, rows=list(range(64)))
+        per_row = (time.perf_counter() - t0) / 64
+        budget_s = 150.0 / max(1, args.steps + args.warmup)
+        rows = None if per_row * nrows <= budget_s else list(range(max(1, int(budget_s / per_row))))
+
+        def step():
+            orc.gqa_decode_paged_fp8(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"], inp["page_table"],
+                                     inp["topk"], inp["k_scale"], inp["v_scale"], cfg.scale, rows=rows)
+    frac = 1.0 if rows is None else len(rows) / nrows
+    for _ in range(args.warmup):
+        step()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        ts.append((time.perf_counter() - t0) * 1e3)
+    total = sum(ts)
+    value = gbs(args.steps * nbytes * frac, total)
+    sample = f"{'all' if rows is None else len(rows)} of {nrows} rows of the workload per step"
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), CPU)",
+        "config": workload_config(cfg), "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None) -> int:
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gqa", "reference"], default="gqa")
+    p.add_argument("--config", default=gqa_inputs.HEADLINE, choices=sorted(gqa_inputs.CONFIGS))
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gqa(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,267 @@
+"""GB300-native grouped-query decode attention: Python binding.
+
+A thin ctypes layer over ``libgqa_decode.so`` (the C ABI declared in
+``include/gqa_decode.h``).  Functions carry the C entry points' names and
+only marshal arguments: torch tensors supply device memory and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+There is no fallback: if the library is missing, importing a function that
+needs it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa_decode.so")
+
+STATUS = {
+    0: "GQA_OK",
+    1: "GQA_ERR_INVALID_ARG",
+    2: "GQA_ERR_UNSUPPORTED",
+    3: "GQA_ERR_ALIGNMENT",
+    4: "GQA_ERR_NO_MEMORY",
+    5: "GQA_ERR_CUDA",
+    6: "GQA_ERR_DEVICE_TIMEOUT",
+    7: "GQA_ERR_DEVICE_INDEX",
+}
+GQA_OK = 0
+
+# Every symbol the headers in include/ declare.
+EXPORTS = [
+    "gqa_status_string", "gqa_version", "gqa_decode", "gqa_decode_num_splits",
+    "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_host", "gqa_decode_paged_fp8",
+    "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
+    "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events",
+]
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {STATUS.get(int(status), status)}")
+
+
+_lib_handle = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libgqa_decode.so (built by ``gqa_decode_attention_gb300.build``)."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m gqa_decode_attention_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i, f, st, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+    lib.gqa_status_string.restype = ctypes.c_char_p
+    lib.gqa_status_string.argtypes = [st]
+    lib.gqa_version.restype = ctypes.c_char_p
+    lib.gqa_version.argtypes = []
+    lib.gqa_decode.restype = st
+    lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.gqa_decode_num_splits.restype = i
+    lib.gqa_decode_num_splits.argtypes = [i] * 6
+    lib.gqa_decode_workspace_bytes.restype = sz
+    lib.gqa_decode_workspace_bytes.argtypes = [i] * 7
+    lib.gqa_decode_ex.restype = st
+    lib.gqa_decode_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.gqa_decode_host.restype = st
+    lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.gqa_decode_paged_fp8.restype = st
+    lib.gqa_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f, f, vp, vp] + [i] * 8 + [f, vp]
+    lib.gqa_paged_gather_fp8.restype = st
+    lib.gqa_paged_gather_fp8.argtypes = [vp, vp, vp, vp] + [i] * 7 + [vp]
+    lib.gqa_fp8_e4m3fn_to_f32.restype = st
+    lib.gqa_fp8_e4m3fn_to_f32.argtypes = [vp, vp, i, vp]
+    lib.gqa_device_status.restype = st
+    lib.gqa_device_status.argtypes = [vp]
+    lib.gqa_set_wait_limit_ns.restype = None
+    lib.gqa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.gqa_debug_set_fault_mode.restype = None
+    lib.gqa_debug_set_fault_mode.argtypes = [i]
+    lib.gqa_debug_set_kernel_events.restype = None
+    lib.gqa_debug_set_kernel_events.argtypes = [vp, vp]
+    _lib_handle = lib
+    return lib
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != GQA_OK:
+        raise GQAError(status, where)
+
+
+def _need(t: torch.Tensor, name: str, dtype, device_type: str):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if t.device.type != device_type:
+        raise ValueError(f"{name}: expected a {device_type} tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _scale_arg(scale):
+    return 0.0 if scale is None else float(scale)
+
+
+# ---------------------------------------------------------------------------
+# dense
+# ---------------------------------------------------------------------------
+def gqa_decode(q, k, v, out=None, lse=None, scale=None, stream=None, with_lse=True):
+    """Dense GQA decode.  q [B,Sq,Hq,D], k/v [B,Skv,Hkv,D] bf16 on CUDA.
+
+    Returns (out [B,Sq,Hq,D] bf16, lse [B,Hq,Sq] fp32 or None).
+    """
+    return gqa_decode_ex(q, k, v, out=out, lse=lse, scale=scale, num_splits=0, workspace=None,
+                         stream=stream, with_lse=with_lse)
+
+
+def gqa_decode_ex(q, k, v, out=None, lse=None, scale=None, num_splits=0, workspace=None, stream=None,
+                  with_lse=True):
+    """gqa_decode with an explicit split count (0 = automatic) and an optional
+    caller workspace (a CUDA uint8 tensor of at least gqa_decode_workspace_bytes)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, "cuda")
+    B, Sq, Hq, D = q.shape
+    _, Skv, Hkv, _ = k.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = lib.gqa_decode_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Skv, Hq, Hkv, D,
+                           _scale_arg(scale), int(num_splits), ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "gqa_decode_ex")
+    return out, lse
+
+
+def gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D) -> int:
+    n = load_library().gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D)
+    if n < 0:
+        raise GQAError(-n, "gqa_decode_num_splits")
+    return n
+
+
+def gqa_decode_workspace_bytes(B, Sq, Skv, Hq, Hkv, D, num_splits=0) -> int:
+    return int(load_library().gqa_decode_workspace_bytes(B, Sq, Skv, Hq, Hkv, D, int(num_splits)))
+
+
+def gqa_decode_host(q, k, v, out, lse=None, scale=None, stream=None):
+    """End-to-end form on HOST (ideally pinned) tensors; returns when done."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, "cpu")
+    B, Sq, Hq, D = q.shape
+    _, Skv, Hkv, _ = k.shape
+    st = lib.gqa_decode_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Skv, Hq, Hkv, D,
+                             _scale_arg(scale), _stream(stream))
+    _check(st, "gqa_decode_host")
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# sparse paged FP8
+# ---------------------------------------------------------------------------
+def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale, v_scale, out=None,
+                         lse=None, scale=None, stream=None, with_lse=True):
+    """Sparse paged decode over an FP8 E4M3FN pool with a sigmoid gate.
+
+    q, gate [B,Hq,D] bf16; pools uint8 [num_pages, page_size, Hkv, D];
+    page_table int32 [B, pages_per_req]; topk_idx int32 [B, topk].
+    Returns (out [B,Hq,D] bf16, lse [B,Hq] fp32 or None).
+    """
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, "cuda")
+    _need(gate, "gate", torch.bfloat16, "cuda")
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, n, torch.uint8, "cuda")
+    _need(page_table, "page_table", torch.int32, "cuda")
+    _need(topk_idx, "topk_idx", torch.int32, "cuda")
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib.gqa_decode_paged_fp8(_ptr(q), _ptr(gate), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                                  _ptr(topk_idx), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
+                                  B, Hq, Hkv, D, page_size, page_table.shape[1], num_pages,
+                                  topk_idx.shape[1], _scale_arg(scale), _stream(stream))
+    _check(st, "gqa_decode_paged_fp8")
+    return out, lse
+
+
+def gqa_paged_gather_fp8(pool, page_table, topk_idx, out=None, stream=None):
+    """Test hook: the paged kernel's index map as a byte copy -> uint8 [B, topk, Hkv, D]."""
+    lib = load_library()
+    _need(pool, "pool", torch.uint8, "cuda")
+    _need(page_table, "page_table", torch.int32, "cuda")
+    _need(topk_idx, "topk_idx", torch.int32, "cuda")
+    num_pages, page_size, Hkv, D = pool.shape
+    B, topk = topk_idx.shape
+    if out is None:
+        out = torch.empty((B, topk, Hkv, D), dtype=torch.uint8, device=pool.device)
+    st = lib.gqa_paged_gather_fp8(_ptr(pool), _ptr(page_table), _ptr(topk_idx), _ptr(out), B, Hkv, D,
+                                  page_size, page_table.shape[1], num_pages, topk, _stream(stream))
+    _check(st, "gqa_paged_gather_fp8")
+    return out
+
+
+def gqa_fp8_e4m3fn_to_f32(codes, out=None, stream=None):
+    """Test hook: the paged kernel's E4M3FN widening, as fp32."""
+    lib = load_library()
+    _need(codes, "codes", torch.uint8, "cuda")
+    if out is None:
+        out = torch.empty(codes.shape, dtype=torch.float32, device=codes.device)
+    st = lib.gqa_fp8_e4m3fn_to_f32(_ptr(codes), _ptr(out), codes.numel(), _stream(stream))
+    _check(st, "gqa_fp8_e4m3fn_to_f32")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# status and controls
+# ---------------------------------------------------------------------------
+def gqa_device_status(stream=None) -> int:
+    """Waits for the stream; returns and clears the device error status code."""
+    return int(load_library().gqa_device_status(_stream(stream)))
+
+
+def gqa_set_wait_limit_ns(ns: int):
+    load_library().gqa_set_wait_limit_ns(int(ns))
+
+
+def gqa_debug_set_fault_mode(mode: int):
+    load_library().gqa_debug_set_fault_mode(int(mode))
+
+
+def gqa_debug_set_kernel_events(before=None, after=None):
+    """Measurement hook: torch.cuda.Event pair recorded around the main kernel
+    of later calls (None, None stops it)."""
+    lib = load_library()
+    if before is None or after is None:
+        lib.gqa_debug_set_kernel_events(None, None)
+    else:
+        lib.gqa_debug_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def gqa_status_string(status: int) -> str:
+    return load_library().gqa_status_string(int(status)).decode()
+
+
+def gqa_version() -> str:
+    return load_library().gqa_version().decode()

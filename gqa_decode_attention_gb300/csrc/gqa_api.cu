@@ -1,0 +1,538 @@
+// gqa_api.cu -- the C ABI front end of libgqa_decode.so.
+//
+// Validation, the split-count heuristic, workspace handling, TMA descriptor
+// encoding and kernel dispatch.  No entry point synchronises except
+// gqa_device_status and gqa_decode_host.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gqa_decode.h"
+#include "../../include/gqa_decode_debug.h"
+#include "gqa_launch.h"
+
+namespace gqa {
+
+__device__ unsigned g_error_word = 0;
+
+namespace {
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int> g_fault_mode{0};
+std::atomic<cudaEvent_t> g_ev_before{nullptr};
+std::atomic<cudaEvent_t> g_ev_after{nullptr};
+
+constexpr int kMaxDevices = 64;
+constexpr int kMinBlocksPerSplit = 2;
+constexpr long kCtasPerSmTarget = 4;
+constexpr int kMaxSplits = 4096;
+constexpr long kMaxGroupRows = 4096;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// ------------------------------------------------------------ device facts
+std::mutex g_mu;
+int g_sm_count[kMaxDevices];
+int g_occ[kMaxDevices][3][kDenseCfgs];
+
+bool current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) return false;
+    return *dev >= 0 && *dev < kMaxDevices;
+}
+
+int sm_count(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+
+unsigned *g_err_ptr[kMaxDevices];
+
+// Device address of the error word on `dev` (the current device).
+unsigned *error_word(int dev) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_err_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_err_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    return g_err_ptr[dev];
+}
+
+// Library-owned stream-ordered memory pool per device.  It keeps freed blocks
+// (release threshold = max) so the per-call workspace allocation is a cheap
+// pool hit after the first call, without touching the device's default pool.
+cudaMemPool_t g_pool[kMaxDevices];
+
+cudaError_t pool_alloc(void **p, size_t bytes, int dev, cudaStream_t stream) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_pool[dev] == nullptr) {
+            cudaMemPoolProps props;
+            std::memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t pool;
+            cudaError_t e = cudaMemPoolCreate(&pool, &props);
+            if (e != cudaSuccess) return e;
+            uint64_t keep = ~uint64_t(0);
+            cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            g_pool[dev] = pool;
+        }
+    }
+    return cudaMallocFromPoolAsync(p, bytes, g_pool[dev], stream);
+}
+
+int dense_occupancy(int dev, int D, int cfg) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int &slot = g_occ[dev][d_index(D)][cfg];
+    if (slot == 0) {
+        slot = D == 64 ? dense_ctas_per_sm_d64(cfg) : D == 128 ? dense_ctas_per_sm_d128(cfg) : dense_ctas_per_sm_d256(cfg);
+    }
+    return slot;
+}
+
+// ------------------------------------------------------------ TMA encoding
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// ------------------------------------------------------------ dense shapes
+struct DenseShape {
+    int B, Sq, Skv, Hq, Hkv, D, G, Mq, cfg, qrows, row_groups, n_blocks;  // blocks of kSplitKeys keys
+};
+
+gqa_status check_dense(int B, int Sq, int Skv, int Hq, int Hkv, int D, DenseShape *s) {
+    if (B < 1 || Sq < 1 || Skv < 1 || Hq < 1 || Hkv < 1) return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || Sq > Skv) return GQA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return GQA_ERR_UNSUPPORTED;
+    const long G = Hq / Hkv;
+    const long Mq = G * Sq;
+    if (Mq > kMaxGroupRows) return GQA_ERR_UNSUPPORTED;
+    if (long(Skv) * Hkv >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
+    if (B > 65535) return GQA_ERR_UNSUPPORTED;
+    s->B = B;
+    s->Sq = Sq;
+    s->Skv = Skv;
+    s->Hq = Hq;
+    s->Hkv = Hkv;
+    s->D = D;
+    s->G = int(G);
+    s->Mq = int(Mq);
+    s->cfg = dense_cfg_for_rows(int(Mq < 128 ? Mq : 128));
+    s->qrows = dense_cfg_rows(s->cfg);
+    s->row_groups = int((Mq + s->qrows - 1) / s->qrows);
+    if (long(Hkv) * s->row_groups > 65535) return GQA_ERR_UNSUPPORTED;
+    s->n_blocks = (Skv + kSplitKeys - 1) / kSplitKeys;
+    return GQA_OK;
+}
+
+// Split count.  The kernel is HBM-bound once about kCtasPerSmTarget CTAs are
+// resident on every SM (enough loads in flight), so:
+//  - units (batch x KV head x row group) already giving that many CTAs: 1 split;
+//  - otherwise the fewest splits that reach the target while the whole grid
+//    stays one wave of resident CTAs;
+//  - when occupancy is too low for that (large CTAs), the split count that
+//    minimises waves x key blocks per CTA, i.e. balanced waves.
+// Every split covers at least kMinBlocksPerSplit blocks of 64 keys, at most
+// kMaxSplits splits are used, and the count is then evened out so that all
+// splits but the last cover the same number of blocks.
+int choose_splits(const DenseShape &s, int requested, int dev) {
+    int S;
+    if (requested > 0) {
+        S = requested;
+    } else {
+        const long units = long(s.B) * s.Hkv * s.row_groups;
+        const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
+        const long occ = dense_occupancy(dev, s.D, s.cfg) > 0 ? dense_occupancy(dev, s.D, s.cfg) : 1;
+        const long slots = nsm * occ;
+        const long target = nsm * (occ < kCtasPerSmTarget ? occ : kCtasPerSmTarget);
+        const long max_s = (s.n_blocks + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
+        if (units >= target) {
+            S = 1;
+        } else {
+            const long s_min = (target + units - 1) / units;
+            const long s_one_wave = slots / units;
+            if (s_min <= s_one_wave) {
+                S = int(s_min);
+            } else {
+                long best = 1, best_cost = -1;
+                for (long c = 1; c <= 4 * s_one_wave + 4 && c <= max_s; ++c) {
+                    const long waves = (units * c + slots - 1) / slots;
+                    const long cost = waves * ((s.n_blocks + c - 1) / c);
+                    if (best_cost < 0 || cost < best_cost) {
+                        best_cost = cost;
+                        best = c;
+                    }
+                }
+                S = int(best);
+            }
+        }
+        if (S > max_s) S = int(max_s);
+    }
+    if (S > s.n_blocks) S = s.n_blocks;
+    if (S > kMaxSplits) S = kMaxSplits;
+    return S < 1 ? 1 : S;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t workspace_bytes(const DenseShape &s, int splits) {
+    if (splits <= 1) return 0;
+    const size_t rows = size_t(s.B) * s.Hkv * splits * s.Mq;
+    return align256(rows * s.D * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+// key blocks per split as the kernel sees it for a split count
+int blocks_per_split(const DenseShape &s, int splits) { return (s.n_blocks + splits - 1) / splits; }
+
+gqa_status run_dense(const void *q, const void *k, const void *v, void *out, float *lse, const DenseShape &s,
+                     float scale, int requested_splits, void *workspace, size_t workspace_size,
+                     cudaStream_t stream) {
+    int dev = 0;
+    if (!current_device(&dev)) return GQA_ERR_CUDA;
+    if (encode_fn() == nullptr) return GQA_ERR_CUDA;
+    int splits = choose_splits(s, requested_splits, dev);
+    // Equalise: the split count actually realised by blocks_per_split.
+    const int tps = blocks_per_split(s, splits);
+    splits = (s.n_blocks + tps - 1) / tps;
+    const size_t need = workspace_bytes(s, splits);
+    void *ws = workspace;
+    bool owned = false;
+    if (need > 0) {
+        if (ws != nullptr) {
+            if (workspace_size < need) return GQA_ERR_NO_MEMORY;
+            if (!aligned(ws, 256)) return GQA_ERR_ALIGNMENT;
+        } else {
+            if (pool_alloc(&ws, need, dev, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return GQA_ERR_NO_MEMORY;
+            }
+            owned = true;
+        }
+    }
+    DenseLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    DenseArgs &a = L.args;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    if (need > 0) {
+        const size_t rows = size_t(s.B) * s.Hkv * splits * s.Mq;
+        a.o_part = static_cast<float *>(ws);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + align256(rows * s.D * sizeof(float)));
+    }
+    a.B = s.B;
+    a.Sq = s.Sq;
+    a.Skv = s.Skv;
+    a.Hq = s.Hq;
+    a.Hkv = s.Hkv;
+    a.G = s.G;
+    a.Mq = s.Mq;
+    a.n_blocks = s.n_blocks;
+    a.blocks_per_split = tps;
+    a.num_splits = splits;
+    a.row_groups = s.row_groups;
+    a.alpha = scale * 1.4426950408889634f;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.fault_mode = g_fault_mode.load();
+    a.err = error_word(dev);
+    L.k = k;
+    L.v = v;
+    L.D = s.D;
+    L.cfg = s.cfg;
+    L.stream = stream;
+    L.ev_before = g_ev_before.load();
+    L.ev_after = g_ev_after.load();
+    cudaError_t e = s.D == 64 ? launch_dense_d64(L) : s.D == 128 ? launch_dense_d128(L) : launch_dense_d256(L);
+    if (owned) cudaFreeAsync(ws, stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+
+float resolve_scale(float scale, int D) {
+    if (!(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt(float(D));
+    return scale;
+}
+
+gqa_status check_dense_ptrs(const void *q, const void *k, const void *v, const void *out, const float *lse) {
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return GQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+        return GQA_ERR_ALIGNMENT;
+    return GQA_OK;
+}
+
+// ------------------------------------------------------------ paged checks
+gqa_status check_paged(int B, int Hq, int Hkv, int D, int page_size, int pages_per_req, int num_pages, int topk) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || pages_per_req < 1 || num_pages < 1 || topk < 0)
+        return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+    if (long(topk) > long(pages_per_req) * page_size) return GQA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return GQA_ERR_UNSUPPORTED;
+    if (long(pages_per_req) * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
+    if (long(num_pages) * page_size >= (1L << 31)) return GQA_ERR_UNSUPPORTED;
+    if (topk > 65536 || B > 65535) return GQA_ERR_UNSUPPORTED;
+    return GQA_OK;
+}
+
+}  // namespace
+
+// K or V as a 4-D tensor (d, kv head, key, batch) with a box of 64 head-dim
+// elements (128 bytes, one swizzle atom) x 1 head x box_keys keys x 1 batch.
+// Keys past Skv read as zeros.
+bool make_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Skv, int Hkv, int D, int box_keys) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(Skv), cuuint64_t(B)};
+    const cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Hkv) * D * 2, cuuint64_t(Skv) * Hkv * D * 2};
+    const cuuint32_t box[4] = {64, 1, cuuint32_t(box_keys), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+const char *gqa_status_string(gqa_status s) {
+    switch (s) {
+        case GQA_OK: return "GQA_OK";
+        case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG";
+        case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
+        case GQA_ERR_ALIGNMENT: return "GQA_ERR_ALIGNMENT";
+        case GQA_ERR_NO_MEMORY: return "GQA_ERR_NO_MEMORY";
+        case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+        case GQA_ERR_DEVICE_TIMEOUT: return "GQA_ERR_DEVICE_TIMEOUT";
+        case GQA_ERR_DEVICE_INDEX: return "GQA_ERR_DEVICE_INDEX";
+    }
+    return "GQA_ERR_UNKNOWN";
+}
+
+const char *gqa_version(void) { return "gqa_decode 0.1.0 (sm_103a)"; }
+
+gqa_status gqa_decode_ex(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Sq, int Skv,
+                         int Hq, int Hkv, int D, float scale, int num_splits, void *workspace,
+                         size_t workspace_bytes_, gqa_stream_t stream) {
+    DenseShape s;
+    gqa_status st = check_dense(B, Sq, Skv, Hq, Hkv, D, &s);
+    if (st != GQA_OK) return st;
+    if (num_splits < 0) return GQA_ERR_INVALID_ARG;
+    st = check_dense_ptrs(q, k, v, out, lse);
+    if (st != GQA_OK) return st;
+    return run_dense(q, k, v, out, lse, s, resolve_scale(scale, D), num_splits, workspace, workspace_bytes_,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+gqa_status gqa_decode(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Sq, int Skv,
+                      int Hq, int Hkv, int D, float scale, gqa_stream_t stream) {
+    return gqa_decode_ex(q, k, v, out, lse, B, Sq, Skv, Hq, Hkv, D, scale, 0, nullptr, 0, stream);
+}
+
+int gqa_decode_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int D) {
+    DenseShape s;
+    gqa_status st = check_dense(B, Sq, Skv, Hq, Hkv, D, &s);
+    if (st != GQA_OK) return -int(st);
+    int dev = 0;
+    if (!current_device(&dev)) return -int(GQA_ERR_CUDA);
+    const int splits = choose_splits(s, 0, dev);
+    const int tps = blocks_per_split(s, splits);
+    return (s.n_blocks + tps - 1) / tps;
+}
+
+size_t gqa_decode_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int D, int num_splits) {
+    DenseShape s;
+    if (check_dense(B, Sq, Skv, Hq, Hkv, D, &s) != GQA_OK || num_splits < 0) return 0;
+    int dev = 0;
+    if (num_splits == 0 && !current_device(&dev)) return 0;
+    const int splits = choose_splits(s, num_splits, dev);
+    const int tps = blocks_per_split(s, splits);
+    return workspace_bytes(s, (s.n_blocks + tps - 1) / tps);
+}
+
+gqa_status gqa_decode_host(const void *q_host, const void *k_host, const void *v_host, void *out_host,
+                           float *lse_host, int B, int Sq, int Skv, int Hq, int Hkv, int D, float scale,
+                           gqa_stream_t stream_) {
+    DenseShape s;
+    gqa_status st = check_dense(B, Sq, Skv, Hq, Hkv, D, &s);
+    if (st != GQA_OK) return st;
+    if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr)
+        return GQA_ERR_INVALID_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const size_t qb = size_t(B) * Sq * Hq * D * 2;
+    const size_t kvb = size_t(B) * Skv * Hkv * D * 2;
+    const size_t lb = size_t(B) * Hq * Sq * sizeof(float);
+    const size_t total = align256(qb) + 2 * align256(kvb) + align256(qb) + align256(lb);
+    char *base = nullptr;
+    int dev = 0;
+    if (!current_device(&dev)) return GQA_ERR_CUDA;
+    if (pool_alloc(reinterpret_cast<void **>(&base), total, dev, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_NO_MEMORY;
+    }
+    char *dq = base;
+    char *dk = dq + align256(qb);
+    char *dv = dk + align256(kvb);
+    char *dout = dv + align256(kvb);
+    float *dlse = reinterpret_cast<float *>(dout + align256(qb));
+    gqa_status result = GQA_OK;
+    if (cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dk, k_host, kvb, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(dv, v_host, kvb, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+        result = GQA_ERR_CUDA;
+    }
+    if (result == GQA_OK)
+        result = run_dense(dq, dk, dv, dout, lse_host ? dlse : nullptr, s, resolve_scale(scale, D), 0, nullptr, 0,
+                           stream);
+    if (result == GQA_OK) {
+        if (cudaMemcpyAsync(out_host, dout, qb, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+            (lse_host && cudaMemcpyAsync(lse_host, dlse, lb, cudaMemcpyDeviceToHost, stream) != cudaSuccess))
+            result = GQA_ERR_CUDA;
+    }
+    cudaFreeAsync(base, stream);
+    if (cudaStreamSynchronize(stream) != cudaSuccess && result == GQA_OK) result = GQA_ERR_CUDA;
+    if (result == GQA_ERR_CUDA) cudaGetLastError();
+    return result;
+}
+
+gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *k_pool, const uint8_t *v_pool,
+                                const int32_t *page_table, const int32_t *topk_idx, float k_scale, float v_scale,
+                                void *out, float *lse, int B, int Hq, int Hkv, int D, int page_size,
+                                int pages_per_req, int num_pages, int topk, float scale, gqa_stream_t stream) {
+    gqa_status st = check_paged(B, Hq, Hkv, D, page_size, pages_per_req, num_pages, topk);
+    if (st != GQA_OK) return st;
+    if (D == 256 || Hq / Hkv > 16) return GQA_ERR_UNSUPPORTED;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return GQA_ERR_INVALID_ARG;
+    if (q == nullptr || gate == nullptr || k_pool == nullptr || v_pool == nullptr || out == nullptr ||
+        page_table == nullptr || (topk > 0 && topk_idx == nullptr))
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(gate, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(out, 16) || !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(topk_idx, 4))
+        return GQA_ERR_ALIGNMENT;
+    PagedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.gate = static_cast<const __nv_bfloat16 *>(gate);
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.page_table = page_table;
+    a.topk = topk_idx;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = Hq / Hkv;
+    a.page_size = page_size;
+    a.pages_per_req = pages_per_req;
+    a.num_pages = num_pages;
+    a.topk_n = topk;
+    a.alpha = resolve_scale(scale, D) * k_scale * 1.4426950408889634f;
+    a.v_scale = v_scale;
+    int dev = 0;
+    if (!current_device(&dev)) return GQA_ERR_CUDA;
+    a.err = error_word(dev);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
+    if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
+    cudaError_t pe = launch_paged_fp8(a, D, cs);
+    if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
+    if (pe != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+
+gqa_status gqa_paged_gather_fp8(const uint8_t *pool, const int32_t *page_table, const int32_t *topk_idx, uint8_t *out,
+                                int B, int Hkv, int D, int page_size, int pages_per_req, int num_pages, int topk,
+                                gqa_stream_t stream) {
+    gqa_status st = check_paged(B, Hkv, Hkv, D, page_size, pages_per_req, num_pages, topk);
+    if (st != GQA_OK) return st;
+    if (pool == nullptr || page_table == nullptr || out == nullptr || (topk > 0 && topk_idx == nullptr))
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned(pool, 16) || !aligned(out, 16) || !aligned(page_table, 4) || !aligned(topk_idx, 4))
+        return GQA_ERR_ALIGNMENT;
+    if (topk == 0) return GQA_OK;
+    int dev = 0;
+    if (!current_device(&dev)) return GQA_ERR_CUDA;
+    if (launch_paged_gather(pool, page_table, topk_idx, out, B, Hkv, D, page_size, pages_per_req, num_pages, topk,
+                            error_word(dev), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+
+gqa_status gqa_fp8_e4m3fn_to_f32(const uint8_t *codes, float *out, int n, gqa_stream_t stream) {
+    if (n < 0 || (n > 0 && (codes == nullptr || out == nullptr))) return GQA_ERR_INVALID_ARG;
+    if (!aligned(out, 4)) return GQA_ERR_ALIGNMENT;
+    if (n == 0) return GQA_OK;
+    if (launch_fp8_to_f32(codes, out, n, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+
+gqa_status gqa_device_status(gqa_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    unsigned word = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    if (word & kErrTimeout) return GQA_ERR_DEVICE_TIMEOUT;
+    if (word & kErrIndex) return GQA_ERR_DEVICE_INDEX;
+    return GQA_OK;
+}
+
+void gqa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns); }
+
+void gqa_debug_set_fault_mode(int mode) { g_fault_mode.store(mode); }
+
+void gqa_debug_set_kernel_events(void *before, void *after) {
+    g_ev_before.store(static_cast<cudaEvent_t>(before));
+    g_ev_after.store(static_cast<cudaEvent_t>(after));
+}
+
+}  // extern "C"

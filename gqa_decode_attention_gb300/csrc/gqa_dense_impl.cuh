@@ -1,0 +1,95 @@
+// gqa_dense_impl.cuh -- launch code of the dense split and combine kernels for
+// one head dimension; included once per head dimension (GQA_HEAD_DIM).
+#pragma once
+
+#include "gqa_dense_kernel.cuh"
+#include "gqa_launch.h"
+
+namespace gqa {
+
+template <int D, int CFG>
+struct DenseInst {
+    static constexpr int RB = 1 << CFG;
+    static constexpr int T = dense_tile_keys(D, CFG);
+    static constexpr int S = dense_stages(D, CFG);
+    using C = DenseCfg<D, RB, T, S>;
+    static constexpr auto kernel() { return gqa_dense_split_kernel<D, RB, T, S>; }
+};
+
+template <int D, int CFG>
+static cudaError_t launch_split_cfg(const DenseLaunch &L) {
+    using I = DenseInst<D, CFG>;
+    using C = typename I::C;
+    auto kern = I::kernel();
+    static bool attr_set = false;  // per process; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap tk, tv;
+    if (!make_kv_tensor_map(&tk, L.k, L.args.B, L.args.Skv, L.args.Hkv, D, I::T) ||
+        !make_kv_tensor_map(&tv, L.v, L.args.B, L.args.Skv, L.args.Hkv, D, I::T))
+        return cudaErrorInvalidValue;
+    const dim3 grid(L.args.Hkv * L.args.row_groups, L.args.num_splits, L.args.B);
+    const bool timed = L.ev_before != nullptr && L.ev_after != nullptr;
+    if (timed) cudaEventRecord(L.ev_before, L.stream);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(tk, tv, L.args);
+    if (timed) cudaEventRecord(L.ev_after, L.stream);
+    return cudaGetLastError();
+}
+
+template <int D, int CFG>
+static int occupancy_cfg() {
+    using I = DenseInst<D, CFG>;
+    using C = typename I::C;
+    auto kern = I::kernel();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM_BYTES) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int D>
+static cudaError_t launch_combine(const DenseLaunch &L) {
+    const DenseArgs &a = L.args;
+    const long rows = long(a.B) * a.Hkv * a.Mq;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(rows));
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = (size_t((a.num_splits + 3) & ~3) + size_t(kCombineThreads) * 4) * sizeof(float);
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, (const float *)a.o_part, (const float *)a.lse_part,
+                              a.out, a.lse, a.Sq, a.Hq, a.Hkv, a.G, a.Mq, a.num_splits);
+}
+
+template <int D>
+static cudaError_t launch_dense(const DenseLaunch &L) {
+    cudaError_t e;
+    switch (L.cfg) {
+        case 0: e = launch_split_cfg<D, 0>(L); break;
+        case 1: e = launch_split_cfg<D, 1>(L); break;
+        case 2: e = launch_split_cfg<D, 2>(L); break;
+        default: e = launch_split_cfg<D, 3>(L); break;
+    }
+    if (e != cudaSuccess || L.args.num_splits == 1) return e;
+    return launch_combine<D>(L);
+}
+
+template <int D>
+static int dense_occupancy(int cfg) {
+    switch (cfg) {
+        case 0: return occupancy_cfg<D, 0>();
+        case 1: return occupancy_cfg<D, 1>();
+        case 2: return occupancy_cfg<D, 2>();
+        default: return occupancy_cfg<D, 3>();
+    }
+}
+
+}  // namespace gqa

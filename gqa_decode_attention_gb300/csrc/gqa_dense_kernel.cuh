@@ -1,0 +1,420 @@
+// gqa_dense_kernel.cuh -- split-KV grouped-query decode attention (sm_103a).
+//
+// One CTA owns one (batch row b, KV head g, KV split s) and up to 128 query
+// rows of that KV head's group: rows r = i * G + hl (decode row i < Sq, local
+// head hl < G = Hq / Hkv, query head h = g * G + hl).  Query head h therefore
+// reads KV head g = h / (Hq / Hkv) in place ("When the K/V copy costs more than
+// the attention", section "What I was looking at"), and each K/V byte of the
+// split is fetched from HBM once for the whole group.
+//
+// Pipeline: warp 0 is the producer -- one lane issues TMA tile loads
+// (cp.async.bulk.tensor, 128-byte swizzle) of K and V into a ring of shared
+// memory stages guarded by full / empty mbarriers.  Each consumer warp owns a
+// block of 16 query rows and walks every key of the split in order, 16 keys
+// per step: S = Q K^T on the tensor cores (bf16 in, fp32 accumulate), the
+// bottom-right causal mask, the online softmax in base 2 with the scale folded
+// into one multiplier, and O += P V.  A row's arithmetic therefore depends
+// only on the split boundaries (multiples of 64 keys) and never on how many
+// rows share the CTA, which makes native GQA bit-identical to the same kernel
+// run on K/V expanded to every query head.  With one split the CTA writes
+// bf16 O and fp32 LSE; otherwise fp32 partials (O / l and log2-domain LSE) for
+// the combine kernel.
+//
+// Every mbarrier wait is bounded in wall time; on expiry the CTA flags the
+// device error word, waits (bounded) for its own loads still in flight, and
+// returns.
+#pragma once
+
+#include "gqa_common.cuh"
+#include "gqa_params.h"
+
+namespace gqa {
+
+// Keys per online-softmax step (one m16n8k16 k-group of keys).
+constexpr int kStepKeys = 16;
+
+// Shape of one kernel instance: RB consumer warps (16 rows each), TMA tiles of
+// T keys, STAGES ring slots.  Chosen per (head dim, row count) so small-group
+// CTAs are small and many fit on an SM.
+template <int D, int RB, int T, int STAGES_>
+struct DenseCfg {
+    static constexpr int NC = RB;
+    static constexpr int THREADS = 32 * (NC + 1);
+    static constexpr int STAGES = STAGES_;
+    static constexpr int CHUNKS = D / 64;  // 128-byte swizzle atoms per row
+    static constexpr int TILE_BYTES = T * D * 2;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int QROWS = RB * 16;
+    static constexpr int Q_BYTES = QROWS * D * 2;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = RING_BYTES + Q_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFF + 2 * STAGES * 8 + 16 + 1024;  // +1024 alignment slack
+    static constexpr int MIN_BLOCKS_RAW = (227 * 1024) / SMEM_BYTES;
+    static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : (MIN_BLOCKS_RAW > 8 ? 8 : MIN_BLOCKS_RAW);
+    static_assert(kSplitKeys % T == 0 && T % kStepKeys == 0, "tile must divide the split granule");
+};
+
+template <int D, int RB, int T, int STAGES_>
+__global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg<D, RB, T, STAGES_>::MIN_BLOCKS)
+    gqa_dense_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const DenseArgs a) {
+    using C = DenseCfg<D, RB, T, STAGES_>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ring = smem;
+    uint8_t *qs = smem + C::RING_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + C::STAGES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // Grid: x = (KV head, row group) fastest, so the CTAs of one split that
+    // stream neighbouring heads of the same keys start together; y = split.
+    const int g = blockIdx.x / a.row_groups;
+    const int rg = blockIdx.x % a.row_groups;
+    const int split = blockIdx.y;
+    const int b = blockIdx.z;
+    const int key_begin = split * a.blocks_per_split * kSplitKeys;
+    const int key_end = min(a.Skv, key_begin + a.blocks_per_split * kSplitKeys);
+    const int n_it = (key_end - key_begin + T - 1) / T;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::NC);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            int issued = 0;
+            bool ok = true;
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % C::STAGES;
+                const int round = it / C::STAGES;
+                if (round > 0 && !mbar_wait_bounded(&empty[st], (round - 1) & 1, a.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (a.fault_mode == 1 && it == 0) {
+                    issued = 1;
+                    continue;  // test hook: this stage never fills
+                }
+                uint8_t *ks = ring + st * C::STAGE_BYTES;
+                uint8_t *vs = ks + C::TILE_BYTES;
+                const int j0 = key_begin + it * T;
+                mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c) tma_load_4d(ks + c * T * 128, &tmK, &full[st], c * 64, g, j0, b);
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c) tma_load_4d(vs + c * T * 128, &tmV, &full[st], c * 64, g, j0, b);
+                issued = it + 1;
+            }
+            if (!ok) {
+                flag_error(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            // Never leave the CTA with a copy still landing in shared memory:
+            // wait for the last loads issued (those not yet released).
+            if (!ok || *abort_flag) {
+                for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+                    if (a.fault_mode == 1 && it == 0) continue;
+                    mbar_wait_bounded(&full[it % C::STAGES], (it / C::STAGES) & 1, a.wait_limit_ns, nullptr);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int rb = warp - 1;  // row block of this warp
+    const int cthreads = C::NC * 32;
+    const int ctid = threadIdx.x - 32;
+
+    // Stage this CTA's query rows into shared memory (128-byte swizzled,
+    // chunk-major like the K/V tiles).  Rows beyond Mq are zero.
+    for (int idx = ctid; idx < C::QROWS * (D / 8); idx += cthreads) {
+        const int lr = idx / (D / 8);
+        const int u = idx % (D / 8);
+        const int r = rg * C::QROWS + lr;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (r < a.Mq) {
+            const int i = r / a.G;
+            const int h = g * a.G + (r % a.G);
+            const __nv_bfloat16 *src = a.q + ((size_t(b) * a.Sq + i) * a.Hq + h) * D + u * 8;
+            val = *reinterpret_cast<const uint4 *>(src);
+        }
+        *reinterpret_cast<uint4 *>(qs + (u >> 3) * (C::QROWS * 128) + swz128(lr, u & 7)) = val;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(cthreads) : "memory");
+
+    // Rows held by this thread: local rows rb*16 + lane/4 and +8.
+    int kmax[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = rg * C::QROWS + rb * 16 + (lane >> 2) + 8 * hr;
+        const int i = r < a.Mq ? r / a.G : a.Sq - 1;
+        kmax[hr] = a.Skv - a.Sq + i;  // last visible key (bottom-right causal)
+    }
+    const int mask_from = a.Skv - a.Sq;  // steps ending at or below this key need no mask
+
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    float o[D / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+
+    const uint32_t q_base = smem_u32(qs);
+    const uint32_t ring_base = smem_u32(ring);
+    bool failed = false;
+
+    for (int it = 0; it < n_it; ++it) {
+        const int st = it % C::STAGES;
+        if (!mbar_wait_bounded(&full[st], (it / C::STAGES) & 1, a.wait_limit_ns, abort_flag)) {
+            failed = true;
+            break;
+        }
+        const uint32_t kb = ring_base + st * C::STAGE_BYTES;
+        const uint32_t vb = kb + C::TILE_BYTES;
+#pragma unroll 1
+        for (int sub = 0; sub < T / kStepKeys; ++sub) {
+            const int krow0 = sub * kStepKeys;  // first key row of this step in the tile
+            const int key0 = key_begin + it * T + krow0;
+            if (key0 >= a.Skv) break;  // past the cache: a fully masked step is a no-op
+
+            // ---- S = Q K^T for this warp's 16 rows x 16 keys
+            float s[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                uint32_t af[4];
+                {
+                    const int unit = kk * 2 + (lane >> 4);
+                    const uint32_t addr =
+                        q_base + (unit >> 3) * (C::QROWS * 128) + swz128(rb * 16 + (lane & 15), unit & 7);
+                    ldsm_x4(addr, af[0], af[1], af[2], af[3]);
+                }
+                const int unit = kk * 2 + ((lane >> 3) & 1);
+                const int krow = krow0 + (lane & 7) + 8 * (lane >> 4);
+                const uint32_t addr = kb + (unit >> 3) * (T * 128) + swz128(krow, unit & 7);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(addr, b0, b1, b2, b3);
+                mma_bf16_16816(s[0], af, b0, b1);
+                mma_bf16_16816(s[1], af, b2, b3);
+            }
+
+            // ---- scale into the log2 domain, mask, online softmax
+            const bool need_mask = (key0 + kStepKeys - 1) > mask_from;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float t = s[nt][e] * a.alpha;
+                    if (need_mask) {
+                        const int key = key0 + nt * 8 + (lane & 3) * 2 + (e & 1);
+                        if (key > kmax[e >> 1]) t = -INFINITY;
+                    }
+                    s[nt][e] = t;
+                }
+            float corr[2];
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                float mx = fmaxf(fmaxf(s[0][2 * hr], s[0][2 * hr + 1]), fmaxf(s[1][2 * hr], s[1][2 * hr + 1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m_run[hr], mx);
+                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                corr[hr] = fast_exp2(m_run[hr] - m_use);
+                m_run[hr] = m_new;
+                float psum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    s[nt][2 * hr] = fast_exp2(s[nt][2 * hr] - m_use);
+                    s[nt][2 * hr + 1] = fast_exp2(s[nt][2 * hr + 1] - m_use);
+                    psum += s[nt][2 * hr] + s[nt][2 * hr + 1];
+                }
+                l_run[hr] = l_run[hr] * corr[hr] + psum;
+            }
+            // P in bf16 as the A operand of the PV product:
+            // a0 (row, k 0-7), a1 (row+8, k 0-7), a2 (row, k 8-15), a3 (row+8, k 8-15)
+            const uint32_t pf[4] = {pack_bf16x2(s[0][0], s[0][1]), pack_bf16x2(s[0][2], s[0][3]),
+                                    pack_bf16x2(s[1][0], s[1][1]), pack_bf16x2(s[1][2], s[1][3])};
+            if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
+#pragma unroll
+                for (int nt = 0; nt < D / 8; ++nt) {
+                    o[nt][0] *= corr[0];
+                    o[nt][1] *= corr[0];
+                    o[nt][2] *= corr[1];
+                    o[nt][3] *= corr[1];
+                }
+            }
+
+            // ---- O += P V
+            const int vrow = krow0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int unit = dp * 2 + (lane >> 4);
+                const uint32_t addr = vb + (unit >> 3) * (T * 128) + swz128(vrow, unit & 7);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(addr, b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * dp], pf, b0, b1);
+                mma_bf16_16816(o[2 * dp + 1], pf, b2, b3);
+            }
+        }
+
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    if (failed) {
+        flag_error(a.err, kErrTimeout);
+        *abort_flag = 1;
+    }
+    pdl_launch_dependents();
+    if (failed || *abort_flag) return;
+
+    // ---- row sums across the 4 lanes that share a row
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
+        l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+    }
+
+    // ---- epilogue
+    const int unit = b * a.Hkv + g;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = rg * C::QROWS + rb * 16 + (lane >> 2) + 8 * hr;
+        if (r >= a.Mq) continue;
+        const float L = l_run[hr];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float lse2 = L > 0.f ? m_run[hr] + log2f(L) : -INFINITY;
+        const int i = r / a.G;
+        const int h = g * a.G + (r % a.G);
+        if (a.num_splits == 1) {
+            __nv_bfloat16 *dst = a.out + ((size_t(b) * a.Sq + i) * a.Hq + h) * D + (lane & 3) * 2;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt)
+                *reinterpret_cast<uint32_t *>(dst + nt * 8) =
+                    pack_bf16x2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
+            if (a.lse != nullptr && (lane & 3) == 0)
+                a.lse[(size_t(b) * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
+        } else {
+            const size_t prow = (size_t(unit) * a.Mq + r) * a.num_splits + split;
+            float *dst = a.o_part + prow * D + (lane & 3) * 2;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt)
+                *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
+            if ((lane & 3) == 0) a.lse_part[prow] = lse2;
+        }
+    }
+}
+
+// LSE-weighted combine of the split partials.  One CTA per output row
+// (b, h, i): the split LSEs give weights w_s = 2^(lse_s - max) (a split that
+// saw no visible key has lse_s = -inf and weight exactly 0), then the CTA's
+// threads split the (split, head-dim) plane, accumulate w_s * O_s with many
+// loads in flight, and reduce across splits through shared memory.
+constexpr int kCombineThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) gqa_combine_kernel(const float *__restrict__ o_part,
+                                                                      const float *__restrict__ lse_part,
+                                                                      __nv_bfloat16 *out, float *lse, int Sq,
+                                                                      int Hq, int Hkv, int G, int Mq, int S) {
+    constexpr int C4 = D / 4;                    // float4 chunks per row
+    constexpr int SL = kCombineThreads / C4;     // split lanes
+    extern __shared__ float sm[];                // [S] weights, then [SL][D] partial sums
+    float *w_s = sm;
+    float4 *red = reinterpret_cast<float4 *>(sm + ((S + 3) & ~3));
+    __shared__ float warp_red[kCombineThreads / 32];
+    __shared__ float bcast[2];
+
+    pdl_wait_primary();
+    const int tid = threadIdx.x;
+    const long row = blockIdx.x;                 // (unit * Mq + r)
+    const int r = int(row % Mq);
+    const long unit = row / Mq;
+    const int g = int(unit % Hkv);
+    const int b = int(unit / Hkv);
+    const float *lp = lse_part + size_t(row) * S;
+    const float *op = o_part + size_t(row) * S * D;
+
+    // 1. max over splits
+    float M = -INFINITY;
+    for (int s = tid; s < S; s += kCombineThreads) M = fmaxf(M, lp[s]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if ((tid & 31) == 0) warp_red[tid >> 5] = M;
+    __syncthreads();
+    if (tid == 0) {
+        float m = warp_red[0];
+        for (int w = 1; w < kCombineThreads / 32; ++w) m = fmaxf(m, warp_red[w]);
+        bcast[0] = m;
+    }
+    __syncthreads();
+    M = bcast[0];
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+
+    // 2. weights and their sum
+    float L = 0.f;
+    for (int s = tid; s < S; s += kCombineThreads) {
+        const float l2 = lp[s];
+        const float w = (l2 == -INFINITY) ? 0.f : fast_exp2(l2 - Mu);
+        w_s[s] = w;
+        L += w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    __syncthreads();  // w_s complete; warp_red free again
+    if ((tid & 31) == 0) warp_red[tid >> 5] = L;
+    __syncthreads();
+    if (tid == 0) {
+        float l = 0.f;
+        for (int w = 0; w < kCombineThreads / 32; ++w) l += warp_red[w];
+        bcast[1] = l;
+    }
+
+    // 3. weighted sum over this thread's splits for its 4 head-dim values
+    const int c = tid % C4;
+    const int sl = tid / C4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s = sl; s < S; s += SL) {
+        const float w = w_s[s];
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(op + size_t(s) * D) + c);
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+    }
+    red[sl * C4 + c] = acc;
+    __syncthreads();
+    L = bcast[1];
+    if (sl != 0) return;
+#pragma unroll
+    for (int k = 1; k < SL; ++k) {
+        const float4 y = red[k * C4 + c];
+        acc.x += y.x;
+        acc.y += y.y;
+        acc.z += y.z;
+        acc.w += y.w;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int i = r / G;
+    const int h = g * G + (r % G);
+    __nv_bfloat16 *dst = out + ((size_t(b) * Sq + i) * Hq + h) * D + c * 4;
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (lse != nullptr && c == 0)
+        lse[(size_t(b) * Hq + h) * Sq + i] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+}
+
+}  // namespace gqa

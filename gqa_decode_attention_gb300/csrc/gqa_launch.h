@@ -1,0 +1,57 @@
+// gqa_launch.h -- host-side launch plumbing shared by the kernel translation
+// units and the C-ABI front end (gqa_api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gqa_params.h"
+
+namespace gqa {
+
+// Dense kernel instances, by the number of query rows a CTA holds: cfg c has
+// 2^c consumer warps of 16 rows (16, 32, 64, 128 rows).  The TMA tile (keys
+// per ring slot) and the ring depth are chosen per (head dim, cfg) so that
+// small-group CTAs stay small and several fit on one SM.
+constexpr int kDenseCfgs = 4;
+inline int dense_cfg_for_rows(int rows) { return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3; }
+inline int dense_cfg_rows(int cfg) { return 16 << cfg; }
+constexpr int dense_tile_keys(int D, int cfg) {
+    return D == 64 ? (cfg == 0 ? 32 : 64) : D == 128 ? (cfg == 0 ? 16 : cfg == 1 ? 32 : 64)
+                                                     : (cfg <= 1 ? 16 : cfg == 2 ? 32 : 64);
+}
+constexpr int dense_stages(int D, int cfg) {
+    return D == 64 ? (cfg <= 1 ? 3 : 4) : D == 128 ? 3 : (cfg == 1 ? 4 : cfg == 3 ? 2 : 3);
+}
+
+struct DenseLaunch {
+    DenseArgs args;
+    const void *k;
+    const void *v;
+    int D;
+    int cfg;
+    cudaStream_t stream;
+    cudaEvent_t ev_before;  // measurement hook: recorded around the split kernel when both are set
+    cudaEvent_t ev_after;
+};
+
+// Encodes the TMA descriptor of a [B, Skv, Hkv, D] bf16 tensor with a
+// (64 x 1 x box_keys x 1) box and 128-byte swizzle.  Returns false on failure.
+bool make_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Skv, int Hkv, int D, int box_keys);
+
+// Per head-dimension launchers (one translation unit each).
+cudaError_t launch_dense_d64(const DenseLaunch &L);
+cudaError_t launch_dense_d128(const DenseLaunch &L);
+cudaError_t launch_dense_d256(const DenseLaunch &L);
+// Resident CTAs per SM of the dense split kernel for (D, cfg); 0 on error.
+int dense_ctas_per_sm_d64(int cfg);
+int dense_ctas_per_sm_d128(int cfg);
+int dense_ctas_per_sm_d256(int cfg);
+
+cudaError_t launch_paged_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+cudaError_t launch_paged_gather(const uint8_t *pool, const int32_t *page_table, const int32_t *topk, uint8_t *out,
+                                int B, int Hkv, int D, int page_size, int pages_per_req, int num_pages, int topk_n,
+                                unsigned *err, cudaStream_t stream);
+cudaError_t launch_fp8_to_f32(const uint8_t *codes, float *out, int n, cudaStream_t stream);
+
+}  // namespace gqa

@@ -1,0 +1,53 @@
+// gqa_params.h -- kernel argument blocks and shape constants shared by the
+// kernels and the host front end.
+#pragma once
+
+#include <stdint.h>
+#include <cuda_bf16.h>
+
+namespace gqa {
+
+// Bits of the sticky device error word.
+enum : unsigned {
+    kErrTimeout = 1u,  // a pipeline wait exceeded its time limit
+    kErrIndex = 2u,    // a page id or top-K index was out of range
+};
+
+// Granule of the dense kernel's KV splits: every split starts at a multiple
+// of this many keys.
+constexpr int kSplitKeys = 64;
+// KV heads (one warp each) per CTA of the paged kernel.
+constexpr int kPagedHeadsPerCta = 8;
+// Top-K entries whose rows are resolved per pass of the paged kernel.
+constexpr int kPagedChunk = 512;
+
+struct DenseArgs {
+    const __nv_bfloat16 *q;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *o_part;    // [B*Hkv, Mq, splits, D] fp32 (splits > 1)
+    float *lse_part;  // [B*Hkv, Mq, splits] fp32, log2 domain (splits > 1)
+    int B, Sq, Skv, Hq, Hkv, G, Mq;
+    int n_blocks, blocks_per_split, num_splits, row_groups;  // blocks of kSplitKeys keys
+    float alpha;  // scale * log2(e)
+    unsigned long long wait_limit_ns;
+    int fault_mode;  // test hook: 1 = the producer never loads the first tile
+    unsigned *err;   // device error word
+};
+
+struct PagedArgs {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *gate;
+    const uint8_t *k_pool;
+    const uint8_t *v_pool;
+    const int32_t *page_table;
+    const int32_t *topk;
+    __nv_bfloat16 *out;
+    float *lse;
+    int B, Hq, Hkv, G, page_size, pages_per_req, num_pages, topk_n;
+    float alpha;    // scale * k_scale * log2(e)
+    float v_scale;
+    unsigned *err;  // device error word
+};
+
+}  // namespace gqa

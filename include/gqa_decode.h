@@ -1,0 +1,196 @@
+/*
+ * gqa_decode.h -- C ABI of the GB300 (sm_103a) grouped-query decode attention
+ * library (libgqa_decode.so).
+ *
+ * The operation (web pages on grouped-query decode attention):
+ *  - "When the K/V copy costs more than the attention", section "What I was
+ *    looking at": several query heads share one KV head, and query head h
+ *    reads KV head h // (Hq / Hkv) in place -- K and V are never copied or
+ *    expanded to the query head count.  The same page names the two decode
+ *    defects this library is built around: a KV walk that is not split across
+ *    CTAs, and a query tile sized for prefill that is nearly empty at decode.
+ *  - "Attention Kernel Portability Across GPU Architectures", section
+ *    "Decode": a decode step reads the whole KV cache once; its traffic is
+ *    2 * B * Hkv * N * D * bytes_per_element.
+ *  - "Sparse paged GQA decode attention with FP8 KV cache on SM89", sections
+ *    "Workload" and "Implementations": the sparse, paged variant -- top-K
+ *    selected token indices per request, a page table, page size 16, an FP8
+ *    E4M3FN K/V pool with per-tensor k_scale / v_scale (k_scale folded into the
+ *    score scale, v_scale applied once on the output), then a sigmoid gate.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - S_q > 1 uses a bottom-right aligned causal mask: query row i of S_q sees
+ *    keys j <= S_kv - S_q + i.
+ *  - LSE is the natural log of sum_j exp(scale * q.k_j) over visible keys.
+ *  - Tensor layouts (all contiguous, row-major, C order):
+ *      q, out         bf16  [B, Sq, Hq, D]
+ *      k, v           bf16  [B, Skv, Hkv, D]
+ *      lse            fp32  [B, Hq, Sq]
+ *      k_pool, v_pool uint8 [num_pages, page_size, Hkv, D]  (E4M3FN codes)
+ *      page_table     int32 [B, pages_per_req]
+ *      topk_idx       int32 [B, topk]  logical token ids, -1 = padding
+ *      q, gate, out (paged) bf16 [B, Hq, D];  lse (paged) fp32 [B, Hq]
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers must be device-accessible memory owned
+ *    by the caller; the library never frees them.  Every bf16 / uint8 tensor
+ *    pointer must be 16-byte aligned, fp32 and int32 pointers 4-byte aligned
+ *    (GQA_ERR_ALIGNMENT otherwise).
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *    and never synchronise, except gqa_device_status and gqa_decode_host.
+ *  - The returned status covers host-detectable errors.  On any error status
+ *    other than GQA_ERR_CUDA nothing has been launched.
+ *  - Device-detected problems (an index out of range in the paged path, a
+ *    pipeline wait that exceeded its time limit) set a sticky device error
+ *    word that gqa_device_status reads and clears.
+ *  - scale <= 0 or NaN selects the default 1 / sqrt(D).
+ *  - Hq must be a multiple of Hkv.
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *gqa_stream_t;
+
+typedef enum gqa_status {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,    /* bad size, null required pointer, Hq % Hkv != 0, Sq > Skv, ... */
+    GQA_ERR_UNSUPPORTED = 2,    /* D not in {64, 128, 256}, or a size beyond the library's limits */
+    GQA_ERR_ALIGNMENT = 3,      /* a tensor pointer is not 16-byte aligned */
+    GQA_ERR_NO_MEMORY = 4,      /* workspace allocation failed or caller workspace too small */
+    GQA_ERR_CUDA = 5,           /* a CUDA runtime/driver call or a launch failed */
+    GQA_ERR_DEVICE_TIMEOUT = 6, /* device: a pipeline wait exceeded its time limit */
+    GQA_ERR_DEVICE_INDEX = 7    /* device: page id or top-K index out of range (paged path) */
+} gqa_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gqa_status_string(gqa_status s);
+
+/* Library version string (static). */
+const char *gqa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Dense grouped-query decode attention.
+ *
+ * For every batch row b, query head h (KV head g = h // (Hq/Hkv)) and query
+ * row i < Sq:  s_j = scale * q[b,i,h,:] . k[b,j,g,:]  for visible j,
+ *   lse[b,h,i] = ln sum_j exp(s_j),  out[b,i,h,:] = sum_j exp(s_j - lse) v[b,j,g,:].
+ * The KV walk is split across CTAs (split count chosen from Skv, B*Hkv and
+ * the SM count); each CTA owns one (b, g, split) and the whole group of
+ * (Hq/Hkv)*Sq query rows, so each K/V byte is read from HBM once.  When more
+ * than one split is used, an LSE-weighted combine kernel produces out / lse.
+ *
+ * q, k, v, out : device, bf16, layouts above.   lse : device fp32 or NULL.
+ * Limits: 1 <= Sq <= Skv, B >= 1, Hkv >= 1, Hq % Hkv == 0,
+ *         (Hq/Hkv)*Sq <= 4096, Skv < 2^31 / Hkv.
+ * D in {64, 128, 256}.  Splits start at multiples of 64 keys.
+ * Workspace: fp32 partials, allocated stream-ordered on `stream` from a
+ * library-owned memory pool and released stream-ordered after the combine;
+ * no allocation happens when a single split is used.
+ * ------------------------------------------------------------------------ */
+gqa_status gqa_decode(const void *q, const void *k, const void *v, void *out, float *lse,
+                      int B, int Sq, int Skv, int Hq, int Hkv, int D, float scale,
+                      gqa_stream_t stream);
+
+/* Split count gqa_decode would use for this shape on the current device
+ * (>= 1), or a negative gqa_status on invalid arguments. */
+int gqa_decode_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int D);
+
+/* Bytes of workspace gqa_decode_ex needs for `num_splits` (0 = automatic
+ * choice); 0 when a single split is used.  Returns 0 on invalid arguments. */
+size_t gqa_decode_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int D, int num_splits);
+
+/* gqa_decode with an explicit split count (0 = automatic; the count is
+ * clamped to the number of 64-key blocks and then evened out so that every
+ * split but the last covers the same number of blocks) and an optional
+ * caller workspace.  When
+ * `workspace` is NULL the library allocates stream-ordered as gqa_decode
+ * does; otherwise `workspace` must be device memory of at least
+ * gqa_decode_workspace_bytes(...) bytes, 256-byte aligned, not used by any
+ * other work in flight on another stream.  The same split count always
+ * gives bitwise-identical results. */
+gqa_status gqa_decode_ex(const void *q, const void *k, const void *v, void *out, float *lse,
+                         int B, int Sq, int Skv, int Hq, int Hkv, int D, float scale,
+                         int num_splits, void *workspace, size_t workspace_bytes,
+                         gqa_stream_t stream);
+
+/* End-to-end form with HOST buffers: copies q, k, v host->device, runs
+ * gqa_decode, copies out (and lse when non-NULL) device->host and waits for
+ * the stream.  Host buffers should be pinned for full copy bandwidth.  Device
+ * buffers are allocated and freed stream-ordered inside the call. */
+gqa_status gqa_decode_host(const void *q_host, const void *k_host, const void *v_host,
+                           void *out_host, float *lse_host,
+                           int B, int Sq, int Skv, int Hq, int Hkv, int D, float scale,
+                           gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Sparse paged GQA decode with an FP8 E4M3FN K/V pool and a sigmoid gate.
+ *
+ * For request b, query head h (KV head g = h // (Hq/Hkv)) and each selected
+ * entry k < topk with t = topk_idx[b,k] >= 0:
+ *   page p = page_table[b, t / page_size], slot r = t % page_size,
+ *   K^ = e4m3fn(k_pool[p, r, g, :]) * k_scale,  V^ = e4m3fn(v_pool[p, r, g, :]) * v_scale,
+ *   s_k = scale * q[b,h,:] . K^.
+ * attn = softmax(s) V^;  out[b,h,:] = sigmoid(gate[b,h,:]) * attn;
+ * lse[b,h] = ln sum_k exp(s_k) of the ungated scores.  Entries with t < 0
+ * are padding and skipped; a row with no valid entry gives out = 0 and
+ * lse = -inf.  Entries are used with multiplicity.
+ *
+ * q, gate, out : device bf16 [B, Hq, D].  lse : device fp32 [B, Hq] or NULL.
+ * k_pool, v_pool : device uint8 [num_pages, page_size, Hkv, D].
+ * page_table : device int32 [B, pages_per_req].  topk_idx : device int32 [B, topk].
+ * k_scale, v_scale : host fp32 scalars (per-tensor dequantisation scales).
+ * Limits: D in {64, 128}; Hq / Hkv <= 16; topk <= pages_per_req * page_size;
+ *         topk <= 65536; num_pages * page_size < 2^31.
+ * Indices are trusted for speed; a t >= pages_per_req * page_size or a page
+ * id outside [0, num_pages) is skipped and flags GQA_ERR_DEVICE_INDEX in the
+ * device error word.  No workspace.
+ * ------------------------------------------------------------------------ */
+gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
+                                const uint8_t *k_pool, const uint8_t *v_pool,
+                                const int32_t *page_table, const int32_t *topk_idx,
+                                float k_scale, float v_scale, void *out, float *lse,
+                                int B, int Hq, int Hkv, int D, int page_size, int pages_per_req,
+                                int num_pages, int topk, float scale, gqa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Test hooks.  They run the paged kernel's own index mapping and FP8
+ * conversion in isolation so those can be checked bit for bit.
+ * ------------------------------------------------------------------------ */
+
+/* out[b, k, g, :] = pool[page_table[b, t/ps], t%ps, g, :] for t = topk_idx[b,k];
+ * padding (t < 0) and out-of-range entries give zero bytes (out-of-range also
+ * flags GQA_ERR_DEVICE_INDEX).  out: device uint8 [B, topk, Hkv, D]. */
+gqa_status gqa_paged_gather_fp8(const uint8_t *pool, const int32_t *page_table,
+                                const int32_t *topk_idx, uint8_t *out,
+                                int B, int Hkv, int D, int page_size, int pages_per_req,
+                                int num_pages, int topk, gqa_stream_t stream);
+
+/* out[i] = value of E4M3FN code codes[i] as fp32, through the same in-register
+ * conversion the paged kernel uses.  n >= 0 elements, device pointers. */
+gqa_status gqa_fp8_e4m3fn_to_f32(const uint8_t *codes, float *out, int n, gqa_stream_t stream);
+
+/* Waits for `stream`, then reads and clears the device error word:
+ * GQA_OK, GQA_ERR_DEVICE_TIMEOUT or GQA_ERR_DEVICE_INDEX (GQA_ERR_CUDA if the
+ * wait itself failed). */
+gqa_status gqa_device_status(gqa_stream_t stream);
+
+/* Sets the time limit, in nanoseconds, of every pipeline wait in the dense
+ * kernel (default 2e9).  Exceeding it aborts the CTA and flags
+ * GQA_ERR_DEVICE_TIMEOUT.  0 restores the default.  Affects later launches
+ * on all streams. */
+void gqa_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_H */

@@ -1,0 +1,38 @@
+/*
+ * gqa_decode_debug.h -- test-only controls of libgqa_decode.so.
+ *
+ * Not part of the operation's interface; the pages have no counterpart.  They
+ * exist so the test suite can exercise the device-side failure path without
+ * faulting a GPU.
+ */
+#ifndef GQA_DECODE_DEBUG_H
+#define GQA_DECODE_DEBUG_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fault injection for the dense kernel's bounded pipeline waits.
+ * mode 0: normal operation (default).
+ * mode 1: the producer never issues the load of each CTA's first KV tile, so
+ *         the consumers' wait on it runs out after the configured wait limit
+ *         (gqa_set_wait_limit_ns); the CTA flags GQA_ERR_DEVICE_TIMEOUT in the
+ *         device error word, lets its other loads land, and returns.  Outputs
+ *         are then undefined.
+ * Affects later gqa_decode / gqa_decode_ex launches on all streams. */
+void gqa_debug_set_fault_mode(int mode);
+
+/* Measurement hook.  When both are non-NULL, every later dense or paged
+ * decode call records `before` on its stream immediately before launching its
+ * main kernel (the split kernel, or the paged kernel) and `after` immediately
+ * after it, so a caller can time that kernel alone with
+ * cudaEventElapsedTime.  The handles are cudaEvent_t created by the caller;
+ * pass NULL, NULL to stop.  Recording between the split and the combine
+ * kernel serialises the combine's early launch, so use it only to measure. */
+void gqa_debug_set_kernel_events(void *before, void *after);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_DECODE_DEBUG_H */

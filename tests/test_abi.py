@@ -1,0 +1,135 @@
+"""C ABI boundary checks that need no GPU: the library loads, exports every
+symbol its headers declare, and rejects bad arguments with the documented
+status before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import gqa_decode_attention_gb300 as gq
+from gqa_decode_attention_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gq.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(gqa_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_headers_declare_something():
+    names = _declared_functions()
+    assert "gqa_decode" in names and "gqa_decode_paged_fp8" in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert sorted(gq.EXPORTS) == _declared_functions()
+
+
+def test_status_strings(lib):
+    for code, name in gq.STATUS.items():
+        assert gq.gqa_status_string(code) == name
+    assert "sm_103a" in gq.gqa_version()
+
+
+# Fake, never-dereferenced device addresses: validation must reject the call
+# before any CUDA work happens.
+A = 0x7F0000000000  # 16-byte aligned
+MIS = A + 2         # misaligned
+
+
+def _dense(lib, q=A, k=A, v=A, out=A, lse=A, B=1, Sq=1, Skv=64, Hq=8, Hkv=2, D=128):
+    return lib.gqa_decode(q, k, v, out, lse, B, Sq, Skv, Hq, Hkv, D, 0.0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), 1),          # Hq % Hkv != 0
+    (dict(Sq=3, Skv=2), 1),          # Sq > Skv
+    (dict(B=0), 1),
+    (dict(Sq=0), 1),
+    (dict(Skv=0), 1),
+    (dict(Hkv=0), 1),
+    (dict(D=96), 2),                 # unsupported head dim
+    (dict(D=512), 2),
+    (dict(Hq=4096 * 2, Hkv=1, Sq=1), 2),  # group rows beyond the limit
+    (dict(q=0), 1),                  # null pointers
+    (dict(k=0), 1),
+    (dict(out=0), 1),
+    (dict(q=MIS), 3),                # alignment
+    (dict(k=MIS), 3),
+    (dict(v=MIS), 3),
+    (dict(out=MIS), 3),
+    (dict(lse=A + 1), 3),
+])
+def test_dense_rejects(lib, kw, status):
+    assert _dense(lib, **kw) == status
+
+
+def test_dense_ex_rejects(lib):
+    assert lib.gqa_decode_ex(A, A, A, A, A, 1, 1, 64, 8, 2, 128, 0.0, -1, None, 0, None) == 1
+    assert lib.gqa_decode_workspace_bytes(1, 1, 64, 6, 4, 128, 0) == 0
+    assert lib.gqa_decode_num_splits(1, 1, 64, 6, 4, 128) == -1
+    assert lib.gqa_decode_num_splits(1, 1, 64, 8, 2, 96) == -2
+
+
+def _paged(lib, q=A, gate=A, kp=A, vp=A, pt=A, tk=A, ks=1.0, vs=1.0, out=A, lse=A, B=2, Hq=8, Hkv=2, D=128,
+           ps=16, ppr=4, num_pages=16, topk=32):
+    return lib.gqa_decode_paged_fp8(q, gate, kp, vp, pt, tk, ks, vs, out, lse, B, Hq, Hkv, D, ps, ppr,
+                                    num_pages, topk, 0.0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), 1),
+    (dict(topk=65), 1),              # more entries than the request has tokens
+    (dict(topk=-1), 1),
+    (dict(ps=0), 1),
+    (dict(num_pages=0), 1),
+    (dict(D=96), 2),
+    (dict(D=256), 2),                # not built for the paged path
+    (dict(Hq=64, Hkv=2), 2),         # group of 32 > 16
+    (dict(ks=float("inf")), 1),
+    (dict(vs=float("nan")), 1),
+    (dict(q=0), 1),
+    (dict(gate=0), 1),
+    (dict(tk=0), 1),
+    (dict(kp=MIS), 3),
+    (dict(gate=MIS), 3),
+    (dict(pt=A + 2), 3),
+])
+def test_paged_rejects(lib, kw, status):
+    assert _paged(lib, **kw) == status
+
+
+def test_gather_and_convert_reject(lib):
+    assert lib.gqa_paged_gather_fp8(A, A, A, A, 2, 2, 128, 16, 4, 16, 65, None) == 1
+    assert lib.gqa_paged_gather_fp8(MIS, A, A, A, 2, 2, 128, 16, 4, 16, 32, None) == 3
+    assert lib.gqa_fp8_e4m3fn_to_f32(A, A, -1, None) == 1
+    assert lib.gqa_fp8_e4m3fn_to_f32(A, A + 2, 4, None) == 3
+    assert lib.gqa_fp8_e4m3fn_to_f32(None, None, 0, None) == 0  # nothing to do
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("gqa_decode_attention_gb300")
+    saved = mod._lib_handle
+    mod._lib_handle = None
+    try:
+        with pytest.raises(ImportError):
+            mod.load_library(str(tmp_path / "missing.so"))
+    finally:
+        mod._lib_handle = saved
