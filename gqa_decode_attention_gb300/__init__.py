@@ -32,7 +32,8 @@ GQA_OK = 0
 # Every symbol the headers in include/ declare.
 EXPORTS = [
     "gqa_status_string", "gqa_version", "gqa_decode", "gqa_decode_num_splits",
-    "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_host", "gqa_decode_paged_fp8",
+    "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
+    "gqa_decode_host", "gqa_decode_paged_fp8",
     "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
     "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events",
 ]
@@ -68,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_workspace_bytes.argtypes = [i] * 7
     lib.gqa_decode_ex.restype = st
     lib.gqa_decode_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.gqa_decode_noalloc.restype = st
+    lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.gqa_decode_noalloc_scratch_bytes.restype = sz
+    lib.gqa_decode_noalloc_scratch_bytes.argtypes = []
     lib.gqa_decode_host.restype = st
     lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.gqa_decode_paged_fp8.restype = st
@@ -148,6 +153,24 @@ def gqa_decode_ex(q, k, v, out=None, lse=None, scale=None, num_splits=0, workspa
                            _scale_arg(scale), int(num_splits), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "gqa_decode_ex")
     return out, lse
+
+
+def gqa_decode_noalloc(q, k, v, out, lse=None, scale=None, num_splits=0, stream=None):
+    """Allocation-free dense decode (fixed in-library scratch, caller-owned
+    out / lse; see include/gqa_decode.h).  Allocates nothing, not even outputs."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        _need(t, n, torch.bfloat16, "cuda")
+    B, Sq, Hq, D = q.shape
+    _, Skv, Hkv, _ = k.shape
+    st = lib.gqa_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Skv, Hq, Hkv, D,
+                                _scale_arg(scale), int(num_splits), _stream(stream))
+    _check(st, "gqa_decode_noalloc")
+    return out, lse
+
+
+def gqa_decode_noalloc_scratch_bytes() -> int:
+    return int(load_library().gqa_decode_noalloc_scratch_bytes())
 
 
 def gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D) -> int:

@@ -122,6 +122,36 @@ gqa_status gqa_decode_ex(const void *q, const void *k, const void *v, void *out,
                          int num_splits, void *workspace, size_t workspace_bytes,
                          gqa_stream_t stream);
 
+/* Allocation-free dense decode.  The pages have no counterpart to this entry
+ * point; it exists for callers that cannot allocate device memory while they
+ * decode (a memory budget fixed at start-up, real-time loops where an
+ * allocation could block or fail, hosts that hand the library only its input
+ * and output tensors).  It runs the same kernels as gqa_decode_ex with the
+ * same arguments, but the split partials live in a scratch array compiled
+ * into the library (GQA_NOALLOC_SCRATCH_BYTES = 32 MiB, present on every GPU
+ * that loads the library until the process exits) instead of a workspace, and
+ * the call allocates nothing: no cudaMalloc, no pool, no library allocator.
+ *  - The caller still passes q, k, v, out and lse as for gqa_decode.
+ *  - A shape whose partials need more than the scratch holds
+ *    (gqa_decode_workspace_bytes(...) > gqa_decode_noalloc_scratch_bytes())
+ *    is refused with GQA_ERR_NO_MEMORY before anything is launched; fewer
+ *    splits (num_splits > 0) need less.
+ *  - The first call on each device resolves the scratch's device address
+ *    with that device current; make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one scratch array and it keeps the
+ *    last call's contents.  Nothing in it needs to start at zero: every
+ *    partial a call reads was written earlier in the same call.  Calls that
+ *    may overlap on the GPU (different streams, or devices' work not ordered
+ *    by the caller) race on the scratch: serialise them. */
+#define GQA_NOALLOC_SCRATCH_BYTES (32u << 20)
+gqa_status gqa_decode_noalloc(const void *q, const void *k, const void *v, void *out, float *lse,
+                              int B, int Sq, int Skv, int Hq, int Hkv, int D, float scale,
+                              int num_splits, gqa_stream_t stream);
+
+/* Size in bytes of the scratch array gqa_decode_noalloc uses. */
+size_t gqa_decode_noalloc_scratch_bytes(void);
+
 /* End-to-end form with HOST buffers: copies q, k, v host->device, runs
  * gqa_decode, copies out (and lse when non-NULL) device->host and waits for
  * the stream.  Host buffers should be pinned for full copy bandwidth.  Device
