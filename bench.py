@@ -38,8 +38,8 @@ import gqa_inputs  # noqa: E402
 
 METRIC = "GQA decode µs/call and KV-cache HBM GB/s (% of measured GB300 peak)"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["gqa_dense_kernel.cuh", "gqa_paged_kernel.cuh", "gqa_common.cuh", "gqa_params.h",
-                  "gqa_dense_impl.cuh"]
+KERNEL_SOURCES = ["gqa_dense_kernel.cuh", "gqa_dense_umma.cuh", "gqa_umma.cuh", "gqa_paged_kernel.cuh",
+                  "gqa_common.cuh", "gqa_params.h", "gqa_dense_impl.cuh"]
 
 
 # ---------------------------------------------------------------------------
@@ -461,8 +461,8 @@ def run_gqa(args) -> int:
             "frac_of_copy_peak_this_run": round(value / world / copy_peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(cfg.name),
-                         "kernel": "gqa_dense_split_kernel" if isinstance(cfg, gqa_inputs.DenseConfig)
-                         else "gqa_paged_fp8_kernel",
+                         "kernel": ("gqa_dense_umma_kernel" if cfg.D == 256 else "gqa_dense_split_kernel")
+                         if isinstance(cfg, gqa_inputs.DenseConfig) else "gqa_paged_fp8_kernel",
                          "kernel_us": round(kern_avg * 1e3, 2),
                          "algorithmic_bytes_per_launch": nbytes},
             "cpu_baseline": cpu_base,

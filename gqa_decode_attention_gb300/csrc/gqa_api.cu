@@ -146,8 +146,8 @@ gqa_status check_dense(int B, int Sq, int Skv, int Hq, int Hkv, int D, DenseShap
     s->D = D;
     s->G = int(G);
     s->Mq = int(Mq);
-    s->cfg = dense_cfg_for_rows(int(Mq < 128 ? Mq : 128));
-    s->qrows = dense_cfg_rows(s->cfg);
+    s->cfg = D == 256 ? 0 : dense_cfg_for_rows(int(Mq < 128 ? Mq : 128));
+    s->qrows = dense_rows_per_cta(D, s->cfg);
     s->row_groups = int((Mq + s->qrows - 1) / s->qrows);
     if (long(Hkv) * s->row_groups > 65535) return GQA_ERR_UNSUPPORTED;
     s->n_blocks = (Skv + kSplitKeys - 1) / kSplitKeys;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include "gqa_dense_kernel.cuh"
+#include "gqa_dense_umma.cuh"
 #include "gqa_launch.h"
 
 namespace gqa {
@@ -67,6 +68,42 @@ static cudaError_t launch_combine(const DenseLaunch &L) {
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, (const float *)a.o_part, (const float *)a.lse_part,
                               a.out, a.lse, a.Sq, a.Hq, a.Hkv, a.G, a.Mq, a.num_splits);
+}
+
+// tcgen05 engine: one instance per head dim, 128 rows per CTA.
+template <int D>
+static cudaError_t launch_umma(const DenseLaunch &L) {
+    using C = UmmaCfg<D>;
+    auto kern = gqa_dense_umma_kernel<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    CUtensorMap tk, tv;
+    if (!make_kv_tensor_map(&tk, L.k, L.args.B, L.args.Skv, L.args.Hkv, D, C::BN) ||
+        !make_kv_tensor_map(&tv, L.v, L.args.B, L.args.Skv, L.args.Hkv, D, C::BN))
+        return cudaErrorInvalidValue;
+    const dim3 grid(L.args.Hkv * L.args.row_groups, L.args.num_splits, L.args.B);
+    const bool timed = L.ev_before != nullptr && L.ev_after != nullptr;
+    if (timed) cudaEventRecord(L.ev_before, L.stream);
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, L.stream>>>(tk, tv, L.args);
+    if (timed) cudaEventRecord(L.ev_after, L.stream);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || L.args.num_splits == 1) return e;
+    return launch_combine<D>(L);
+}
+
+template <int D>
+static int umma_occupancy() {
+    using C = UmmaCfg<D>;
+    auto kern = gqa_dense_umma_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM_BYTES) != cudaSuccess) return 0;
+    return n;
 }
 
 template <int D>

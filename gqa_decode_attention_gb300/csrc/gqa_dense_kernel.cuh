@@ -177,7 +177,9 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
 
     for (int it = 0; it < n_it; ++it) {
         const int st = it % C::STAGES;
-        if (!mbar_wait_bounded(&full[st], (it / C::STAGES) & 1, a.wait_limit_ns, abort_flag)) {
+        // ldmatrix / mma.sync are warp-collective: the whole warp leaves together.
+        const bool got = mbar_wait_bounded(&full[st], (it / C::STAGES) & 1, a.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
             failed = true;
             break;
         }

@@ -1,0 +1,385 @@
+// gqa_dense_umma.cuh -- split-KV grouped-query decode on the fifth-generation
+// tensor cores (tcgen05 + TMEM), for the wide head dimension (D = 256).
+//
+// Same unit of work as the mma.sync kernel: one CTA owns (batch row b, KV
+// head g, KV split s) and up to 128 query rows of that head's group (rows
+// r = i * G + hl, h = g * G + hl), so query head h reads KV head
+// g = h / (Hq / Hkv) in place ("When the K/V copy costs more than the
+// attention", section "What I was looking at") and each K/V byte of the split
+// is read from HBM once for the whole group.
+//
+// Roles (6 warps):
+//   warp 0      TMA producer: K and V tiles of 64 keys x D into a ring of
+//               shared-memory stages (128-byte swizzle), full / empty mbarriers.
+//   warp 1      allocates TMEM; lane 0 issues every MMA:
+//                 S(j) = Q K(j)^T   M=128 rows, N=64 keys, K=D  -> TMEM S[j%2]
+//                 O   += P(j) V(j)  M=128 rows, N=D,  K=64 keys -> TMEM O
+//               in the order QK(0), QK(1), PV(0), QK(2), PV(1), ... so the
+//               tensor core computes the next scores while the softmax runs.
+//   warps 2..5  one thread per query row (TMEM lane): load the S row, scale
+//               into the log2 domain, causal mask, online softmax, write P as
+//               bf16 to shared memory (the A operand of PV), and the epilogue.
+// The online softmax keeps a per-row reference maximum and rescales O (in
+// TMEM) only when a row's maximum grows by more than 2^8; in between, the
+// weights are exp2(s - reference) <= 2^8, which changes rounding only.  Every
+// row is processed by its own thread with the same instruction sequence, so
+// a row's result never depends on how many rows share the CTA.
+//
+// Every wait is bounded in wall time; on expiry the CTA flags the device
+// error word, drains its own copies and MMAs, frees its TMEM and returns.
+#pragma once
+
+#include "gqa_common.cuh"
+#include "gqa_params.h"
+#include "gqa_umma.cuh"
+
+namespace gqa {
+
+template <int D>
+struct UmmaCfg {
+    static constexpr int BM = 128;  // query rows per CTA (TMEM lanes)
+    static constexpr int BN = 64;   // keys per tile
+    static constexpr int CHUNKS = D / 64;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int TILE_BYTES = BN * D * 2;  // K or V tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int P_BYTES = BM * BN * 2;
+    static constexpr int BUDGET = 227 * 1024 - 1024 - 256;
+    static constexpr int STAGES_FIT = (BUDGET - Q_BYTES - 2 * P_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+    static constexpr int RING_OFF = Q_BYTES;
+    static constexpr int P_OFF = RING_OFF + STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+    static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
+    static constexpr int THREADS = 192;
+    static constexpr uint32_t S_COL = 0;     // two 64-column score buffers
+    static constexpr uint32_t O_COL = 128;   // D columns of fp32 output
+    static constexpr uint32_t TMEM_COLS = (O_COL + D) <= 256 ? 256 : 512;
+    static constexpr float kRescaleLog2 = 8.f;
+    static_assert(STAGES >= 2, "ring needs two stages");
+    static_assert(D % 64 == 0 && D <= 256, "head dim");
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    gqa_dense_umma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const DenseArgs a) {
+    using C = UmmaCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qs = smem;
+    uint8_t *ring = smem + C::RING_OFF;
+    uint8_t *ps = smem + C::P_OFF;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    uint64_t *s_full = empty + C::STAGES;  // [2]
+    uint64_t *p_ready = s_full + 2;        // [2]
+    uint64_t *o_done = p_ready + 2;        // [1]
+    uint64_t *fin = o_done + 1;            // [1]
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(fin + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_s + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = blockIdx.x / a.row_groups;
+    const int rg = blockIdx.x % a.row_groups;
+    const int split = blockIdx.y;
+    const int b = blockIdx.z;
+    const int key_begin = split * a.blocks_per_split * kSplitKeys;
+    const int key_end = min(a.Skv, key_begin + a.blocks_per_split * kSplitKeys);
+    const int n_it = (key_end - key_begin + C::BN - 1) / C::BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_ready[s], 128);
+        }
+        mbar_init(o_done, 1);
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_base_s, C::TMEM_COLS);
+    if (warp >= 2) {
+        // Stage the CTA's query rows (K-major, 128-byte swizzle, chunk-major).
+        const int t = threadIdx.x - 64;
+        for (int idx = t; idx < C::BM * (D / 8); idx += 128) {
+            const int lr = idx / (D / 8);
+            const int u = idx % (D / 8);
+            const int r = rg * C::BM + lr;
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (r < a.Mq) {
+                const int i = r / a.G;
+                const int h = g * a.G + (r % a.G);
+                val = *reinterpret_cast<const uint4 *>(a.q + ((size_t(b) * a.Sq + i) * a.Hq + h) * D + u * 8);
+            }
+            *reinterpret_cast<uint4 *>(qs + (u >> 3) * (C::BM * 128) + swz128(lr, u & 7)) = val;
+        }
+        fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tbase = *tmem_base_s;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            int issued = 0;
+            bool ok = true;
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % C::STAGES;
+                const int round = it / C::STAGES;
+                if (round > 0 && !mbar_wait_bounded(&empty[st], (round - 1) & 1, a.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (a.fault_mode == 1 && it == 0) {
+                    issued = 1;
+                    continue;  // test hook: this stage never fills
+                }
+                uint8_t *ks = ring + st * C::STAGE_BYTES;
+                uint8_t *vs = ks + C::TILE_BYTES;
+                const int j0 = key_begin + it * C::BN;
+                mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_4d(ks + c * C::BN * 128, &tmK, &full[st], c * 64, g, j0, b);
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    tma_load_4d(vs + c * C::BN * 128, &tmV, &full[st], c * 64, g, j0, b);
+                issued = it + 1;
+            }
+            if (!ok) {
+                flag_error(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            if (!ok || *abort_flag) {
+                for (int it = max(0, issued - C::STAGES); it < issued; ++it) {
+                    if (a.fault_mode == 1 && it == 0) continue;
+                    mbar_wait_bounded(&full[it % C::STAGES], (it / C::STAGES) & 1, a.wait_limit_ns, nullptr);
+                }
+            }
+        }
+        return;  // the producer never touches TMEM
+    }
+
+    if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_qk = idesc_bf16_f32(C::BM, C::BN, false, false);
+            const uint32_t idesc_pv = idesc_bf16_f32(C::BM, D, false, true);
+            const uint32_t q_addr = smem_u32(qs);
+            const uint32_t ring_addr = smem_u32(ring);
+            const uint32_t p_addr = smem_u32(ps);
+            bool ok = true;
+            auto issue_qk = [&](int j) -> bool {
+                const int st = j % C::STAGES;
+                if (!mbar_wait_bounded(&full[st], (j / C::STAGES) & 1, a.wait_limit_ns, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t kaddr = ring_addr + st * C::STAGE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t ad = smem_desc_sw128(q_addr + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024);
+                    umma_bf16(tbase + C::S_COL + (j & 1) * C::BN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&s_full[j & 1]);
+                return true;
+            };
+            if (n_it > 0) ok = issue_qk(0);
+            for (int j = 0; ok && j < n_it; ++j) {
+                if (j + 1 < n_it && !issue_qk(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait_bounded(&p_ready[j & 1], (j >> 1) & 1, a.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const int st = j % C::STAGES;
+                const uint32_t vaddr = ring_addr + st * C::STAGE_BYTES + C::TILE_BYTES;
+                const uint32_t paddr = p_addr + (j & 1) * C::P_BYTES;
+#pragma unroll
+                for (int kg = 0; kg < C::BN / 16; ++kg) {
+                    const uint64_t ad = smem_desc_sw128(paddr + kg * 32, 16, 1024);
+                    const uint64_t bd = smem_desc_sw128(vaddr + kg * 2048, C::BN * 128, 1024);
+                    umma_bf16(tbase + C::O_COL, ad, bd, idesc_pv, (j > 0 || kg > 0) ? 1u : 0u);
+                }
+                umma_commit(o_done);
+                umma_commit(&empty[st]);
+            }
+            if (!ok) {
+                flag_error(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+            // Drain: every MMA this thread issued has finished before TMEM is freed.
+            umma_commit(fin);
+            mbar_wait_bounded(fin, 0, a.wait_limit_ns, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+        const int lr = quarter * 32 + lane;     // local row = TMEM lane
+        const int r = rg * C::BM + lr;
+        const int i_row = r < a.Mq ? r / a.G : a.Sq - 1;
+        const int kmax = a.Skv - a.Sq + i_row;  // last visible key (bottom-right causal)
+        const int mask_from = a.Skv - a.Sq;
+        const uint32_t lane_base = tbase + (uint32_t(quarter * 32) << 16);
+        float m_ref = -INFINITY;  // reference maximum (log2 domain)
+        float l = 0.f;
+        bool failed = false;
+        uint8_t *prow_base = ps + lr * 128;
+
+        // tcgen05.ld / st are warp-collective: every TMEM access below is made
+        // by all 32 lanes together; per-row conditions only select values and
+        // guard the global stores.
+        for (int j = 0; j < n_it; ++j) {
+            const int sb = j & 1;
+            const bool got = mbar_wait_bounded(&s_full[sb], (j >> 1) & 1, a.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                failed = true;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t sr[2][32];
+            tmem_ld32(lane_base + C::S_COL + sb * C::BN, sr[0]);
+            tmem_ld32(lane_base + C::S_COL + sb * C::BN + 32, sr[1]);
+            tmem_wait_ld();
+
+            const int key0 = key_begin + j * C::BN;
+            const bool need_mask = key0 + C::BN - 1 > mask_from;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float t = __uint_as_float(sr[h][c]) * a.alpha;
+                    if (need_mask && key0 + h * 32 + c > kmax) t = -INFINITY;
+                    sr[h][c] = __float_as_uint(t);
+                    mx = fmaxf(mx, t);
+                }
+            // A row whose maximum grew by more than 2^8 takes it as the new
+            // reference; if it had accumulated anything, its O row is rescaled.
+            const bool renew = mx > m_ref + C::kRescaleLog2;
+            const bool rescale = renew && l > 0.f;
+            if (__any_sync(0xffffffffu, rescale)) {
+                // PV(j-1) must have finished writing O
+                const bool od = mbar_wait_bounded(o_done, (j - 1) & 1, a.wait_limit_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, od)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after_sync();
+                const float corr = rescale ? fast_exp2(m_ref - mx) : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_base + C::O_COL + c * 32, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+                    tmem_st32(lane_base + C::O_COL + c * 32, ov);
+                }
+                tmem_wait_st();
+                l *= corr;
+            }
+            if (renew) m_ref = mx;
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+            // P = exp2(t - reference) as bf16, straight into the swizzled P tile
+            uint8_t *prow = prow_base + sb * C::P_BYTES;
+            float psum = 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = u * 8 + e * 2;
+                    const float p0 = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_use);
+                    const float p1 = fast_exp2(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]) - m_use);
+                    psum += p0 + p1;
+                    w[e] = pack_bf16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(prow + ((u ^ (lr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l += psum;
+            fence_proxy_async_shared();
+            tc_fence_before_sync();
+            mbar_arrive(&p_ready[sb]);
+        }
+
+        if (failed) {
+            flag_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
+        pdl_launch_dependents();
+        bool have_o = false;
+        if (!failed && n_it > 0) {
+            const bool od = mbar_wait_bounded(o_done, (n_it - 1) & 1, a.wait_limit_ns, abort_flag) && !*abort_flag;
+            have_o = __all_sync(0xffffffffu, od);
+            if (!have_o) {
+                flag_error(a.err, kErrTimeout);
+                *abort_flag = 1;
+            }
+        }
+        if (have_o) {
+            tc_fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
+            const bool real = r < a.Mq;
+            const int h = g * a.G + (r % a.G);
+            const int unit = b * a.Hkv + g;
+            __nv_bfloat16 *dst = a.out + ((size_t(b) * a.Sq + i_row) * a.Hq + h) * D;
+            const size_t prow_i = (size_t(unit) * a.Mq + r) * a.num_splits + split;
+            float *pdst = a.o_part + prow_i * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + C::O_COL + c * 32, ov);
+                tmem_wait_ld();
+                if (!real) continue;
+                if (a.num_splits == 1) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<uint4 *>(dst + c * 32 + e * 8) =
+                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        *reinterpret_cast<float4 *>(pdst + c * 32 + e * 4) =
+                            make_float4(__uint_as_float(ov[4 * e]) * inv, __uint_as_float(ov[4 * e + 1]) * inv,
+                                        __uint_as_float(ov[4 * e + 2]) * inv, __uint_as_float(ov[4 * e + 3]) * inv);
+                }
+            }
+            if (real) {
+                if (a.num_splits == 1) {
+                    if (a.lse != nullptr) a.lse[(size_t(b) * a.Hq + h) * a.Sq + i_row] = lse2 * 0.69314718055994530942f;
+                } else {
+                    a.lse_part[prow_i] = lse2;
+                }
+            }
+        }
+    }
+
+    // ---- teardown (warps 1..5): every TMEM access and MMA is done; free TMEM
+    tc_fence_before_sync();
+    asm volatile("bar.sync 2, 160;" ::: "memory");
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+}  // namespace gqa

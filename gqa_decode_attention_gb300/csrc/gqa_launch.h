@@ -16,6 +16,10 @@ namespace gqa {
 constexpr int kDenseCfgs = 4;
 inline int dense_cfg_for_rows(int rows) { return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3; }
 inline int dense_cfg_rows(int cfg) { return 16 << cfg; }
+// Query rows per CTA of the engine serving head dim D: the tcgen05 engine
+// (D = 256) always holds 128 rows (its TMEM lanes); the mma.sync engine holds
+// the group's rows rounded up to 16, at most 128.
+inline int dense_rows_per_cta(int D, int cfg) { return D == 256 ? 128 : dense_cfg_rows(cfg); }
 constexpr int dense_tile_keys(int D, int cfg) {
     return D == 64 ? (cfg == 0 ? 32 : 64) : D == 128 ? (cfg == 0 ? 16 : cfg == 1 ? 32 : 64)
                                                      : (cfg <= 1 ? 16 : cfg == 2 ? 32 : 64);

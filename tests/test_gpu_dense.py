@@ -82,10 +82,11 @@ def test_same_splits_bitwise_repeatable(gq):
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 4), (8, 2), (4, 2), (16, 4), (8, 1), (64, 8), (32, 2)])
 @pytest.mark.parametrize("Sq", [1, 2])
-def test_gqa_bitwise_equals_expanded_mha(gq, Hq, Hkv, Sq):
+@pytest.mark.parametrize("D", [128, 256])
+def test_gqa_bitwise_equals_expanded_mha(gq, Hq, Hkv, Sq, D):
     """Native GQA == the same kernel on K/V pre-expanded to Hq heads, bit for bit
     (split count pinned: the automatic choice depends on B*Hkv)."""
-    B, Skv, D = 2, 700, 128
+    B, Skv = 2, 700
     q, k, v = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=Hq * 100 + Hkv)
     G = Hq // Hkv
     o1, l1 = _run(gq, q, k, v, num_splits=5)
@@ -112,14 +113,15 @@ def test_causal_row0_sees_one_key(gq):
     assert torch.equal(out[:, 0], v[:, 0].repeat_interleave(4, dim=1))
 
 
-def test_short_last_split_fully_masked(gq, orc):
+@pytest.mark.parametrize("D", [128, 256])
+def test_short_last_split_fully_masked(gq, orc, D):
     """The last split holds keys no earlier row may see: its partial LSE is -inf
     and its weight in the combine must be exactly zero (no NaN)."""
     for (Sq, Skv, splits) in [(2, 65, 2), (8, 70, 2), (8, 129, 3), (3, 130, 3)]:
-        q, k, v = gqa_inputs.dense_inputs(1, Sq, Skv, 16, 2, 128, seed=Skv)
+        q, k, v = gqa_inputs.dense_inputs(1, Sq, Skv, 16, 2, D, seed=Skv)
         out, lse = _run(gq, q, k, v, num_splits=splits)
         assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
-        ref_o, ref_l = orc.gqa_decode(q, k, v, 1 / math.sqrt(128))
+        ref_o, ref_l = orc.gqa_decode(q, k, v, 1 / math.sqrt(D))
         assert_o_close(out, ref_o, f"short last split {Sq},{Skv},{splits}")
         assert_lse_close(lse, ref_l)
 
@@ -195,10 +197,11 @@ def test_invalid_args_launch_nothing(gq):
     assert gq.gqa_device_status() == 0
 
 
-def test_wait_timeout_is_reported_not_hung(gq):
+@pytest.mark.parametrize("D", [128, 256])
+def test_wait_timeout_is_reported_not_hung(gq, D):
     """A load that never arrives makes the bounded pipeline wait run out: the
     kernel flags GQA_ERR_DEVICE_TIMEOUT and returns; the context stays usable."""
-    q, k, v = (t.cuda() for t in gqa_inputs.dense_inputs(1, 1, 1000, 8, 2, 128, seed=17))
+    q, k, v = (t.cuda() for t in gqa_inputs.dense_inputs(1, 1, 1000, 8, 2, D, seed=17))
     gq.gqa_set_wait_limit_ns(50_000_000)
     gq.gqa_debug_set_fault_mode(1)
     try:
