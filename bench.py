@@ -541,11 +541,21 @@ def main(argv=None) -> int:
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["gqa", "reference"], default="gqa")
     p.add_argument("--config", default=gqa_inputs.HEADLINE, choices=sorted(gqa_inputs.CONFIGS))
+    p.add_argument("--skv", type=int, default=0,
+                   help="override the KV length of a dense configuration (smaller cases for profiling)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
+    if args.skv:
+        import dataclasses
+        cfg = gqa_inputs.CONFIGS[args.config]
+        if not isinstance(cfg, gqa_inputs.DenseConfig):
+            p.error("--skv applies to dense configurations only")
+        name = f"{cfg.name}@skv{args.skv}"
+        gqa_inputs.CONFIGS[name] = dataclasses.replace(cfg, name=name, Skv=args.skv)
+        args.config = name
     if args.impl == "reference":
         return run_reference(args)
     return run_gqa(args)

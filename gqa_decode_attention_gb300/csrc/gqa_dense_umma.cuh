@@ -179,9 +179,10 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t ring_addr = smem_u32(ring);
             const uint32_t p_addr = smem_u32(ps);
             bool ok = true;
-            auto issue_qk = [&](int j) -> bool {
+            // QK(j): the tile must have landed; S[j % 2] is free because the
+            // row threads released it (p_ready) before QK(j - 2)'s successor.
+            auto issue_qk = [&](int j) {
                 const int st = j % C::STAGES;
-                if (!mbar_wait_bounded(&full[st], (j / C::STAGES) & 1, a.wait_limit_ns, abort_flag)) return false;
                 tc_fence_after_sync();
                 const uint32_t kaddr = ring_addr + st * C::STAGE_BYTES;
 #pragma unroll
@@ -191,18 +192,32 @@ __global__ void __launch_bounds__(192, 1)
                     umma_bf16(tbase + C::S_COL + (j & 1) * C::BN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&s_full[j & 1]);
-                return true;
             };
-            if (n_it > 0) ok = issue_qk(0);
+            int qk_issued = 0;  // QK(0 .. qk_issued-1) have been issued
+            if (n_it > 0) {
+                ok = mbar_wait_bounded(&full[0], 0, a.wait_limit_ns, abort_flag);
+                if (ok) {
+                    issue_qk(0);
+                    qk_issued = 1;
+                }
+            }
             for (int j = 0; ok && j < n_it; ++j) {
-                if (j + 1 < n_it && !issue_qk(j + 1)) {
-                    ok = false;
-                    break;
+                // Wait for P(j) while issuing QK(j+1) the moment its tile lands,
+                // so PV(j) never waits on the next tile's copy.
+                const uint64_t t0 = globaltimer_ns();
+                for (uint32_t spin = 1;; ++spin) {
+                    if (qk_issued == j + 1 && j + 1 < n_it &&
+                        mbar_test_wait(&full[(j + 1) % C::STAGES], ((j + 1) / C::STAGES) & 1)) {
+                        issue_qk(j + 1);
+                        qk_issued = j + 2;
+                    }
+                    if (mbar_test_wait(&p_ready[j & 1], (j >> 1) & 1)) break;
+                    if ((spin & 63u) == 0u && (*abort_flag || globaltimer_ns() - t0 > a.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
                 }
-                if (!mbar_wait_bounded(&p_ready[j & 1], (j >> 1) & 1, a.wait_limit_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                if (!ok) break;
                 tc_fence_after_sync();
                 const int st = j % C::STAGES;
                 const uint32_t vaddr = ring_addr + st * C::STAGE_BYTES + C::TILE_BYTES;
@@ -215,6 +230,16 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 umma_commit(o_done);
                 umma_commit(&empty[st]);
+                if (qk_issued == j + 1 && j + 1 < n_it) {
+                    // the next tile was not in yet while P(j) was produced
+                    if (!mbar_wait_bounded(&full[(j + 1) % C::STAGES], ((j + 1) / C::STAGES) & 1, a.wait_limit_ns,
+                                           abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_qk(j + 1);
+                    qk_issued = j + 2;
+                }
             }
             if (!ok) {
                 flag_error(a.err, kErrTimeout);
