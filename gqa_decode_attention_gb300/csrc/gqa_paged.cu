@@ -4,16 +4,26 @@
 
 namespace gqa {
 
-cudaError_t launch_paged_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
+template <int D, int NT>
+static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
+    using C = PagedCfg<D, NT>;
+    auto kern = gqa_paged_fp8_kernel<D, NT>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     const dim3 grid((a.Hkv + kPagedHeadsPerCta - 1) / kPagedHeadsPerCta, a.B);
-    const dim3 block(32 * kPagedHeadsPerCta);
-    if (D == 64)
-        gqa_paged_fp8_kernel<64><<<grid, block, 0, stream>>>(a);
-    else if (D == 128)
-        gqa_paged_fp8_kernel<128><<<grid, block, 0, stream>>>(a);
-    else
-        return cudaErrorInvalidValue;
+    kern<<<grid, 32 * kPagedHeadsPerCta, C::SMEM_BYTES, stream>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_paged_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
+    const bool two = a.G > 8;  // groups of 9..16 rows use two n-tiles of 8 rows
+    if (D == 64) return two ? launch_paged_inst<64, 2>(a, stream) : launch_paged_inst<64, 1>(a, stream);
+    if (D == 128) return two ? launch_paged_inst<128, 2>(a, stream) : launch_paged_inst<128, 1>(a, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_paged_gather(const uint8_t *pool, const int32_t *page_table, const int32_t *topk, uint8_t *out,

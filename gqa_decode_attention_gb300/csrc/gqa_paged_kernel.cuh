@@ -10,26 +10,32 @@
 // (base-2 exponentials), v_scale applied once to the output, then
 // out = sigmoid(gate) * attn.
 //
-// Mapping: one CTA per (request, block of up to 8 KV heads); one warp per KV
-// head owning that head's whole group of G = Hq / Hkv query heads.  Unlike the
-// page's per-warp design, the warp loads each selected K/V row exactly once for
-// the whole group (the page's open problem: its grouped kernels fetched each
-// row once per query head).  Rows are gathered straight into registers in the
-// layout of the tensor-core fragments: K rows as B operands of S = Q K^T (the
-// head dimension is permuted consistently in Q and K, which a dot product
-// allows), V rows byte-interleaved across token pairs as B operands of
-// O = P V.  FP8 codes are widened to f16 with the packed cvt instruction --
-// exact, since every E4M3FN value is an f16 value -- and the MMAs run in f16
-// with fp32 accumulation.  q is converted to f16 per row with a power-of-two
-// row scale (folded back into the score multiplier), so no q value overflows.
+// Mapping: one warp per (request, KV head) owns that head's whole group of
+// G = Hq / Hkv query heads, so each selected K/V row is fetched from HBM once
+// for the group (the page's "Open problem": its grouped kernels requested
+// every row once per query head).  CTAs hold two such warps, so about a
+// thousand small CTAs spread evenly over the SMs.
+//
+// Per 16 selected tokens a warp computes, on the tensor cores in f16 with
+// fp32 accumulation,
+//   S^T[16 tokens x 8 rows] = K[16 x D] . Q^T[D x 8]     (D/16 MMAs)
+//   O^T[D x 8 rows]        += V^T[D x 16] . P^T[16 x 8]  (D/16 MMAs)
+// with the query rows in the MMA's N dimension (8 rows per n-tile), so no
+// accumulator lane is spent on padding rows of the group.  The head
+// dimension is permuted identically in Q and K (a dot product allows it) and
+// the output dimension is mapped back in the epilogue, which lets every lane
+// fetch whole 16-byte pieces of its K / V rows.  Those pieces are staged by
+// cp.async in a lane-private, three-deep shared-memory ring (loads for two
+// steps ahead are always in flight and hold no registers).  FP8 codes are
+// widened to f16 with the packed cvt instruction -- exact, since every E4M3FN
+// value is an f16 value.  q is converted to f16 per row with a power-of-two
+// row scale folded back into the score multiplier, so no q value overflows.
 #pragma once
 
 #include "gqa_common.cuh"
 #include "gqa_params.h"
 
 namespace gqa {
-
-
 
 // Physical pool row (page * page_size + slot) of logical token t of request b,
 // or -1 for padding (t < 0).  Out-of-range entries give -1 and set *bad.
@@ -48,69 +54,80 @@ __device__ __forceinline__ int paged_token_row(const int32_t *page_table, int b,
     return p * page_size + t % page_size;
 }
 
-__device__ __forceinline__ uint4 ldg_stream16(const void *p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint2 ldg_stream8(const void *p) {
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
     return r;
 }
 
-template <int D>
+// cp.async of `bytes` (16 or 8) from global to shared; src_bytes = 0 writes zeros.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, uint32_t src_bytes) {
+    if constexpr (BYTES == 16) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    } else {
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                     : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int D, int NT>
 struct PagedCfg {
     static_assert(D == 64 || D == 128, "paged kernel supports D = 64 or 128");
-    static constexpr int KU = D / 64;       // 16-byte K pieces per lane per token (lane owns D/4 bytes)
-    static constexpr int KSTEPS = D / 16;   // MMA k-steps over the head dimension
-    static constexpr int VB = D / 8;        // V bytes per lane per token
-    static constexpr int DT = D / 8;        // output d-tiles of 8
+    static constexpr int KU = D / 64;        // 16-byte K pieces per lane per token (the lane owns D/4 bytes)
+    static constexpr int KSTEPS = D / 16;    // MMA k-steps over the head dimension
+    static constexpr int VB = D / 8;         // V bytes per lane per token
+    static constexpr int DB = D / 16;        // output d-blocks of 16
+    static constexpr int SLOTS = 2 * KU + 4; // 16-byte smem slots per lane per step
+    static constexpr int STAGES = 3;
+    static constexpr int WARPS = kPagedHeadsPerCta;
+    static constexpr int RING_BYTES = WARPS * STAGES * SLOTS * 32 * 16;
+    static constexpr int ROWS_BYTES = kPagedChunk * 4;
+    static constexpr int SMEM_BYTES = RING_BYTES + ROWS_BYTES;
+    static constexpr int MIN_BLOCKS = NT == 1 ? 8 : 4;
 };
 
-// Lane (n = lane/4, c = lane%4) holds, for k-step kk, head-dimension bytes
-// d0(kk) .. d0(kk)+3 of its K rows, where d0 = (kk/4) * 64 + 16c + 4 (kk%4).
+// Lane (gi = lane/4, c = lane%4) holds, for k-step kk, head-dimension bytes
+// k_dbase(kk, c) .. +3 of its K rows: word kk%4 of its 16-byte piece kk/4,
+// which sits at byte (kk/4) * 64 + 16 c of the row.
 __device__ __forceinline__ int k_dbase(int kk, int c) { return (kk >> 2) * 64 + 16 * c + 4 * (kk & 3); }
 
-template <int D>
-__global__ void __launch_bounds__(32 * kPagedHeadsPerCta, 2) gqa_paged_fp8_kernel(const PagedArgs a) {
-    using C = PagedCfg<D>;
-    __shared__ int rows_s[kPagedChunk];
-    // Q fragments, per warp / k-step / lane (registers are the scarce resource here)
-    __shared__ uint4 qf_s[kPagedHeadsPerCta][C::KSTEPS][32];
+template <int D, int NT>
+__global__ void __launch_bounds__(32 * kPagedHeadsPerCta, PagedCfg<D, NT>::MIN_BLOCKS)
+    gqa_paged_fp8_kernel(const PagedArgs a) {
+    using C = PagedCfg<D, NT>;
+    extern __shared__ uint4 psmem[];
+    int *rows_s = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(psmem) + C::RING_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
-    const int g = blockIdx.x * kPagedHeadsPerCta + warp;
+    const int g = blockIdx.x * C::WARPS + warp;
     const bool active = g < a.Hkv;
-    const int n = lane >> 2;
+    const int gi = lane >> 2;
     const int c = lane & 3;
+    uint4 *ring = psmem + warp * (C::STAGES * C::SLOTS * 32);
+    const uint32_t ring_addr = smem_u32(ring);
 
-    // ---- Q fragments (f16, per-row power-of-two scale), staged in shared memory
-    float alpha_r[2];
-    {
-    uint32_t qf[C::KSTEPS][4];
+    // ---- Q^T fragments (f16, per-row power-of-two scale).  Lane gi holds
+    // query row gi (+8 per n-tile) at head-dim bytes k_dbase(kk, c) .. +3.
+    uint32_t qf[NT][C::KSTEPS][2];
+    float row_alpha[NT];
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int hl = n + 8 * hr;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hl = gi + 8 * nt;
         const bool real = active && hl < a.G;
         float qv[C::KSTEPS][4];
         float mx = 0.f;
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
             if (real) {
-                const __nv_bfloat16 *src = a.q + (size_t(b) * a.Hq + g * a.G + hl) * D + k_dbase(kk, c);
-                const uint2 raw = *reinterpret_cast<const uint2 *>(src);
+                const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + (size_t(b) * a.Hq + g * a.G + hl) * D +
+                                                                   k_dbase(kk, c));
                 qv[kk][0] = __uint_as_float(raw.x << 16);
                 qv[kk][1] = __uint_as_float(raw.x & 0xffff0000u);
                 qv[kk][2] = __uint_as_float(raw.y << 16);
@@ -123,204 +140,216 @@ __global__ void __launch_bounds__(32 * kPagedHeadsPerCta, 2) gqa_paged_fp8_kerne
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504).
-        int ex = 0;
-        if (mx >= 32768.f) ex = ilogbf(mx) - 14;
+        // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504)
+        const int ex = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
         const float down = ldexpf(1.f, -ex);
-        alpha_r[hr] = a.alpha * ldexpf(1.f, ex);
+        row_alpha[nt] = a.alpha * ldexpf(1.f, ex);
 #pragma unroll
         for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            qf[kk][hr] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);      // k = 2c, 2c+1
-            qf[kk][2 + hr] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+            qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
+            qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
         }
     }
+    // score multipliers of the rows this lane holds in S^T: 8 nt + 2c + e
+    float alpha_s[NT][2];
 #pragma unroll
-    for (int kk = 0; kk < C::KSTEPS; ++kk) qf_s[warp][kk][lane] = make_uint4(qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-    }
-    __syncwarp();
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) alpha_s[nt][e] = __shfl_sync(0xffffffffu, row_alpha[nt], 4 * (2 * c + e));
 
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
-    float o[C::DT][4];
+    float m_run[NT][2], l_run[NT][2];
+    float o[NT][C::DB][4];
 #pragma unroll
-    for (int nt = 0; nt < C::DT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+        for (int t = 0; t < C::DB; ++t) o[nt][t][0] = o[nt][t][1] = o[nt][t][2] = o[nt][t][3] = 0.f;
+    }
 
     const size_t head_off = size_t(active ? g : 0) * D;
     const size_t row_stride = size_t(a.Hkv) * D;
     bool bad = false;
 
-    for (int base = 0; base < a.topk_n; base += kPagedChunk) {
-        const int cn = min(kPagedChunk, a.topk_n - base);
+    // Issue the cp.async copies of step s (16 tokens from s*16) into ring stage st.
+    auto issue = [&](int s, int cn, int st) {
+        const uint32_t base = ring_addr + uint32_t(st * C::SLOTS * 32 + lane) * 16u;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // K rows of tokens gi and gi + 8
+            const int k = s * 16 + gi + 8 * j;
+            const int row = k < cn ? rows_s[k] : -1;
+            const uint8_t *src = a.k_pool + (row >= 0 ? size_t(row) * row_stride + head_off : 0);
+#pragma unroll
+            for (int u = 0; u < C::KU; ++u)
+                cp_async<16>(base + uint32_t((j * C::KU + u) * 32) * 16u, src + u * 64 + 16 * c, row >= 0 ? 16u : 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // V rows of tokens 2c, 2c+1, 2c+8, 2c+9
+            const int k = s * 16 + 2 * c + (j & 1) + 8 * (j >> 1);
+            const int row = k < cn ? rows_s[k] : -1;
+            const uint8_t *src = a.v_pool + (row >= 0 ? size_t(row) * row_stride + head_off : 0);
+            cp_async<C::VB>(base + uint32_t((2 * C::KU + j) * 32) * 16u, src + C::VB * gi, row >= 0 ? uint32_t(C::VB) : 0u);
+        }
+    };
+
+    for (int base_k = 0; base_k < a.topk_n; base_k += kPagedChunk) {
+        const int cn = min(kPagedChunk, a.topk_n - base_k);
         __syncthreads();  // previous chunk fully consumed
         for (int k = threadIdx.x; k < cn; k += blockDim.x) {
-            const int t = __ldg(a.topk + size_t(b) * a.topk_n + base + k);
+            const int t = __ldg(a.topk + size_t(b) * a.topk_n + base_k + k);
             rows_s[k] = paged_token_row(a.page_table, b, a.pages_per_req, a.page_size, a.num_pages, t, &bad);
         }
         __syncthreads();
         if (!active) continue;
+        const int steps = (cn + 15) / 16;
+#pragma unroll
+        for (int s = 0; s < C::STAGES - 1; ++s) {
+            if (s < steps) issue(s, cn, s);
+            cp_async_commit();
+        }
+        for (int s = 0; s < steps; ++s) {
+            cp_async_wait<C::STAGES - 2>();  // this lane's copies of step s have landed
+            if (s + C::STAGES - 1 < steps) issue(s + C::STAGES - 1, cn, (s + C::STAGES - 1) % C::STAGES);
+            cp_async_commit();
+            const uint4 *slot = ring + (s % C::STAGES) * C::SLOTS * 32 + lane;
 
-        for (int s0 = 0; s0 < cn; s0 += 16) {
-            // ---- gather K rows (tokens n and n+8 of this step) and V rows
-            // (tokens 2c, 2c+1, 2c+8, 2c+9) straight into registers
-            int krow[2], vrow[4];
+            // token validity of the two tokens this lane holds in S^T (gi, gi + 8)
+            bool tv[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int k = s0 + n + 8 * j;
-                krow[j] = k < cn ? rows_s[k] : -1;
+                const int k = s * 16 + gi + 8 * j;
+                tv[j] = k < cn && rows_s[k] >= 0;
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int k = s0 + 2 * c + (j & 1) + 8 * (j >> 1);
-                vrow[j] = k < cn ? rows_s[k] : -1;
-            }
+
+            // ---- S^T = K . Q^T
             uint4 kr[2][C::KU];
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int u = 0; u < C::KU; ++u) {
-                    if (krow[j] >= 0)
-                        kr[j][u] = ldg_stream16(a.k_pool + size_t(krow[j]) * row_stride + head_off + u * 64 + 16 * c);
-                    else
-                        kr[j][u] = make_uint4(0, 0, 0, 0);
-                }
-            uint32_t vr[4][C::VB / 4];
+                for (int u = 0; u < C::KU; ++u) kr[j][u] = slot[(j * C::KU + u) * 32];
+            float st_[NT][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if constexpr (C::VB == 16) {
-                    uint4 x = make_uint4(0, 0, 0, 0);
-                    if (vrow[j] >= 0) x = ldg_stream16(a.v_pool + size_t(vrow[j]) * row_stride + head_off + C::VB * n);
-                    vr[j][0] = x.x;
-                    vr[j][1] = x.y;
-                    vr[j][2] = x.z;
-                    vr[j][3] = x.w;
-                } else {
-                    uint2 x = make_uint2(0, 0);
-                    if (vrow[j] >= 0) x = ldg_stream8(a.v_pool + size_t(vrow[j]) * row_stride + head_off + C::VB * n);
-                    vr[j][0] = x.x;
-                    vr[j][1] = x.y;
-                }
-            }
-
-            // ---- S = Q K^T  (16 query rows x 16 tokens)
-            float s[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            for (int nt = 0; nt < NT; ++nt) st_[nt][0] = st_[nt][1] = st_[nt][2] = st_[nt][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                const uint4 qv4 = qf_s[warp][kk][lane];
-                const uint32_t qa[4] = {qv4.x, qv4.y, qv4.z, qv4.w};
+                const int u = kk >> 2, w = kk & 3;
+                const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
+                const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
+                const uint32_t af[4] = {e4m3x2_to_f16x2(uint16_t(w0 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(w1 & 0xffffu)),
+                                        e4m3x2_to_f16x2(uint16_t(w0 >> 16)), e4m3x2_to_f16x2(uint16_t(w1 >> 16))};
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint4 &x = kr[nt][kk >> 2];
-                    const uint32_t w = (kk & 3) == 0 ? x.x : (kk & 3) == 1 ? x.y : (kk & 3) == 2 ? x.z : x.w;
-                    const uint32_t b0 = e4m3x2_to_f16x2(uint16_t(w & 0xffffu));
-                    const uint32_t b1 = e4m3x2_to_f16x2(uint16_t(w >> 16));
-                    mma_f16_16816(s[nt], qa, b0, b1);
+                for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
+            }
+
+            // ---- online softmax over the 16 tokens, rows 8 nt + 2c + e
+            uint32_t pb[NT][2];
+            float corr[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float pv[4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float t0 = tv[0] ? st_[nt][e] * alpha_s[nt][e] : -INFINITY;
+                    const float t1 = tv[1] ? st_[nt][2 + e] * alpha_s[nt][e] : -INFINITY;
+                    float mx = fmaxf(t0, t1);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    const float m_new = fmaxf(m_run[nt][e], mx);
+                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                    corr[nt][e] = fast_exp2(m_run[nt][e] - m_use);
+                    m_run[nt][e] = m_new;
+                    pv[e] = fast_exp2(t0 - m_use);
+                    pv[2 + e] = fast_exp2(t1 - m_use);
+                    l_run[nt][e] = l_run[nt][e] * corr[nt][e] + pv[e] + pv[2 + e];
+                }
+                // P^T B fragments: b0 = rows gi at tokens 2c, 2c+1; b1 = tokens 2c+8, 2c+9.
+                const uint32_t pk_lo = pack_f16x2(pv[0], pv[1]);  // token gi,     rows 2c, 2c+1
+                const uint32_t pk_hi = pack_f16x2(pv[2], pv[3]);  // token gi + 8, rows 2c, 2c+1
+                const int src0 = 4 * (2 * c) + (gi >> 1), src1 = 4 * (2 * c + 1) + (gi >> 1);
+                const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;
+                pb[nt][0] = prmt(__shfl_sync(0xffffffffu, pk_lo, src0), __shfl_sync(0xffffffffu, pk_lo, src1), sel);
+                pb[nt][1] = prmt(__shfl_sync(0xffffffffu, pk_hi, src0), __shfl_sync(0xffffffffu, pk_hi, src1), sel);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int t = 0; t < C::DB; ++t) {
+                    o[nt][t][0] *= corr[nt][0];
+                    o[nt][t][1] *= corr[nt][1];
+                    o[nt][t][2] *= corr[nt][0];
+                    o[nt][t][3] *= corr[nt][1];
+                }
+
+            // ---- O^T += V^T . P^T.  d-block t: rows m = gi (byte 2t) and gi + 8
+            // (byte 2t + 1) of the lane's VB-byte piece, tokens 2c, 2c+1 (a0, a1)
+            // and 2c+8, 2c+9 (a2, a3).
+            uint32_t vw[4][C::VB / 4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 x = slot[(2 * C::KU + j) * 32];
+                vw[j][0] = x.x;
+                vw[j][1] = x.y;
+                if constexpr (C::VB == 16) {
+                    vw[j][2] = x.z;
+                    vw[j][3] = x.w;
                 }
             }
-
-            // ---- mask padding, online softmax (base 2)
-            float corr[2];
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int k = s0 + nt * 8 + 2 * c + e;
-                        const bool valid = k < cn && rows_s[k] >= 0;
-                        float t = valid ? s[nt][2 * hr + e] * alpha_r[hr] : -INFINITY;
-                        s[nt][2 * hr + e] = t;
-                        mx = fmaxf(mx, t);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float m_new = fmaxf(m_run[hr], mx);
-                const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                corr[hr] = fast_exp2(m_run[hr] - m_use);
-                m_run[hr] = m_new;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) s[nt][2 * hr + e] = fast_exp2(s[nt][2 * hr + e] - m_use);
-            }
-            // P in f16 as the A operand; the normaliser sums the fp32 weights.
-            uint32_t pf[4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                pf[nt * 2 + 0] = pack_f16x2(s[nt][0], s[nt][1]);
-                pf[nt * 2 + 1] = pack_f16x2(s[nt][2], s[nt][3]);
-            }
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr)
-                l_run[hr] = l_run[hr] * corr[hr] + (s[0][2 * hr] + s[0][2 * hr + 1] + s[1][2 * hr] + s[1][2 * hr + 1]);
-#pragma unroll
-            for (int nt = 0; nt < C::DT; ++nt) {
-                o[nt][0] *= corr[0];
-                o[nt][1] *= corr[0];
-                o[nt][2] *= corr[1];
-                o[nt][3] *= corr[1];
-            }
-
-            // ---- O += P V.  B fragment of d-tile t: b0 = (tok 2c, tok 2c+1),
-            // b1 = (tok 2c+8, tok 2c+9) at head-dim byte n * VB + t.
 #pragma unroll
             for (int w = 0; w < C::VB / 4; ++w) {
-                const uint32_t ab01 = prmt(vr[0][w], vr[1][w], 0x5140u);  // bytes 0,1 of tok 2c / 2c+1
-                const uint32_t ab23 = prmt(vr[0][w], vr[1][w], 0x7362u);  // bytes 2,3
-                const uint32_t cd01 = prmt(vr[2][w], vr[3][w], 0x5140u);
-                const uint32_t cd23 = prmt(vr[2][w], vr[3][w], 0x7362u);
-                mma_f16_16816(o[4 * w + 0], pf, e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)),
-                              e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)));
-                mma_f16_16816(o[4 * w + 1], pf, e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
-                              e4m3x2_to_f16x2(uint16_t(cd01 >> 16)));
-                mma_f16_16816(o[4 * w + 2], pf, e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)),
-                              e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)));
-                mma_f16_16816(o[4 * w + 3], pf, e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
-                              e4m3x2_to_f16x2(uint16_t(cd23 >> 16)));
+                const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
+                const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
+                const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
+                const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
+                const uint32_t a_t0[4] = {e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
+                                          e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd01 >> 16))};
+                const uint32_t a_t1[4] = {e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
+                                          e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd23 >> 16))};
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);
+                    mma_f16_16816(o[nt][2 * w + 1], a_t1, pb[nt][0], pb[nt][1]);
+                }
             }
         }
+        cp_async_wait<0>();
     }
     if (bad) flag_error(a.err, kErrIndex);
     if (!active) return;
 
-    // ---- epilogue: v_scale, normalise, sigmoid gate, bf16
+    // ---- epilogue: v_scale, normalise, sigmoid gate, bf16.  Lane holds rows
+    // 8 nt + 2c + e at head-dim bytes VB*gi .. VB*gi + VB-1 (d-block t:
+    // 2t from o[t][e], 2t + 1 from o[t][2 + e]).
 #pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
-        l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
-    }
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-        const int hl = n + 8 * hr;
-        if (hl >= a.G) continue;
-        const int h = g * a.G + hl;
-        const float L = l_run[hr];
-        const float f = L > 0.f ? a.v_scale / L : 0.f;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            // d = (2c + e) * DT + t for d-tiles t = 0 .. DT-1: one contiguous run
-            const int d0 = (2 * c + e) * C::DT;
-            const size_t off = (size_t(b) * a.Hq + h) * D + d0;
-            uint32_t packed[C::DT / 2];
+            float L = l_run[nt][e];
+            L += __shfl_xor_sync(0xffffffffu, L, 4);
+            L += __shfl_xor_sync(0xffffffffu, L, 8);
+            L += __shfl_xor_sync(0xffffffffu, L, 16);
+            const int hl = 8 * nt + 2 * c + e;
+            if (hl >= a.G) continue;
+            const int h = g * a.G + hl;
+            const float f = L > 0.f ? a.v_scale / L : 0.f;
+            const size_t off = (size_t(b) * a.Hq + h) * D + C::VB * gi;
+            uint32_t packed[C::VB / 2];
 #pragma unroll
-            for (int t = 0; t < C::DT; t += 2) {
-                const uint32_t graw = *reinterpret_cast<const uint32_t *>(a.gate + off + t);
+            for (int t = 0; t < C::DB; ++t) {
+                const uint32_t graw = *reinterpret_cast<const uint32_t *>(a.gate + off + 2 * t);
                 const float g0 = __uint_as_float(graw << 16);
                 const float g1 = __uint_as_float(graw & 0xffff0000u);
                 const float s0 = 1.f / (1.f + __expf(-g0));
                 const float s1 = 1.f / (1.f + __expf(-g1));
-                packed[t / 2] = pack_bf16x2(o[t][2 * hr + e] * f * s0, o[t + 1][2 * hr + e] * f * s1);
+                packed[t] = pack_bf16x2(o[nt][t][e] * f * s0, o[nt][t][2 + e] * f * s1);
             }
 #pragma unroll
-            for (int t = 0; t < C::DT / 2; t += 4)
+            for (int t = 0; t < C::VB / 2; t += 4)
                 *reinterpret_cast<uint4 *>(a.out + off + 2 * t) =
                     make_uint4(packed[t], packed[t + 1], packed[t + 2], packed[t + 3]);
+            if (a.lse != nullptr && gi == 0)
+                a.lse[size_t(b) * a.Hq + h] = L > 0.f ? (m_run[nt][e] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
         }
-        if (a.lse != nullptr && c == 0)
-            a.lse[size_t(b) * a.Hq + h] = L > 0.f ? (m_run[hr] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
-    }
 }
 
 // Test hook: byte copy of the selected rows through the kernel's own index map.

@@ -17,7 +17,7 @@ enum : unsigned {
 // of this many keys.
 constexpr int kSplitKeys = 64;
 // KV heads (one warp each) per CTA of the paged kernel.
-constexpr int kPagedHeadsPerCta = 8;
+constexpr int kPagedHeadsPerCta = 2;
 // Top-K entries whose rows are resolved per pass of the paged kernel.
 constexpr int kPagedChunk = 512;
 
