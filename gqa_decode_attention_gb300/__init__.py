@@ -15,7 +15,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgqa_decode.so")
+# GQA_DECODE_LIB selects another build of the library (for example a tuning build).
+LIB_PATH = os.environ.get("GQA_DECODE_LIB") or os.path.join(_HERE, "libgqa_decode.so")
 
 STATUS = {
     0: "GQA_OK",

@@ -35,28 +35,41 @@
 
 namespace gqa {
 
+// Keys per tile of the tcgen05 engine; a compile-time knob for tuning builds.
+#ifndef GQA_UMMA_TILE_KEYS
+#define GQA_UMMA_TILE_KEYS 64
+#endif
+
 template <int D>
 struct UmmaCfg {
-    static constexpr int BM = 128;  // query rows per CTA (TMEM lanes)
-    static constexpr int BN = 64;   // keys per tile
+    static constexpr int BM = 128;                  // query rows per CTA (TMEM lanes)
+    static constexpr int BN = GQA_UMMA_TILE_KEYS;   // keys per tile (32 or 64)
     static constexpr int CHUNKS = D / 64;
-    static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;  // K or V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int P_BYTES = BM * BN * 2;
+    static constexpr int P_BYTES = BM * 128;  // P rows use one 128-byte swizzle row (BN <= 64 keys)
     static constexpr int BUDGET = 227 * 1024 - 1024 - 256;
-    static constexpr int STAGES_FIT = (BUDGET - Q_BYTES - 2 * P_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
-    static constexpr int RING_OFF = Q_BYTES;
+    static constexpr int STAGES_FIT = (BUDGET - 2 * P_BYTES) / STAGE_BYTES;
+#ifndef GQA_UMMA_MAX_STAGES
+#define GQA_UMMA_MAX_STAGES 4
+#endif
+    static constexpr int STAGES = STAGES_FIT > GQA_UMMA_MAX_STAGES ? GQA_UMMA_MAX_STAGES : STAGES_FIT;
+    static constexpr int RING_OFF = 0;
     static constexpr int P_OFF = RING_OFF + STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
     static constexpr int THREADS = 192;
-    static constexpr uint32_t S_COL = 0;     // two 64-column score buffers
-    static constexpr uint32_t O_COL = 128;   // D columns of fp32 output
-    static constexpr uint32_t TMEM_COLS = (O_COL + D) <= 256 ? 256 : 512;
-    static constexpr float kRescaleLog2 = 8.f;
+    static constexpr uint32_t S_COL = 0;            // two BN-column score buffers
+    static constexpr uint32_t O_COL = 2 * BN;       // D columns of fp32 output
+    static constexpr uint32_t Q_COL = O_COL + D;    // the CTA's queries, D/2 columns (A operand of QK)
+    static constexpr uint32_t TMEM_COLS = (Q_COL + D / 2) <= 256 ? 256 : 512;
+    static_assert(Q_COL + D / 2 <= 512, "TMEM budget");
+#ifndef GQA_UMMA_RESCALE_LOG2
+#define GQA_UMMA_RESCALE_LOG2 8.f
+#endif
+    static constexpr float kRescaleLog2 = GQA_UMMA_RESCALE_LOG2;
     static_assert(STAGES >= 2, "ring needs two stages");
+    static_assert(BN == 32 || BN == 64, "tile keys");
     static_assert(D % 64 == 0 && D <= 256, "head dim");
 };
 
@@ -67,7 +80,6 @@ __global__ void __launch_bounds__(192, 1)
     using C = UmmaCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *qs = smem;
     uint8_t *ring = smem + C::RING_OFF;
     uint8_t *ps = smem + C::P_OFF;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
@@ -76,7 +88,8 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *p_ready = s_full + 2;        // [2]
     uint64_t *o_done = p_ready + 2;        // [1]
     uint64_t *fin = o_done + 1;            // [1]
-    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(fin + 1);
+    uint64_t *q_ready = fin + 1;           // [1]
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(q_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_s + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -100,27 +113,11 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(o_done, 1);
         mbar_init(fin, 1);
+        mbar_init(q_ready, 128);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_base_s, C::TMEM_COLS);
-    if (warp >= 2) {
-        // Stage the CTA's query rows (K-major, 128-byte swizzle, chunk-major).
-        const int t = threadIdx.x - 64;
-        for (int idx = t; idx < C::BM * (D / 8); idx += 128) {
-            const int lr = idx / (D / 8);
-            const int u = idx % (D / 8);
-            const int r = rg * C::BM + lr;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (r < a.Mq) {
-                const int i = r / a.G;
-                const int h = g * a.G + (r % a.G);
-                val = *reinterpret_cast<const uint4 *>(a.q + ((size_t(b) * a.Sq + i) * a.Hq + h) * D + u * 8);
-            }
-            *reinterpret_cast<uint4 *>(qs + (u >> 3) * (C::BM * 128) + swz128(lr, u & 7)) = val;
-        }
-        fence_proxy_async_shared();  // generic-proxy writes -> tensor-core reads
-    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -175,7 +172,6 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_bf16_f32(C::BM, C::BN, false, false);
             const uint32_t idesc_pv = idesc_bf16_f32(C::BM, D, false, true);
-            const uint32_t q_addr = smem_u32(qs);
             const uint32_t ring_addr = smem_u32(ring);
             const uint32_t p_addr = smem_u32(ps);
             bool ok = true;
@@ -187,14 +183,15 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t kaddr = ring_addr + st * C::STAGE_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t ad = smem_desc_sw128(q_addr + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t bd = smem_desc_sw128(kaddr + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tbase + C::S_COL + (j & 1) * C::BN, ad, bd, idesc_qk, kk > 0 ? 1u : 0u);
+                    umma_bf16_ta(tbase + C::S_COL + (j & 1) * C::BN, tbase + C::Q_COL + kk * 8, bd, idesc_qk,
+                                 kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&s_full[j & 1]);
             };
             int qk_issued = 0;  // QK(0 .. qk_issued-1) have been issued
-            if (n_it > 0) {
+            ok = mbar_wait_bounded(q_ready, 0, a.wait_limit_ns, abort_flag);  // Q is in TMEM
+            if (ok && n_it > 0) {
                 ok = mbar_wait_bounded(&full[0], 0, a.wait_limit_ns, abort_flag);
                 if (ok) {
                     issue_qk(0);
@@ -259,6 +256,28 @@ __global__ void __launch_bounds__(192, 1)
         const int kmax = a.Skv - a.Sq + i_row;  // last visible key (bottom-right causal)
         const int mask_from = a.Skv - a.Sq;
         const uint32_t lane_base = tbase + (uint32_t(quarter * 32) << 16);
+        // This thread's query row -> its TMEM lane, columns Q_COL.. (zeros past Mq).
+        {
+            const __nv_bfloat16 *qrow =
+                a.q + ((size_t(b) * a.Sq + i_row) * a.Hq + g * a.G + (r < a.Mq ? r % a.G : 0)) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 x = r < a.Mq ? *reinterpret_cast<const uint4 *>(qrow + c * 64 + e * 8)
+                                             : make_uint4(0, 0, 0, 0);
+                    qv[4 * e] = x.x;
+                    qv[4 * e + 1] = x.y;
+                    qv[4 * e + 2] = x.z;
+                    qv[4 * e + 3] = x.w;
+                }
+                tmem_st32(lane_base + C::Q_COL + c * 32, qv);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(q_ready);
+        }
         float m_ref = -INFINITY;  // reference maximum (log2 domain)
         float l = 0.f;
         bool failed = false;
@@ -275,16 +294,16 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc_fence_after_sync();
-            uint32_t sr[2][32];
-            tmem_ld32(lane_base + C::S_COL + sb * C::BN, sr[0]);
-            tmem_ld32(lane_base + C::S_COL + sb * C::BN + 32, sr[1]);
+            uint32_t sr[C::BN / 32][32];
+#pragma unroll
+            for (int h = 0; h < C::BN / 32; ++h) tmem_ld32(lane_base + C::S_COL + sb * C::BN + h * 32, sr[h]);
             tmem_wait_ld();
 
             const int key0 = key_begin + j * C::BN;
             const bool need_mask = key0 + C::BN - 1 > mask_from;
             float mx = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < C::BN / 32; ++h)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     float t = __uint_as_float(sr[h][c]) * a.alpha;
@@ -297,7 +316,9 @@ __global__ void __launch_bounds__(192, 1)
             const bool renew = mx > m_ref + C::kRescaleLog2;
             const bool rescale = renew && l > 0.f;
             if (__any_sync(0xffffffffu, rescale)) {
-                // PV(j-1) must have finished writing O
+                // PV(j-1) must have finished writing O.  Unambiguous: S(j) was
+                // committed after QK(j), which was issued after PV(j-2), so at
+                // least j-1 PV phases are complete when this thread gets here.
                 const bool od = mbar_wait_bounded(o_done, (j - 1) & 1, a.wait_limit_ns, abort_flag);
                 if (!__all_sync(0xffffffffu, od)) {
                     failed = true;
@@ -323,7 +344,7 @@ __global__ void __launch_bounds__(192, 1)
             uint8_t *prow = prow_base + sb * C::P_BYTES;
             float psum = 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < C::BN / 8; ++u) {
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -348,7 +369,11 @@ __global__ void __launch_bounds__(192, 1)
         pdl_launch_dependents();
         bool have_o = false;
         if (!failed && n_it > 0) {
-            const bool od = mbar_wait_bounded(o_done, (n_it - 1) & 1, a.wait_limit_ns, abort_flag) && !*abort_flag;
+            // All MMAs done: `fin` completes once, after the issuer's last PV.  (Waiting
+            // on o_done's parity here would be ambiguous: when QK(j+1) is issued
+            // before PV(j), the row threads can reach this point two PV phases
+            // ahead of o_done, and a parity wait cannot tell phase n-1 from n-3.)
+            const bool od = mbar_wait_bounded(fin, 0, a.wait_limit_ns, abort_flag) && !*abort_flag;
             have_o = __all_sync(0xffffffffu, od);
             if (!have_o) {
                 flag_error(a.err, kErrTimeout);

@@ -20,12 +20,20 @@ inline int dense_cfg_rows(int cfg) { return 16 << cfg; }
 // (D = 256) always holds 128 rows (its TMEM lanes); the mma.sync engine holds
 // the group's rows rounded up to 16, at most 128.
 inline int dense_rows_per_cta(int D, int cfg) { return D == 256 ? 128 : dense_cfg_rows(cfg); }
+// Tile keys and ring depth of the 16-row instance at D = 128 (the decode
+// shape with the most traffic); compile-time knobs for tuning builds.
+#ifndef GQA_D128_R16_TILE
+#define GQA_D128_R16_TILE 16
+#endif
+#ifndef GQA_D128_R16_STAGES
+#define GQA_D128_R16_STAGES 3
+#endif
 constexpr int dense_tile_keys(int D, int cfg) {
-    return D == 64 ? (cfg == 0 ? 32 : 64) : D == 128 ? (cfg == 0 ? 16 : cfg == 1 ? 32 : 64)
+    return D == 64 ? (cfg == 0 ? 32 : 64) : D == 128 ? (cfg == 0 ? GQA_D128_R16_TILE : cfg == 1 ? 32 : 64)
                                                      : (cfg <= 1 ? 16 : cfg == 2 ? 32 : 64);
 }
 constexpr int dense_stages(int D, int cfg) {
-    return D == 64 ? (cfg <= 1 ? 3 : 4) : D == 128 ? 3 : (cfg == 1 ? 4 : cfg == 3 ? 2 : 3);
+    return D == 64 ? (cfg <= 1 ? 3 : 4) : D == 128 ? (cfg == 0 ? GQA_D128_R16_STAGES : 3) : (cfg == 1 ? 4 : cfg == 3 ? 2 : 3);
 }
 
 struct DenseLaunch {
