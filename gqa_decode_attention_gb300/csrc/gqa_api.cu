@@ -463,6 +463,8 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     a.topk_n = topk;
     a.alpha = resolve_scale(scale, D) * k_scale * 1.4426950408889634f;
     a.v_scale = v_scale;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.fault_mode = g_fault_mode.load();
     int dev = 0;
     if (!current_device(&dev)) return GQA_ERR_CUDA;
     a.err = error_word(dev);

@@ -109,6 +109,14 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// Contiguous bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_dst),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

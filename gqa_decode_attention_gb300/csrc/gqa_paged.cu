@@ -4,25 +4,47 @@
 
 namespace gqa {
 
-template <int D, int NT>
+template <int D, int NT, int HB>
 static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
-    using C = PagedCfg<D, NT>;
-    auto kern = gqa_paged_fp8_kernel<D, NT>;
+    using C = PagedCfg<D, NT, HB>;
+    auto kern = gqa_paged_fp8_kernel<D, NT, HB>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    const dim3 grid((a.Hkv + kPagedHeadsPerCta - 1) / kPagedHeadsPerCta, a.B);
-    kern<<<grid, 32 * kPagedHeadsPerCta, C::SMEM_BYTES, stream>>>(a);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the CTAs may be scheduled while the
+    // previous kernel in the stream drains; they wait for it before reading.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.Hkv + HB - 1) / HB, a.B);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Heads per CTA: the smallest power of two covering the KV heads, at most 8
+// (4 when each consumer holds two n-tiles of query rows).
+template <int D, int NT>
+static cudaError_t launch_paged_nt(const PagedArgs &a, cudaStream_t stream) {
+    const int cap = NT == 2 ? 4 : 8;
+    const int want = a.Hkv < cap ? a.Hkv : cap;
+    if (want <= 1) return launch_paged_inst<D, NT, 1>(a, stream);
+    if (want <= 2) return launch_paged_inst<D, NT, 2>(a, stream);
+    if (want <= 4 || NT == 2) return launch_paged_inst<D, NT, 4>(a, stream);
+    return launch_paged_inst<D, NT, (NT == 2 ? 4 : 8)>(a, stream);
 }
 
 cudaError_t launch_paged_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
     const bool two = a.G > 8;  // groups of 9..16 rows use two n-tiles of 8 rows
-    if (D == 64) return two ? launch_paged_inst<64, 2>(a, stream) : launch_paged_inst<64, 1>(a, stream);
-    if (D == 128) return two ? launch_paged_inst<128, 2>(a, stream) : launch_paged_inst<128, 1>(a, stream);
+    if (D == 64) return two ? launch_paged_nt<64, 2>(a, stream) : launch_paged_nt<64, 1>(a, stream);
+    if (D == 128) return two ? launch_paged_nt<128, 2>(a, stream) : launch_paged_nt<128, 1>(a, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -10,26 +10,30 @@
 // (base-2 exponentials), v_scale applied once to the output, then
 // out = sigmoid(gate) * attn.
 //
-// Mapping: one warp per (request, KV head) owns that head's whole group of
-// G = Hq / Hkv query heads, so each selected K/V row is fetched from HBM once
-// for the group (the page's "Open problem": its grouped kernels requested
-// every row once per query head).  CTAs hold two such warps, so about a
-// thousand small CTAs spread evenly over the SMs.
+// Mapping: a CTA serves one request and a block of up to eight KV heads, one
+// consumer warp per head; each consumer owns its head's whole group of
+// G = Hq / Hkv query heads, so every selected K/V row is fetched from HBM
+// once for the group (the page's "Open problem": its grouped kernels
+// requested every row once per query head).  A producer warp gathers the
+// selected token rows: per token one bulk asynchronous copy of the block's
+// contiguous K piece (heads x D bytes) and one of its V piece, into a ring
+// of shared-memory stages of 16 tokens completed on mbarriers.  The copy
+// engine moves whole row pieces, so the streaming rate does not depend on
+// per-lane load issue, and the ring's rows are padded so every fragment read
+// below is free of bank conflicts.
 //
-// Per 16 selected tokens a warp computes, on the tensor cores in f16 with
-// fp32 accumulation,
+// Per 16 selected tokens a consumer computes, on the tensor cores in f16
+// with fp32 accumulation,
 //   S^T[16 tokens x 8 rows] = K[16 x D] . Q^T[D x 8]     (D/16 MMAs)
 //   O^T[D x 8 rows]        += V^T[D x 16] . P^T[16 x 8]  (D/16 MMAs)
 // with the query rows in the MMA's N dimension (8 rows per n-tile), so no
 // accumulator lane is spent on padding rows of the group.  The head
 // dimension is permuted identically in Q and K (a dot product allows it) and
 // the output dimension is mapped back in the epilogue, which lets every lane
-// fetch whole 16-byte pieces of its K / V rows.  Those pieces are staged by
-// cp.async in a lane-private, three-deep shared-memory ring (loads for two
-// steps ahead are always in flight and hold no registers).  FP8 codes are
-// widened to f16 with the packed cvt instruction -- exact, since every E4M3FN
-// value is an f16 value.  q is converted to f16 per row with a power-of-two
-// row scale folded back into the score multiplier, so no q value overflows.
+// read whole 16-byte pieces of its K / V rows.  FP8 codes are widened to f16
+// with the packed cvt instruction -- exact, since every E4M3FN value is an
+// f16 value.  q is converted to f16 per row with a power-of-two row scale
+// folded back into the score multiplier, so no q value overflows.
 #pragma once
 
 #include "gqa_common.cuh"
@@ -60,35 +64,33 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// cp.async of `bytes` (16 or 8) from global to shared; src_bytes = 0 writes zeros.
-template <int BYTES>
-__device__ __forceinline__ void cp_async(uint32_t dst, const void *src, uint32_t src_bytes) {
-    if constexpr (BYTES == 16) {
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                     : "memory");
-    } else {
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-                     : "memory");
-    }
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-template <int D, int NT>
+template <int D, int NT, int HB>
 struct PagedCfg {
     static_assert(D == 64 || D == 128, "paged kernel supports D = 64 or 128");
+    static_assert(HB >= 1 && HB <= kPagedMaxHeadsPerCta, "heads per CTA");
+    static constexpr int T = kPagedStageTokens;
     static constexpr int KU = D / 64;        // 16-byte K pieces per lane per token (the lane owns D/4 bytes)
     static constexpr int KSTEPS = D / 16;    // MMA k-steps over the head dimension
     static constexpr int VB = D / 8;         // V bytes per lane per token
     static constexpr int DB = D / 16;        // output d-blocks of 16
-    static constexpr int SLOTS = 2 * KU + 4; // 16-byte smem slots per lane per step
-    static constexpr int STAGES = 3;
-    static constexpr int WARPS = kPagedHeadsPerCta;
-    static constexpr int RING_BYTES = WARPS * STAGES * SLOTS * 32 * 16;
-    static constexpr int ROWS_BYTES = kPagedChunk * 4;
-    static constexpr int SMEM_BYTES = RING_BYTES + ROWS_BYTES;
-    static constexpr int MIN_BLOCKS = NT == 1 ? 8 : 4;
+    static constexpr int PIECE = HB * D;     // bytes of a token row the CTA copies (its heads)
+    // Row strides in the ring.  K: rows gi and gi + 1 of a quarter-warp must
+    // sit 16 banks apart (stride = 64 mod 128 bytes); V: rows 2c of a
+    // quarter-warp must sit 8 banks apart (stride = 16 mod 128 bytes).
+    static constexpr int KRS = PIECE + 64;
+    static constexpr int VRS = PIECE + 16;
+    static constexpr int STAGE_BYTES = T * (KRS + VRS);
+    static constexpr int STAGES = (96 * 1024) / STAGE_BYTES < 3 ? 3 : ((96 * 1024) / STAGE_BYTES > 8 ? 8 : (96 * 1024) / STAGE_BYTES);
+    static constexpr int WARPS = HB + 1;     // HB consumers, then the producer
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int BAR_OFF = STAGES * STAGE_BYTES;             // full[STAGES], empty[STAGES]
+    static constexpr int MASK_OFF = BAR_OFF + 2 * STAGES * 8;        // valid-token mask per stage
+    static constexpr int FLAG_OFF = MASK_OFF + STAGES * 4;           // abort flag
+    static constexpr int ROWS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;   // physical rows of the chunk
+    static constexpr int SMEM_BYTES = ROWS_OFF + kPagedChunk * 4;
+    static constexpr int IPT = (kPagedChunk + THREADS - 1) / THREADS;  // index-map entries per thread
+    static constexpr int MIN_BLOCKS = (220 * 1024) / (SMEM_BYTES + 1024) < 1 ? 1 : ((220 * 1024) / (SMEM_BYTES + 1024) > 8 ? 8 : (220 * 1024) / (SMEM_BYTES + 1024));
+    static_assert(STAGE_BYTES % 16 == 0 && KRS % 16 == 0 && VRS % 16 == 0, "bulk copy alignment");
 };
 
 // Lane (gi = lane/4, c = lane%4) holds, for k-step kk, head-dimension bytes
@@ -96,230 +98,313 @@ struct PagedCfg {
 // which sits at byte (kk/4) * 64 + 16 c of the row.
 __device__ __forceinline__ int k_dbase(int kk, int c) { return (kk >> 2) * 64 + 16 * c + 4 * (kk & 3); }
 
-template <int D, int NT>
-__global__ void __launch_bounds__(32 * kPagedHeadsPerCta, PagedCfg<D, NT>::MIN_BLOCKS)
+template <int D, int NT, int HB>
+__global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, HB>::MIN_BLOCKS)
     gqa_paged_fp8_kernel(const PagedArgs a) {
-    using C = PagedCfg<D, NT>;
-    extern __shared__ uint4 psmem[];
-    int *rows_s = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(psmem) + C::RING_BYTES);
+    using C = PagedCfg<D, NT, HB>;
+    extern __shared__ __align__(128) uint8_t psmem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(psmem + C::BAR_OFF);
+    uint64_t *empty = full + C::STAGES;
+    uint32_t *vmask = reinterpret_cast<uint32_t *>(psmem + C::MASK_OFF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(psmem + C::FLAG_OFF);
+    int *rows_s = reinterpret_cast<int *>(psmem + C::ROWS_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
-    const int g = blockIdx.x * C::WARPS + warp;
-    const bool active = g < a.Hkv;
+    const int hb0 = blockIdx.x * HB;
+    const int nh = min(HB, a.Hkv - hb0);  // heads of this CTA
+    const bool producer = warp == HB;
+    const int g = hb0 + warp;
+    const bool active = !producer && warp < nh;
     const int gi = lane >> 2;
     const int c = lane & 3;
-    uint4 *ring = psmem + warp * (C::STAGES * C::SLOTS * 32);
-    const uint32_t ring_addr = smem_u32(ring);
+    const uint32_t ring_addr = smem_u32(psmem);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            mbar_init(full + st, 1);
+            mbar_init(empty + st, nh);
+        }
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    pdl_wait_primary();  // inputs may be written by the previous kernel in the stream
 
     // ---- Q^T fragments (f16, per-row power-of-two scale).  Lane gi holds
     // query row gi (+8 per n-tile) at head-dim bytes k_dbase(kk, c) .. +3.
     uint32_t qf[NT][C::KSTEPS][2];
-    float row_alpha[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int hl = gi + 8 * nt;
-        const bool real = active && hl < a.G;
-        float qv[C::KSTEPS][4];
-        float mx = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            if (real) {
-                const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + (size_t(b) * a.Hq + g * a.G + hl) * D +
-                                                                   k_dbase(kk, c));
-                qv[kk][0] = __uint_as_float(raw.x << 16);
-                qv[kk][1] = __uint_as_float(raw.x & 0xffff0000u);
-                qv[kk][2] = __uint_as_float(raw.y << 16);
-                qv[kk][3] = __uint_as_float(raw.y & 0xffff0000u);
-            } else {
-                qv[kk][0] = qv[kk][1] = qv[kk][2] = qv[kk][3] = 0.f;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(qv[kk][e]));
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504)
-        const int ex = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
-        const float down = ldexpf(1.f, -ex);
-        row_alpha[nt] = a.alpha * ldexpf(1.f, ex);
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS; ++kk) {
-            qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
-            qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
-        }
-    }
-    // score multipliers of the rows this lane holds in S^T: 8 nt + 2c + e
     float alpha_s[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) alpha_s[nt][e] = __shfl_sync(0xffffffffu, row_alpha[nt], 4 * (2 * c + e));
-
     float m_run[NT][2], l_run[NT][2];
     float o[NT][C::DB][4];
+    if (!producer) {
+        float row_alpha[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
-        l_run[nt][0] = l_run[nt][1] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hl = gi + 8 * nt;
+            const bool real = active && hl < a.G;
+            float qv[C::KSTEPS][4];
+            float mx = 0.f;
 #pragma unroll
-        for (int t = 0; t < C::DB; ++t) o[nt][t][0] = o[nt][t][1] = o[nt][t][2] = o[nt][t][3] = 0.f;
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                if (real) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + (size_t(b) * a.Hq + g * a.G + hl) * D +
+                                                                       k_dbase(kk, c));
+                    qv[kk][0] = __uint_as_float(raw.x << 16);
+                    qv[kk][1] = __uint_as_float(raw.x & 0xffff0000u);
+                    qv[kk][2] = __uint_as_float(raw.y << 16);
+                    qv[kk][3] = __uint_as_float(raw.y & 0xffff0000u);
+                } else {
+                    qv[kk][0] = qv[kk][1] = qv[kk][2] = qv[kk][3] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(qv[kk][e]));
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504)
+            const int ex = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
+            const float down = ldexpf(1.f, -ex);
+            row_alpha[nt] = a.alpha * ldexpf(1.f, ex);
+#pragma unroll
+            for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
+                qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+            }
+        }
+        // score multipliers of the rows this lane holds in S^T: 8 nt + 2c + e
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) alpha_s[nt][e] = __shfl_sync(0xffffffffu, row_alpha[nt], 4 * (2 * c + e));
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m_run[nt][0] = m_run[nt][1] = -INFINITY;
+            l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+            for (int t = 0; t < C::DB; ++t) o[nt][t][0] = o[nt][t][1] = o[nt][t][2] = o[nt][t][3] = 0.f;
+        }
     }
 
-    const size_t head_off = size_t(active ? g : 0) * D;
-    const size_t row_stride = size_t(a.Hkv) * D;
+    const size_t row_bytes = size_t(a.Hkv) * D;
+    const uint32_t piece = uint32_t(nh) * D;
     bool bad = false;
-
-    // Issue the cp.async copies of step s (16 tokens from s*16) into ring stage st.
-    auto issue = [&](int s, int cn, int st) {
-        const uint32_t base = ring_addr + uint32_t(st * C::SLOTS * 32 + lane) * 16u;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {  // K rows of tokens gi and gi + 8
-            const int k = s * 16 + gi + 8 * j;
-            const int row = k < cn ? rows_s[k] : -1;
-            const uint8_t *src = a.k_pool + (row >= 0 ? size_t(row) * row_stride + head_off : 0);
-#pragma unroll
-            for (int u = 0; u < C::KU; ++u)
-                cp_async<16>(base + uint32_t((j * C::KU + u) * 32) * 16u, src + u * 64 + 16 * c, row >= 0 ? 16u : 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {  // V rows of tokens 2c, 2c+1, 2c+8, 2c+9
-            const int k = s * 16 + 2 * c + (j & 1) + 8 * (j >> 1);
-            const int row = k < cn ? rows_s[k] : -1;
-            const uint8_t *src = a.v_pool + (row >= 0 ? size_t(row) * row_stride + head_off : 0);
-            cp_async<C::VB>(base + uint32_t((2 * C::KU + j) * 32) * 16u, src + C::VB * gi, row >= 0 ? uint32_t(C::VB) : 0u);
-        }
-    };
+    bool failed = false;
+    int gs0 = 0;     // global step index of the chunk's first step (mbarrier phases)
+    int issued = 0;  // producer: steps issued so far (all of 0 .. issued-1)
 
     for (int base_k = 0; base_k < a.topk_n; base_k += kPagedChunk) {
         const int cn = min(kPagedChunk, a.topk_n - base_k);
-        __syncthreads();  // previous chunk fully consumed
-        for (int k = threadIdx.x; k < cn; k += blockDim.x) {
-            const int t = __ldg(a.topk + size_t(b) * a.topk_n + base_k + k);
-            rows_s[k] = paged_token_row(a.page_table, b, a.pages_per_req, a.page_size, a.num_pages, t, &bad);
+        __syncthreads();  // previous chunk fully consumed (and, first time, barriers initialised)
+        if (*abort_flag) break;
+        // Index map, batched so each thread has all its top-K loads and then
+        // all its page-table loads in flight together.
+        int tk[C::IPT];
+#pragma unroll
+        for (int u = 0; u < C::IPT; ++u) {
+            const int k = threadIdx.x + u * C::THREADS;
+            tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + base_k + k) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < C::IPT; ++u) {
+            const int k = threadIdx.x + u * C::THREADS;
+            const int row = paged_token_row(a.page_table, b, a.pages_per_req, a.page_size, a.num_pages, tk[u], &bad);
+            if (k < cn) rows_s[k] = row;
         }
         __syncthreads();
-        if (!active) continue;
-        const int steps = (cn + 15) / 16;
-#pragma unroll
-        for (int s = 0; s < C::STAGES - 1; ++s) {
-            if (s < steps) issue(s, cn, s);
-            cp_async_commit();
-        }
-        for (int s = 0; s < steps; ++s) {
-            cp_async_wait<C::STAGES - 2>();  // this lane's copies of step s have landed
-            if (s + C::STAGES - 1 < steps) issue(s + C::STAGES - 1, cn, (s + C::STAGES - 1) % C::STAGES);
-            cp_async_commit();
-            const uint4 *slot = ring + (s % C::STAGES) * C::SLOTS * 32 + lane;
+        const int steps = (cn + C::T - 1) / C::T;
 
-            // token validity of the two tokens this lane holds in S^T (gi, gi + 8)
-            bool tv[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int k = s * 16 + gi + 8 * j;
-                tv[j] = k < cn && rows_s[k] >= 0;
-            }
-
-            // ---- S^T = K . Q^T
-            uint4 kr[2][C::KU];
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int u = 0; u < C::KU; ++u) kr[j][u] = slot[(j * C::KU + u) * 32];
-            float st_[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) st_[nt][0] = st_[nt][1] = st_[nt][2] = st_[nt][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                const int u = kk >> 2, w = kk & 3;
-                const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
-                const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
-                const uint32_t af[4] = {e4m3x2_to_f16x2(uint16_t(w0 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(w1 & 0xffffu)),
-                                        e4m3x2_to_f16x2(uint16_t(w0 >> 16)), e4m3x2_to_f16x2(uint16_t(w1 >> 16))};
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
-            }
-
-            // ---- online softmax over the 16 tokens, rows 8 nt + 2c + e
-            uint32_t pb[NT][2];
-            float corr[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float pv[4];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float t0 = tv[0] ? st_[nt][e] * alpha_s[nt][e] : -INFINITY;
-                    const float t1 = tv[1] ? st_[nt][2 + e] * alpha_s[nt][e] : -INFINITY;
-                    float mx = fmaxf(t0, t1);
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m_run[nt][e], mx);
-                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                    corr[nt][e] = fast_exp2(m_run[nt][e] - m_use);
-                    m_run[nt][e] = m_new;
-                    pv[e] = fast_exp2(t0 - m_use);
-                    pv[2 + e] = fast_exp2(t1 - m_use);
-                    l_run[nt][e] = l_run[nt][e] * corr[nt][e] + pv[e] + pv[2 + e];
+        if (producer) {
+            // lanes 0..15 copy the K pieces of the stage's 16 tokens, lanes 16..31 the V pieces
+            const int tok = lane & (C::T - 1);
+            const bool is_v = lane >= C::T;
+            const uint8_t *pool = (is_v ? a.v_pool : a.k_pool) + size_t(hb0) * D;
+            const uint32_t dst_off = is_v ? uint32_t(C::T * C::KRS + tok * C::VRS) : uint32_t(tok * C::KRS);
+            for (int s = 0; s < steps && !failed; ++s) {
+                const int gs = gs0 + s;
+                const int st = gs % C::STAGES;
+                if (gs >= C::STAGES) {
+                    bool ok = true;
+                    if (lane == 0) ok = mbar_wait_bounded(empty + st, ((gs / C::STAGES) - 1) & 1, a.wait_limit_ns, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        failed = true;
+                        break;
+                    }
                 }
-                // P^T B fragments: b0 = rows gi at tokens 2c, 2c+1; b1 = tokens 2c+8, 2c+9.
-                const uint32_t pk_lo = pack_f16x2(pv[0], pv[1]);  // token gi,     rows 2c, 2c+1
-                const uint32_t pk_hi = pack_f16x2(pv[2], pv[3]);  // token gi + 8, rows 2c, 2c+1
-                const int src0 = 4 * (2 * c) + (gi >> 1), src1 = 4 * (2 * c + 1) + (gi >> 1);
-                const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;
-                pb[nt][0] = prmt(__shfl_sync(0xffffffffu, pk_lo, src0), __shfl_sync(0xffffffffu, pk_lo, src1), sel);
-                pb[nt][1] = prmt(__shfl_sync(0xffffffffu, pk_hi, src0), __shfl_sync(0xffffffffu, pk_hi, src1), sel);
+                const int k = s * C::T + tok;
+                const int row = k < cn ? rows_s[k] : -1;
+                const unsigned valid = __ballot_sync(0xffffffffu, row >= 0);
+                issued = gs + 1;
+                if (a.fault_mode == 1 && gs == 0) continue;  // test hook: stage never completes
+                if (lane == 0) {
+                    vmask[st] = valid & 0xffffu;
+                    mbar_arrive_expect_tx(full + st, uint32_t(__popc(valid)) * piece);
+                }
+                __syncwarp();
+                if (row >= 0)
+                    bulk_load(ring_addr + uint32_t(st * C::STAGE_BYTES) + dst_off, pool + size_t(row) * row_bytes,
+                              piece, full + st);
             }
+        } else if (active) {
+            const uint32_t kcol = uint32_t(warp * D);
+            for (int s = 0; s < steps; ++s) {
+                const int gs = gs0 + s;
+                const int st = gs % C::STAGES;
+                const uint32_t okw = mbar_wait_bounded(full + st, (gs / C::STAGES) & 1, a.wait_limit_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, okw)) {
+                    failed = true;
+                    break;
+                }
+                const uint8_t *kst = psmem + st * C::STAGE_BYTES;
+                const uint8_t *vst = kst + C::T * C::KRS;
+                const uint32_t mask = vmask[st];
+
+                // token validity of the two tokens this lane holds in S^T (gi, gi + 8)
+                const bool tv0 = (mask >> gi) & 1u, tv1 = (mask >> (gi + 8)) & 1u;
+
+                // ---- S^T = K . Q^T
+                uint4 kr[2][C::KU];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int t = 0; t < C::DB; ++t) {
-                    o[nt][t][0] *= corr[nt][0];
-                    o[nt][t][1] *= corr[nt][1];
-                    o[nt][t][2] *= corr[nt][0];
-                    o[nt][t][3] *= corr[nt][1];
+                    for (int u = 0; u < C::KU; ++u)
+                        kr[j][u] = *reinterpret_cast<const uint4 *>(kst + (gi + 8 * j) * C::KRS + kcol + u * 64 + 16 * c);
+                float st_[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) st_[nt][0] = st_[nt][1] = st_[nt][2] = st_[nt][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    const int u = kk >> 2, w = kk & 3;
+                    const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
+                    const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
+                    const uint32_t af[4] = {e4m3x2_to_f16x2(uint16_t(w0 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(w1 & 0xffffu)),
+                                            e4m3x2_to_f16x2(uint16_t(w0 >> 16)), e4m3x2_to_f16x2(uint16_t(w1 >> 16))};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
                 }
 
-            // ---- O^T += V^T . P^T.  d-block t: rows m = gi (byte 2t) and gi + 8
-            // (byte 2t + 1) of the lane's VB-byte piece, tokens 2c, 2c+1 (a0, a1)
-            // and 2c+8, 2c+9 (a2, a3).
-            uint32_t vw[4][C::VB / 4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint4 x = slot[(2 * C::KU + j) * 32];
-                vw[j][0] = x.x;
-                vw[j][1] = x.y;
-                if constexpr (C::VB == 16) {
-                    vw[j][2] = x.z;
-                    vw[j][3] = x.w;
-                }
-            }
-#pragma unroll
-            for (int w = 0; w < C::VB / 4; ++w) {
-                const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
-                const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
-                const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
-                const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
-                const uint32_t a_t0[4] = {e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
-                                          e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd01 >> 16))};
-                const uint32_t a_t1[4] = {e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
-                                          e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd23 >> 16))};
+                // ---- online softmax over the 16 tokens, rows 8 nt + 2c + e
+                uint32_t pb[NT][2];
+                float corr[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);
-                    mma_f16_16816(o[nt][2 * w + 1], a_t1, pb[nt][0], pb[nt][1]);
+                    float pv[4];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float t0 = tv0 ? st_[nt][e] * alpha_s[nt][e] : -INFINITY;
+                        const float t1 = tv1 ? st_[nt][2 + e] * alpha_s[nt][e] : -INFINITY;
+                        float mx = fmaxf(t0, t1);
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                        const float m_new = fmaxf(m_run[nt][e], mx);
+                        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                        corr[nt][e] = fast_exp2(m_run[nt][e] - m_use);
+                        m_run[nt][e] = m_new;
+                        pv[e] = fast_exp2(t0 - m_use);
+                        pv[2 + e] = fast_exp2(t1 - m_use);
+                        l_run[nt][e] = l_run[nt][e] * corr[nt][e] + pv[e] + pv[2 + e];
+                    }
+                    // P^T B fragments: b0 = rows gi at tokens 2c, 2c+1; b1 = tokens 2c+8, 2c+9.
+                    const uint32_t pk_lo = pack_f16x2(pv[0], pv[1]);  // token gi,     rows 2c, 2c+1
+                    const uint32_t pk_hi = pack_f16x2(pv[2], pv[3]);  // token gi + 8, rows 2c, 2c+1
+                    const int src0 = 4 * (2 * c) + (gi >> 1), src1 = 4 * (2 * c + 1) + (gi >> 1);
+                    const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;
+                    pb[nt][0] = prmt(__shfl_sync(0xffffffffu, pk_lo, src0), __shfl_sync(0xffffffffu, pk_lo, src1), sel);
+                    pb[nt][1] = prmt(__shfl_sync(0xffffffffu, pk_hi, src0), __shfl_sync(0xffffffffu, pk_hi, src1), sel);
+                }
+                bool moved = false;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) moved |= corr[nt][0] != 1.f || corr[nt][1] != 1.f;
+                if (__any_sync(0xffffffffu, moved)) {  // a row's running maximum grew: rescale O
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int t = 0; t < C::DB; ++t) {
+                            o[nt][t][0] *= corr[nt][0];
+                            o[nt][t][1] *= corr[nt][1];
+                            o[nt][t][2] *= corr[nt][0];
+                            o[nt][t][3] *= corr[nt][1];
+                        }
+                }
+
+                // ---- O^T += V^T . P^T.  d-block t: rows m = gi (byte 2t) and gi + 8
+                // (byte 2t + 1) of the lane's VB-byte piece, tokens 2c, 2c+1 (a0, a1)
+                // and 2c+8, 2c+9 (a2, a3).  Rows of invalid tokens are zeroed here
+                // (their ring slots hold stale bytes, possibly NaN codes).
+                uint32_t vw[4][C::VB / 4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tkn = 2 * c + (j & 1) + 8 * (j >> 1);
+                    const bool ok = (mask >> tkn) & 1u;
+                    const uint8_t *src = vst + tkn * C::VRS + kcol + C::VB * gi;
+                    if constexpr (C::VB == 16) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(src);
+                        vw[j][0] = ok ? x.x : 0u;
+                        vw[j][1] = ok ? x.y : 0u;
+                        vw[j][2] = ok ? x.z : 0u;
+                        vw[j][3] = ok ? x.w : 0u;
+                    } else {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(src);
+                        vw[j][0] = ok ? x.x : 0u;
+                        vw[j][1] = ok ? x.y : 0u;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + st);  // ring slot free for the producer
+#pragma unroll
+                for (int w = 0; w < C::VB / 4; ++w) {
+                    const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
+                    const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
+                    const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
+                    const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
+                    const uint32_t a_t0[4] = {e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
+                                              e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd01 >> 16))};
+                    const uint32_t a_t1[4] = {e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
+                                              e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd23 >> 16))};
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);
+                        mma_f16_16816(o[nt][2 * w + 1], a_t1, pb[nt][0], pb[nt][1]);
+                    }
                 }
             }
         }
-        cp_async_wait<0>();
+        if (failed && lane == 0) {
+            flag_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
+        gs0 += steps;
     }
     if (bad) flag_error(a.err, kErrIndex);
-    if (!active) return;
+    if (producer) {
+        // Every copy this CTA issued must land before its shared memory is
+        // released; after an abort some may not have been waited for.
+        for (int st = 0; st < C::STAGES && st < issued; ++st) {
+            const int last = st + ((issued - 1 - st) / C::STAGES) * C::STAGES;  // last step issued into st
+            if (a.fault_mode == 1 && last == 0) continue;
+            if (lane == 0 && !mbar_wait_bounded(full + st, (last / C::STAGES) & 1, a.wait_limit_ns, nullptr))
+                flag_error(a.err, kErrTimeout);
+        }
+        return;
+    }
+    if (!active || *abort_flag) return;
 
     // ---- epilogue: v_scale, normalise, sigmoid gate, bf16.  Lane holds rows
     // 8 nt + 2c + e at head-dim bytes VB*gi .. VB*gi + VB-1 (d-block t:
-    // 2t from o[t][e], 2t + 1 from o[t][2 + e]).
+    // 2t from o[t][e], 2t + 1 from o[t][2 + e]).  All gate words are loaded
+    // before the first store so they are in flight together.
+    uint32_t graw[NT][2][C::DB];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int hl = 8 * nt + 2 * c + e;
+            const size_t off = (size_t(b) * a.Hq + g * a.G + hl) * D + C::VB * gi;
+#pragma unroll
+            for (int t = 0; t < C::DB; ++t)
+                graw[nt][e][t] = hl < a.G ? __ldg(reinterpret_cast<const unsigned int *>(a.gate + off + 2 * t)) : 0u;
+        }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -336,9 +421,8 @@ __global__ void __launch_bounds__(32 * kPagedHeadsPerCta, PagedCfg<D, NT>::MIN_B
             uint32_t packed[C::VB / 2];
 #pragma unroll
             for (int t = 0; t < C::DB; ++t) {
-                const uint32_t graw = *reinterpret_cast<const uint32_t *>(a.gate + off + 2 * t);
-                const float g0 = __uint_as_float(graw << 16);
-                const float g1 = __uint_as_float(graw & 0xffff0000u);
+                const float g0 = __uint_as_float(graw[nt][e][t] << 16);
+                const float g1 = __uint_as_float(graw[nt][e][t] & 0xffff0000u);
                 const float s0 = 1.f / (1.f + __expf(-g0));
                 const float s1 = 1.f / (1.f + __expf(-g1));
                 packed[t] = pack_bf16x2(o[nt][t][e] * f * s0, o[nt][t][2 + e] * f * s1);

@@ -16,10 +16,12 @@ enum : unsigned {
 // Granule of the dense kernel's KV splits: every split starts at a multiple
 // of this many keys.
 constexpr int kSplitKeys = 64;
-// KV heads (one warp each) per CTA of the paged kernel.
-constexpr int kPagedHeadsPerCta = 2;
+// Most KV heads (one consumer warp each) a CTA of the paged kernel serves.
+constexpr int kPagedMaxHeadsPerCta = 8;
+// Selected tokens per stage of the paged kernel's copy pipeline (one MMA tile).
+constexpr int kPagedStageTokens = 16;
 // Top-K entries whose rows are resolved per pass of the paged kernel.
-constexpr int kPagedChunk = 512;
+constexpr int kPagedChunk = 2048;
 
 struct DenseArgs {
     const __nv_bfloat16 *q;
@@ -47,7 +49,9 @@ struct PagedArgs {
     int B, Hq, Hkv, G, page_size, pages_per_req, num_pages, topk_n;
     float alpha;    // scale * k_scale * log2(e)
     float v_scale;
-    unsigned *err;  // device error word
+    unsigned long long wait_limit_ns;
+    int fault_mode;  // test hook: 1 = the producer never issues the first stage
+    unsigned *err;   // device error word
 };
 
 }  // namespace gqa

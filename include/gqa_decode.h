@@ -214,7 +214,7 @@ gqa_status gqa_fp8_e4m3fn_to_f32(const uint8_t *codes, float *out, int n, gqa_st
 gqa_status gqa_device_status(gqa_stream_t stream);
 
 /* Sets the time limit, in nanoseconds, of every pipeline wait in the dense
- * kernel (default 2e9).  Exceeding it aborts the CTA and flags
+ * and the paged kernels (default 2e9).  Exceeding it aborts the CTA and flags
  * GQA_ERR_DEVICE_TIMEOUT.  0 restores the default.  Affects later launches
  * on all streams. */
 void gqa_set_wait_limit_ns(uint64_t ns);

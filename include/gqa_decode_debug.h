@@ -12,14 +12,17 @@
 extern "C" {
 #endif
 
-/* Fault injection for the dense kernel's bounded pipeline waits.
+/* Fault injection for the bounded pipeline waits of the dense and the paged
+ * kernels.
  * mode 0: normal operation (default).
- * mode 1: the producer never issues the load of each CTA's first KV tile, so
- *         the consumers' wait on it runs out after the configured wait limit
+ * mode 1: the producer never issues the loads of each CTA's first KV tile
+ *         (dense) or first stage of selected rows (paged), so the consumers'
+ *         wait on it runs out after the configured wait limit
  *         (gqa_set_wait_limit_ns); the CTA flags GQA_ERR_DEVICE_TIMEOUT in the
  *         device error word, lets its other loads land, and returns.  Outputs
  *         are then undefined.
- * Affects later gqa_decode / gqa_decode_ex launches on all streams. */
+ * Affects later gqa_decode / gqa_decode_ex / gqa_decode_paged_fp8 launches on
+ * all streams. */
 void gqa_debug_set_fault_mode(int mode);
 
 /* Measurement hook.  When both are non-NULL, every later dense or paged

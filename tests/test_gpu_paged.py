@@ -82,6 +82,10 @@ SMALL = [
     (2, 8, 2, 64, 16, 4, 64, 0), (3, 32, 8, 128, 16, 32, 512, 0), (2, 16, 1, 128, 16, 8, 100, 0),
     (1, 4, 4, 128, 1, 70, 70, 5), (2, 12, 4, 64, 64, 2, 97, 3), (1, 16, 16, 128, 8, 200, 1300, 0),
     (2, 2, 2, 128, 16, 2, 1, 0), (2, 8, 8, 64, 16, 2, 17, 16),
+    # CTAs serving part of a head block: 3 heads of 4, 12 heads as 8 + 4, two n-tiles with 3 heads of 4
+    (2, 6, 3, 128, 16, 4, 50, 2), (2, 96, 12, 64, 16, 4, 60, 0), (2, 48, 3, 128, 16, 8, 120, 2),
+    # more selected entries than one pass of the index map resolves (2048), ragged last pass
+    (1, 8, 2, 64, 16, 170, 2600, 3), (1, 16, 8, 128, 32, 80, 2049, 0),
 ]
 
 
@@ -97,6 +101,26 @@ def test_paged_small_vs_oracle(gq, orc, shape):
     assert_o_close(out, ref_o, f"paged {shape}")
     assert_lse_close(lse, ref_l, f"paged {shape}")
     assert gq.gqa_device_status() == 0
+
+
+def test_wait_timeout_is_reported_not_hung(gq):
+    """The producer withholds each CTA's first stage (test hook): the consumers'
+    bounded waits run out, the kernel returns and flags a timeout, and the
+    context stays usable for the next call."""
+    inp = gqa_inputs.paged_inputs(2, 32, 8, 128, 16, 8, 17, 128, seed=31)
+    d = _cuda(inp)
+    gq.gqa_set_wait_limit_ns(50_000_000)
+    gq.gqa_debug_set_fault_mode(1)
+    try:
+        gq.gqa_decode_paged_fp8(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["page_table"], d["topk"],
+                                d["k_scale"], d["v_scale"])
+        assert gq.gqa_device_status() == 6
+    finally:
+        gq.gqa_debug_set_fault_mode(0)
+        gq.gqa_set_wait_limit_ns(0)
+    out, lse = _paged_run(gq, inp)
+    assert gq.gqa_device_status() == 0
+    assert torch.isfinite(lse).all()
 
 
 def test_all_padding_row(gq):
