@@ -14,7 +14,13 @@ library is benchmarked on):
   size 16, 32 pages per request drawn as a random permutation of a shared
   pool, top-K = 512 token indices per request (a random permutation of its
   tokens), q and gate bf16 N(0, 1), K/V pools FP8 E4M3FN quantised from
-  N(0, 1) with a per-tensor scale amax / 448.
+  N(0, 1) with a per-tensor scale amax / 448;
+* paged decode over whole requests (the serving layout: no top-K, every
+  token of each request up to its own length): q [B, Sq, Hq, D] bf16, K/V
+  pools [num_pages, page_size, Hkv, D] in bf16 (N(0, 1) rounded) or FP8
+  E4M3FN (quantised as above), each request's pages a random permutation of
+  the pool, sequence lengths drawn uniformly from [capacity / 2, capacity]
+  (a length mix), or given.
 """
 from __future__ import annotations
 
@@ -58,6 +64,28 @@ class PagedConfig:
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.D)
+
+
+@dataclasses.dataclass(frozen=True)
+class PagedKVConfig:
+    name: str
+    B: int
+    Sq: int
+    Hq: int
+    Hkv: int
+    D: int
+    page_size: int
+    pages_per_req: int
+    kv_dtype: str  # "bf16" or "fp8"
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def num_pages(self) -> int:
+        return self.B * self.pages_per_req
 
 
 CONFIGS = {
@@ -159,3 +187,44 @@ def paged_inputs(B, Hq, Hkv, D, page_size, pages_per_req, num_pages, topk, seed,
 def paged_config_inputs(cfg: PagedConfig, device="cpu"):
     return paged_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
                         cfg.num_pages, cfg.topk, cfg.seed, device)
+
+
+def paged_kv_inputs(B, Sq, Hq, Hkv, D, page_size, pages_per_req, num_pages, seed, kv_dtype="bf16",
+                    seq_lens=None, device="cpu"):
+    """Paged inputs over whole requests.
+
+    Returns dict with q [B,Sq,Hq,D] bf16; k_pool, v_pool [num_pages,
+    page_size, Hkv, D] (bf16, or uint8 E4M3FN codes for kv_dtype "fp8");
+    k_scale, v_scale floats (1.0 for bf16); page_table int32 [B, pages_per_req]
+    (distinct pages from a random permutation of the pool); seq_lens int32 [B]
+    (given, or uniform in [capacity / 2, capacity]).
+    """
+    assert B * pages_per_req <= num_pages and kv_dtype in ("bf16", "fp8")
+    cap = pages_per_req * page_size
+    g = _gen(seed, device)
+    q = _randn_bf16((B, Sq, Hq, D), g, device)
+    shape = (num_pages, page_size, Hkv, D)
+    if kv_dtype == "bf16":
+        k_pool = _randn_bf16(shape, g, device)
+        v_pool = _randn_bf16(shape, g, device)
+        k_scale = v_scale = 1.0
+    else:
+        kx = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        k_pool, k_scale = quantize_e4m3fn(kx)
+        del kx
+        vx = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        v_pool, v_scale = quantize_e4m3fn(vx)
+        del vx
+    perm = torch.randperm(num_pages, generator=g, device=device)[: B * pages_per_req]
+    page_table = perm.view(B, pages_per_req).to(torch.int32).contiguous()
+    if seq_lens is None:
+        lo = max(Sq, cap // 2)
+        seq_lens = torch.randint(lo, cap + 1, (B,), generator=g, device=device, dtype=torch.int64)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32, device=device).contiguous()
+    return dict(q=q, k_pool=k_pool.contiguous(), v_pool=v_pool.contiguous(), k_scale=float(k_scale),
+                v_scale=float(v_scale), page_table=page_table, seq_lens=seq_lens, page_size=page_size)
+
+
+def paged_kv_config_inputs(cfg: PagedKVConfig, device="cpu"):
+    return paged_kv_inputs(cfg.B, cfg.Sq, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
+                           cfg.num_pages, cfg.seed, cfg.kv_dtype, device=device)

@@ -26,6 +26,10 @@ attention):
 * ``gqa_decode_paged_fp8`` -- same page, sections "Workload" and
   "Implementations": attention over the selected tokens with k_scale in the
   scores, v_scale on the values, then a sigmoid gate.
+* ``gqa_decode_paged`` -- the same page-table addressing without a top-K list:
+  every token of each request up to its own sequence length, bf16 or FP8
+  pools, the dense path's bottom-right mask per request (the serving layout
+  both pages leave as an open question).
 """
 from __future__ import annotations
 
@@ -124,6 +128,11 @@ class Oracle:
             _u16_p, _u16_p, _u8_p, _u8_p, _i32_p, _i32_p,
             ctypes.c_double, ctypes.c_double] + [ctypes.c_int] * 8 + [
             ctypes.c_double, _i32_p, ctypes.c_int, _dbl_p, _dbl_p, _dbl_p]
+        lib.oracle_gqa_decode_paged.restype = None
+        lib.oracle_gqa_decode_paged.argtypes = [
+            _u16_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+            _i32_p, _i32_p] + [ctypes.c_int] * 7 + [
+            ctypes.c_double, _i32_p, ctypes.c_int, _dbl_p, _dbl_p]
         self._lib = lib
 
     # -- formats and mapping -------------------------------------------
@@ -213,6 +222,46 @@ class Oracle:
         if rows is not None:
             return out, lse, attn
         return out.reshape(B, Hq, D), lse.reshape(B, Hq), attn.reshape(B, Hq, D)
+
+    # -- paged, whole requests -------------------------------------------
+    def gqa_decode_paged(self, q, k_pool, v_pool, page_table, seq_lens, scale: float,
+                         k_scale: float = 1.0, v_scale: float = 1.0, rows=None):
+        """Paged decode over every token of each request (no top-K).
+
+        q [B,Sq,Hq,D] bf16; pools [num_pages, ps, Hkv, D] of bf16 or E4M3FN
+        codes (uint8 / float8 tensors); page_table [B, ppr] int32; seq_lens [B]
+        int32.  Returns (O, LSE): O [B,Sq,Hq,D] and LSE [B,Hq,Sq] float64, or
+        with ``rows`` (flattened ids (b*Hq + h)*Sq + i) O [n,D] and LSE [n].
+        """
+        qa = _as_u16(q)
+        kv_fp8 = not (hasattr(k_pool, "dtype") and str(k_pool.dtype) in ("torch.bfloat16", "uint16"))
+        if kv_fp8:
+            ka, va = _as_u8(k_pool), _as_u8(v_pool)
+        else:
+            ka, va = _as_u16(k_pool), _as_u16(v_pool)
+        pt, sl = _as_i32(page_table), _as_i32(seq_lens)
+        B, Sq, Hq, D = qa.shape
+        _, ps, Hkv, D2 = ka.shape
+        assert D2 == D and va.shape == ka.shape and sl.shape == (B,)
+        ppr = pt.shape[1]
+        assert int(sl.min(initial=0)) >= 0 and int(sl.max(initial=0)) <= ppr * ps
+        if rows is None:
+            n = B * Hq * Sq
+            rp = None
+        else:
+            ra = _as_i32(np.asarray(rows, dtype=np.int32))
+            n = ra.size
+            rp = _p(ra, _i32_p)
+        out = np.zeros((n, D), dtype=np.float64)
+        lse = np.zeros((n,), dtype=np.float64)
+        self._lib.oracle_gqa_decode_paged(
+            _p(qa, _u16_p), ka.ctypes.data_as(ctypes.c_void_p), va.ctypes.data_as(ctypes.c_void_p),
+            int(kv_fp8), float(k_scale), float(v_scale), _p(pt, _i32_p), _p(sl, _i32_p),
+            B, Sq, Hq, Hkv, D, ps, ppr, float(scale), rp, n, _p(out, _dbl_p), _p(lse, _dbl_p))
+        if rows is not None:
+            return out, lse
+        o = out.reshape(B, Hq, Sq, D).transpose(0, 2, 1, 3).copy()
+        return o, lse.reshape(B, Hq, Sq)
 
 
 _default: Oracle | None = None

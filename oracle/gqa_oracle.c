@@ -19,6 +19,10 @@
  *    k_scale / v_scale (k_scale goes into the score, v_scale onto the
  *    output), scaled dot-product attention over the selected tokens, then a
  *    sigmoid gate on the output.
+ *  - The same page-table addressing without a top-K list (every token of the
+ *    request, up to its own sequence length) is the serving layout the
+ *    kv-copies page's "Open questions" and the FP8 page's "Workload" point
+ *    to; its masking follows the dense rule below, per request.
  *  - The masking rule for S_q > 1 is not printed on the pages; the reading
  *    taken here is bottom-right alignment: query row i of S_q sees keys
  *    j <= S_kv - S_q + i.
@@ -288,6 +292,92 @@ void oracle_gqa_decode_paged_fp8(const uint16_t *q, const uint16_t *gate,
                 if (a)
                     a[d] = acc;
                 o[d] = sig * acc;
+            }
+            if (lse)
+                lse[n] = L;
+        }
+        free(row_at);
+        free(s);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* paged decode over whole requests (no top-K), bf16 or FP8 pools       */
+/* ------------------------------------------------------------------ */
+
+/* Value of element d of pool row `row` (byte offset of the row's first element
+ * divided by the element size): a bf16 pattern, or an E4M3FN code. */
+static double pool_value(const void *pool, int kv_fp8, size_t row, int d)
+{
+    if (kv_fp8)
+        return oracle_e4m3fn_value(((const uint8_t *)pool)[row + d]);
+    return bf16_value(((const uint16_t *)pool)[row + d]);
+}
+
+/*
+ * q : bf16 [B, Sq, Hq, D]
+ * k_pool, v_pool : [num_pages, ps, Hkv, D] of bf16 patterns (kv_fp8 = 0) or
+ *                  E4M3FN codes (kv_fp8 = 1)
+ * page_table : int32 [B, ppr]      seq_lens : int32 [B], 0 <= seq_lens[b] <= ppr*ps
+ * rows : optional list of flattened row ids r = (b*Hq + h)*Sq + i; NULL = all.
+ * out : [n_rows, D] double        lse : [n_rows] double (natural log)
+ *
+ * Request b holds tokens t = 0 .. seq_lens[b]-1, token t at page
+ * page_table[b][t / ps], slot t % ps.  Query row i of Sq sees tokens
+ * t <= seq_lens[b] - Sq + i (bottom-right alignment, as in the dense case).
+ * K^ = val(k) * k_scale, V^ = val(v) * v_scale (pass 1 for bf16 pools),
+ * s_t = scale * q.K^_t, LSE = m + ln sum_t exp(s_t - m),
+ * O = sum_t exp(s_t - LSE) V^_t.  A row that sees no token has O = 0 and
+ * LSE = -inf.
+ */
+void oracle_gqa_decode_paged(const uint16_t *q, const void *k_pool, const void *v_pool, int kv_fp8,
+                             double k_scale, double v_scale,
+                             const int32_t *page_table, const int32_t *seq_lens,
+                             int B, int Sq, int Hq, int Hkv, int D, int ps, int ppr,
+                             double scale, const int32_t *rows, int n_rows,
+                             double *out, double *lse)
+{
+    long cap = (long)ppr * ps;
+    long total = rows ? n_rows : (long)B * Hq * Sq;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
+        size_t *row_at = (size_t *)malloc(sizeof(size_t) * (size_t)(cap > 0 ? cap : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long n = 0; n < total; ++n) {
+            long r = rows ? rows[n] : n;
+            int i = (int)(r % Sq);
+            int h = (int)((r / Sq) % Hq);
+            int b = (int)(r / ((long)Sq * Hq));
+            int g = oracle_kv_head(h, Hq, Hkv);
+            long len = PLANT(11) ? cap : (long)seq_lens[b];
+            long last = last_visible_key(i, Sq, (int)len);
+            double ks = PLANT(12) ? v_scale : k_scale;
+            double vs = PLANT(12) ? k_scale : v_scale;
+            const uint16_t *qrow = q + (((size_t)b * Sq + i) * Hq + h) * D;
+            double m = -INFINITY;
+            for (long t = 0; t <= last && t < len; ++t) {
+                long slot = 0;
+                long p = token_page(page_table, b, ppr, t, ps, &slot);
+                row_at[t] = pool_row(p, slot, g, ps, Hkv, D);
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d)
+                    dot += bf16_value(qrow[d]) * (pool_value(k_pool, kv_fp8, row_at[t], d) * ks);
+                s[t] = scale * dot;
+                if (s[t] > m)
+                    m = s[t];
+            }
+            double sum = 0.0;
+            for (long t = 0; t <= last && t < len; ++t)
+                sum += exp(s[t] - m);
+            double L = (sum > 0.0) ? m + log(sum) : -INFINITY;
+            double *o = out + (size_t)n * D;
+            for (int d = 0; d < D; ++d)
+                o[d] = 0.0;
+            for (long t = 0; t <= last && t < len; ++t) {
+                double w = exp(s[t] - L);
+                for (int d = 0; d < D; ++d)
+                    o[d] += w * (pool_value(v_pool, kv_fp8, row_at[t], d) * vs);
             }
             if (lse)
                 lse[n] = L;

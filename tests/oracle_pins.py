@@ -377,8 +377,85 @@ def pin_gate_and_scales(orc):
     _assert_close(out4, expit(_f64(gate)) * attn4, 1e-15, 1e-15, "sigmoid gate")
 
 
+# ----------------------------------------------------------------------
+# paged decode over whole requests (no top-K)
+# ----------------------------------------------------------------------
+def _logical_cache(pool, pt, lens):
+    """Fancy-index route: request b's cache is its pages in order, cut at its
+    own length.  Returns a list of [len_b, Hkv, D] tensors."""
+    num_pages, ps, Hkv, D = pool.shape
+    B, ppr = pt.shape
+    return [pool[pt[b].long()].reshape(ppr * ps, Hkv, D)[: int(lens[b])] for b in range(B)]
+
+
+def _paged_kv_small(seed, B=3, Sq=2, Hq=8, Hkv=2, D=16, ps=4, ppr=5, lens=(20, 7, 13)):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, Sq, Hq, D), generator=g).to(torch.bfloat16)
+    num_pages = B * ppr + 3
+    kp = torch.randn((num_pages, ps, Hkv, D), generator=g).to(torch.bfloat16)
+    vp = torch.randn((num_pages, ps, Hkv, D), generator=g).to(torch.bfloat16)
+    pt = torch.randperm(num_pages, generator=g)[: B * ppr].view(B, ppr).to(torch.int32).contiguous()
+    sl = torch.tensor(lens, dtype=torch.int32)
+    return q, kp, vp, pt, sl
+
+
+def pin_paged_requests_equal_dense(orc):
+    """Each request of a bf16 paged cache equals the dense oracle run on that
+    request's own logical cache (its pages in table order, cut at its own
+    length), bit for bit, for S_q = 1 and 2 and page sizes 1, 4, 16."""
+    for ci, (Sq, ps, ppr, lens) in enumerate([(2, 4, 5, (20, 7, 13)), (1, 1, 9, (9, 1, 4)), (2, 16, 2, (32, 17, 2))]):
+        q, kp, vp, pt, sl = _paged_kv_small(1700 + ci, Sq=Sq, ps=ps, ppr=ppr, lens=lens)
+        O, L = orc.gqa_decode_paged(q, kp, vp, pt, sl, 0.3)
+        ks, vs = _logical_cache(kp, pt, sl), _logical_cache(vp, pt, sl)
+        for b in range(q.shape[0]):
+            Od, Ld = orc.gqa_decode(q[b:b + 1], ks[b][None], vs[b][None], 0.3)
+            assert np.array_equal(O[b:b + 1], Od), (ci, b)
+            assert np.array_equal(L[b:b + 1], Ld), (ci, b)
+
+
+def pin_paged_fp8_equals_bf16(orc):
+    """An FP8 pool with power-of-two k_scale != v_scale equals a bf16 pool that
+    holds the dequantised values (bf16-exact), bit for bit."""
+    q, _, _, pt, sl = _paged_kv_small(1800)
+    g = torch.Generator().manual_seed(1801)
+    shape = (pt.numel() + 3, 4, 2, 16)
+    k8 = (torch.randn(shape, generator=g) * 40).to(torch.float8_e4m3fn)
+    v8 = (torch.randn(shape, generator=g) * 40).to(torch.float8_e4m3fn)
+    ks, vs = 0.125, 4.0
+    kb = (k8.double() * ks).to(torch.bfloat16)
+    vb = (v8.double() * vs).to(torch.bfloat16)
+    assert torch.equal(kb.double(), k8.double() * ks) and torch.equal(vb.double(), v8.double() * vs)
+    O8, L8 = orc.gqa_decode_paged(q, k8.view(torch.uint8), v8.view(torch.uint8), pt, sl, 0.3, ks, vs)
+    Ob, Lb = orc.gqa_decode_paged(q, kb, vb, pt, sl, 0.3)
+    assert np.array_equal(O8, Ob) and np.array_equal(L8, Lb)
+
+
+def pin_paged_zero_keys_and_short_requests(orc):
+    """K = 0: LSE = ln(#visible tokens) and O = the mean of the visible V rows
+    (numpy over the fancy-indexed cache); a request shorter than S_q leaves its
+    first rows with no visible token: O = 0, LSE = -inf."""
+    q, kp, vp, pt, sl = _paged_kv_small(1900, Sq=3, lens=(20, 2, 0))
+    kz = torch.zeros_like(kp)
+    O, L = orc.gqa_decode_paged(q, kz, vp, pt, sl, 0.3)
+    vs = _logical_cache(vp, pt, sl)
+    B, Sq, Hq, D = q.shape
+    Hkv = kp.shape[2]
+    for b in range(B):
+        for i in range(Sq):
+            n_vis = int(sl[b]) - Sq + i + 1
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                if n_vis <= 0:
+                    assert np.all(O[b, i, h] == 0.0) and np.isneginf(L[b, h, i]), (b, i, h)
+                    continue
+                assert abs(L[b, h, i] - math.log(n_vis)) <= 1e-13
+                mean = _f64(vs[b][:n_vis, g]).mean(axis=0)
+                _assert_close(O[b, i, h], mean, 1e-13, 1e-13, "paged mean of visible V")
+
+
 DENSE_PINS = [pin_bruteforce_dense, pin_library_dense, pin_gqa_equals_expanded_mha, pin_head_map_table,
               pin_zero_keys, pin_constant_v, pin_single_key, pin_zero_scale, pin_hardmax]
 PAGED_PINS = [pin_e4m3fn_table, pin_paged_gather, pin_bruteforce_paged, pin_paged_equals_dense,
               pin_topk_order_and_padding, pin_gate_and_scales]
-ALL_PINS = DENSE_PINS + PAGED_PINS
+PAGED_KV_PINS = [pin_paged_requests_equal_dense, pin_paged_fp8_equals_bf16, pin_paged_zero_keys_and_short_requests]
+ALL_PINS = DENSE_PINS + PAGED_PINS + PAGED_KV_PINS

@@ -5,7 +5,9 @@ suite must reject every one of them.  The mistakes are the ones the pages warn
 about (the two wrong head maps of the kv-copies-gqa head-map table) plus the
 plausible slips in each step: an off-by-one or top-left causal mask, a
 dropped log-sum in the LSE, a dropped softmax scale, page and slot swapped,
-an ungated (identity) gate, the wrong FP8 exponent bias, a dropped v_scale.
+an ungated (identity) gate, the wrong FP8 exponent bias, a dropped v_scale,
+and for whole-request paged decode an ignored sequence length or swapped
+K / V scales.
 """
 import os
 
@@ -25,6 +27,8 @@ MUTANTS = {
     8: "E4M3 exponent bias 8",
     9: "v_scale dropped",
     10: "top-left causal alignment",
+    11: "paged: per-request sequence length ignored",
+    12: "paged: k_scale and v_scale swapped",
 }
 
 
