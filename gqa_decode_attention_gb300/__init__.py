@@ -34,7 +34,8 @@ GQA_OK = 0
 EXPORTS = [
     "gqa_status_string", "gqa_version", "gqa_decode", "gqa_decode_num_splits",
     "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
-    "gqa_decode_host", "gqa_decode_paged_fp8",
+    "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged", "gqa_decode_paged_ex",
+    "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes",
     "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
     "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events",
 ]
@@ -78,6 +79,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.gqa_decode_paged_fp8.restype = st
     lib.gqa_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f, f, vp, vp] + [i] * 8 + [f, vp]
+    lib.gqa_decode_paged.restype = st
+    lib.gqa_decode_paged.argtypes = [vp, vp, vp, i, f, f, vp, vp, vp, vp] + [i] * 8 + [f, vp]
+    lib.gqa_decode_paged_ex.restype = st
+    lib.gqa_decode_paged_ex.argtypes = [vp, vp, vp, i, f, f, vp, vp, vp, vp] + [i] * 8 + [f, i, vp, sz, vp]
+    lib.gqa_decode_paged_num_splits.restype = i
+    lib.gqa_decode_paged_num_splits.argtypes = [i] * 8
+    lib.gqa_decode_paged_workspace_bytes.restype = sz
+    lib.gqa_decode_paged_workspace_bytes.argtypes = [i] * 9
     lib.gqa_paged_gather_fp8.restype = st
     lib.gqa_paged_gather_fp8.argtypes = [vp, vp, vp, vp] + [i] * 7 + [vp]
     lib.gqa_fp8_e4m3fn_to_f32.restype = st
@@ -228,6 +237,61 @@ def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale,
                                   topk_idx.shape[1], _scale_arg(scale), _stream(stream))
     _check(st, "gqa_decode_paged_fp8")
     return out, lse
+
+
+GQA_KV_BF16 = 0
+GQA_KV_FP8_E4M3FN = 1
+
+
+def _kv_dtype(k_pool) -> int:
+    if k_pool.dtype == torch.bfloat16:
+        return GQA_KV_BF16
+    if k_pool.dtype == torch.uint8:
+        return GQA_KV_FP8_E4M3FN
+    raise TypeError(f"k_pool: expected bfloat16 or uint8 (E4M3FN codes), got {k_pool.dtype}")
+
+
+def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_scale=1.0, out=None, lse=None,
+                     scale=None, num_splits=0, workspace=None, stream=None, with_lse=True):
+    """Paged decode over every token of each request (no top-K).
+
+    q [B,Sq,Hq,D] bf16; pools [num_pages, page_size, Hkv, D] of bf16, or of
+    uint8 E4M3FN codes (then k_scale / v_scale apply); page_table int32
+    [B, pages_per_req]; seq_lens int32 [B].  num_splits 0 = automatic;
+    workspace: optional CUDA uint8 tensor of gqa_decode_paged_workspace_bytes.
+    Returns (out [B,Sq,Hq,D] bf16, lse [B,Hq,Sq] fp32 or None).
+    """
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, "cuda")
+    kvd = _kv_dtype(k_pool)
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, n, k_pool.dtype, "cuda")
+    _need(page_table, "page_table", torch.int32, "cuda")
+    _need(seq_lens, "seq_lens", torch.int32, "cuda")
+    B, Sq, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_pool.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = lib.gqa_decode_paged_ex(_ptr(q), _ptr(k_pool), _ptr(v_pool), kvd, float(k_scale), float(v_scale),
+                                 _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D,
+                                 page_size, page_table.shape[1], num_pages, _scale_arg(scale), int(num_splits),
+                                 ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "gqa_decode_paged_ex")
+    return out, lse
+
+
+def gqa_decode_paged_num_splits(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req) -> int:
+    return load_library().gqa_decode_paged_num_splits(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req)
+
+
+def gqa_decode_paged_workspace_bytes(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req, num_splits=0) -> int:
+    return load_library().gqa_decode_paged_workspace_bytes(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req,
+                                                           num_splits)
 
 
 def gqa_paged_gather_fp8(pool, page_table, topk_idx, out=None, stream=None):

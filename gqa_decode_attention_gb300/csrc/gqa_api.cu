@@ -305,7 +305,102 @@ gqa_status check_paged(int B, int Hq, int Hkv, int D, int page_size, int pages_p
     return GQA_OK;
 }
 
+// ------------------------------------------------------------ paged, whole requests
+constexpr int kPagedMinSplitTokens = 256;
+
+struct PagedShape {
+    int B, Sq, Hq, Hkv, D, G, Mq, ps, ppr, num_pages, cap;
+    bool kv8;
+};
+
+gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int page_size, int pages_per_req,
+                          int num_pages, PagedShape *s) {
+    if (B < 1 || Sq < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || pages_per_req < 1 || num_pages < 1)
+        return GQA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+    if (kv_dtype != GQA_KV_BF16 && kv_dtype != GQA_KV_FP8_E4M3FN) return GQA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+    const long G = Hq / Hkv;
+    if (G * Sq > 16) return GQA_ERR_UNSUPPORTED;
+    if (long(pages_per_req) * page_size >= (1L << 31) || long(num_pages) * page_size >= (1L << 31))
+        return GQA_ERR_UNSUPPORTED;
+    if (B > 65535) return GQA_ERR_UNSUPPORTED;
+    s->B = B;
+    s->Sq = Sq;
+    s->Hq = Hq;
+    s->Hkv = Hkv;
+    s->D = D;
+    s->G = int(G);
+    s->Mq = int(G * Sq);
+    s->ps = page_size;
+    s->ppr = pages_per_req;
+    s->num_pages = num_pages;
+    s->cap = pages_per_req * page_size;
+    s->kv8 = kv_dtype == GQA_KV_FP8_E4M3FN;
+    return GQA_OK;
+}
+
+// Resident CTAs per SM of the paged instance serving shape s (cached).
+int paged_occupancy(int dev, const PagedShape &s) {
+    static int cache[kMaxDevices][2][2][2][4];  // [dev][kv8][D][two n-tiles][log2 heads per CTA]
+    const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
+    const int lh = hb == 1 ? 0 : hb == 2 ? 1 : hb == 4 ? 2 : 3;
+    std::lock_guard<std::mutex> lk(g_mu);
+    int &slot = cache[dev][s.kv8][s.D == 128][s.Mq > 8][lh];
+    if (slot == 0) {
+        PagedArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.Hkv = s.Hkv;
+        a.Mq = s.Mq;
+        slot = s.kv8 ? paged_range_ctas_per_sm_fp8(a, s.D) : paged_range_ctas_per_sm_bf16(a, s.D);
+    }
+    return slot;
+}
+
+// Token splits of each request: one wave of resident CTAs when the requests
+// alone do not fill it, every split at least kPagedMinSplitTokens tokens of
+// the table's capacity, then evened out to multiples of 16 tokens.  Returns
+// the split count and sets *tps (tokens per split).
+int choose_paged_splits(const PagedShape &s, int requested, int dev, int *tps) {
+    int S;
+    const int max_s = (s.cap + kPagedMinSplitTokens - 1) / kPagedMinSplitTokens;
+    if (requested > 0) {
+        S = requested;
+    } else {
+        const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
+        const long units = long(s.B) * ((s.Hkv + hb - 1) / hb);
+        const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
+        const long occ = paged_occupancy(dev, s) > 0 ? paged_occupancy(dev, s) : 1;
+        const long slots = nsm * occ;
+        S = units >= slots ? 1 : int(slots / units);
+        if (S > max_s) S = max_s;
+    }
+    const int max_split = (s.cap + 15) / 16;
+    if (S > max_split) S = max_split;
+    if (S > kMaxSplits) S = kMaxSplits;
+    if (S < 1) S = 1;
+    int t = (s.cap + S - 1) / S;
+    t = (t + 15) / 16 * 16;
+    *tps = t;
+    return (s.cap + t - 1) / t;
+}
+
+size_t paged_workspace_bytes(const PagedShape &s, int splits) {
+    if (splits <= 1) return 0;
+    const size_t rows = size_t(s.B) * s.Hkv * s.Mq * splits;
+    return align256(rows * s.D * sizeof(float)) + align256(rows * sizeof(float));
+}
+
 }  // namespace
+
+cudaError_t launch_combine_partials(int D, const float *o_part, const float *lse_part, __nv_bfloat16 *out,
+                                    float *lse, int B, int Sq, int Hq, int Hkv, int G, int Mq, int S,
+                                    cudaStream_t stream) {
+    if (D == 64) return launch_combine_d64(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
+    if (D == 128) return launch_combine_d128(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
+    if (D == 256) return launch_combine_d256(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
+    return cudaErrorInvalidValue;
+}
 
 // K or V as a 4-D tensor (d, kv head, key, batch) with a box of 64 head-dim
 // elements (128 bytes, one swizzle atom) x 1 head x box_keys keys x 1 batch.
@@ -461,6 +556,9 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     a.pages_per_req = pages_per_req;
     a.num_pages = num_pages;
     a.topk_n = topk;
+    a.Sq = 1;
+    a.Mq = a.G;
+    a.num_splits = 1;
     a.alpha = resolve_scale(scale, D) * k_scale * 1.4426950408889634f;
     a.v_scale = v_scale;
     a.wait_limit_ns = g_wait_limit_ns.load();
@@ -471,13 +569,124 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
     if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
-    cudaError_t pe = launch_paged_fp8(a, D, cs);
+    cudaError_t pe = launch_paged_topk_fp8(a, D, cs);
     if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
     if (pe != cudaSuccess) {
         cudaGetLastError();
         return GQA_ERR_CUDA;
     }
     return GQA_OK;
+}
+
+gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_pool, int kv_dtype, float k_scale,
+                               float v_scale, const int32_t *page_table, const int32_t *seq_lens, void *out,
+                               float *lse, int B, int Sq, int Hq, int Hkv, int D, int page_size, int pages_per_req,
+                               int num_pages, float scale, int num_splits, void *workspace,
+                               size_t workspace_bytes_, gqa_stream_t stream) {
+    PagedShape s;
+    gqa_status st = check_paged_kv(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req, num_pages, &s);
+    if (st != GQA_OK) return st;
+    if (num_splits < 0) return GQA_ERR_INVALID_ARG;
+    if (s.kv8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale))) return GQA_ERR_INVALID_ARG;
+    if (q == nullptr || k_pool == nullptr || v_pool == nullptr || page_table == nullptr || seq_lens == nullptr ||
+        out == nullptr)
+        return GQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(page_table, 4) || !aligned(seq_lens, 4))
+        return GQA_ERR_ALIGNMENT;
+    int dev = 0;
+    if (!current_device(&dev)) return GQA_ERR_CUDA;
+    int tps = 0;
+    const int splits = choose_paged_splits(s, num_splits, dev, &tps);
+    if (splits > 65535) return GQA_ERR_UNSUPPORTED;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t need = paged_workspace_bytes(s, splits);
+    void *ws = workspace;
+    bool owned = false;
+    if (need > 0) {
+        if (ws != nullptr) {
+            if (workspace_bytes_ < need) return GQA_ERR_NO_MEMORY;
+            if (!aligned(ws, 256)) return GQA_ERR_ALIGNMENT;
+        } else {
+            if (pool_alloc(&ws, need, dev, cs) != cudaSuccess) {
+                cudaGetLastError();
+                return GQA_ERR_NO_MEMORY;
+            }
+            owned = true;
+        }
+    }
+    PagedArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k_pool = static_cast<const uint8_t *>(k_pool);
+    a.v_pool = static_cast<const uint8_t *>(v_pool);
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    if (need > 0) {
+        const size_t rows = size_t(s.B) * s.Hkv * s.Mq * splits;
+        a.o_part = static_cast<float *>(ws);
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + align256(rows * s.D * sizeof(float)));
+    }
+    a.B = B;
+    a.Sq = Sq;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = s.G;
+    a.Mq = s.Mq;
+    a.page_size = page_size;
+    a.pages_per_req = pages_per_req;
+    a.num_pages = num_pages;
+    a.num_splits = splits;
+    a.tokens_per_split = tps;
+    a.alpha = resolve_scale(scale, D) * (s.kv8 ? k_scale : 1.0f) * 1.4426950408889634f;
+    a.v_scale = s.kv8 ? v_scale : 1.0f;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.fault_mode = g_fault_mode.load();
+    a.err = error_word(dev);
+    cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
+    if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
+    cudaError_t e = s.kv8 ? launch_paged_range_fp8(a, D, cs) : launch_paged_range_bf16(a, D, cs);
+    if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
+    if (e == cudaSuccess && splits > 1)
+        e = launch_combine_partials(D, a.o_part, a.lse_part, a.out, lse, B, Sq, Hq, Hkv, s.G, s.Mq, splits, cs);
+    if (owned) cudaFreeAsync(ws, cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+}
+
+gqa_status gqa_decode_paged(const void *q, const void *k_pool, const void *v_pool, int kv_dtype, float k_scale,
+                            float v_scale, const int32_t *page_table, const int32_t *seq_lens, void *out, float *lse,
+                            int B, int Sq, int Hq, int Hkv, int D, int page_size, int pages_per_req, int num_pages,
+                            float scale, gqa_stream_t stream) {
+    return gqa_decode_paged_ex(q, k_pool, v_pool, kv_dtype, k_scale, v_scale, page_table, seq_lens, out, lse, B, Sq,
+                               Hq, Hkv, D, page_size, pages_per_req, num_pages, scale, 0, nullptr, 0, stream);
+}
+
+int gqa_decode_paged_num_splits(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int page_size,
+                                int pages_per_req) {
+    PagedShape s;
+    gqa_status st = check_paged_kv(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req, 1, &s);
+    if (st != GQA_OK) return -int(st);
+    int dev = 0;
+    if (!current_device(&dev)) return -int(GQA_ERR_CUDA);
+    int tps = 0;
+    return choose_paged_splits(s, 0, dev, &tps);
+}
+
+size_t gqa_decode_paged_workspace_bytes(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int page_size,
+                                        int pages_per_req, int num_splits) {
+    PagedShape s;
+    if (check_paged_kv(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req, 1, &s) != GQA_OK || num_splits < 0)
+        return 0;
+    int dev = 0;
+    if (num_splits == 0 && !current_device(&dev)) return 0;
+    int tps = 0;
+    return paged_workspace_bytes(s, choose_paged_splits(s, num_splits, dev, &tps));
 }
 
 gqa_status gqa_paged_gather_fp8(const uint8_t *pool, const int32_t *page_table, const int32_t *topk_idx, uint8_t *out,

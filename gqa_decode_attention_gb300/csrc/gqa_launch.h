@@ -60,7 +60,34 @@ int dense_ctas_per_sm_d64(int cfg);
 int dense_ctas_per_sm_d128(int cfg);
 int dense_ctas_per_sm_d256(int cfg);
 
-cudaError_t launch_paged_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+// Paged kernel.  Heads per CTA: the smallest power of two covering Hkv, at
+// most the number whose row pieces fit 1 KiB per token (8 FP8 heads of 128,
+// 4 bf16 heads of 128), and at most 4 when a consumer holds two n-tiles.
+inline int paged_heads_per_cta(int D, bool kv8, int Mq, int Hkv) {
+    int cap = 1024 / (D * (kv8 ? 1 : 2));
+    if (cap > 8) cap = 8;
+    if (Mq > 8 && cap > 4) cap = 4;
+    int hb = 1;
+    while (hb < Hkv && hb < cap) hb *= 2;
+    return hb;
+}
+cudaError_t launch_paged_topk_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+cudaError_t launch_paged_range_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+cudaError_t launch_paged_range_bf16(const PagedArgs &a, int D, cudaStream_t stream);
+int paged_range_ctas_per_sm_fp8(const PagedArgs &a, int D);
+int paged_range_ctas_per_sm_bf16(const PagedArgs &a, int D);
+cudaError_t launch_combine_d64(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
+                               int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
+cudaError_t launch_combine_d128(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
+                                int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
+cudaError_t launch_combine_d256(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
+                                int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
+// LSE-weighted combine of fp32 split partials laid out [B*Hkv, Mq, S, D]
+// (and [B*Hkv, Mq, S] log2-domain LSE) into out [B, Sq, Hq, D] bf16 and
+// lse [B, Hq, Sq] (nullable), launched as a programmatic dependent.
+cudaError_t launch_combine_partials(int D, const float *o_part, const float *lse_part, __nv_bfloat16 *out,
+                                    float *lse, int B, int Sq, int Hq, int Hkv, int G, int Mq, int S,
+                                    cudaStream_t stream);
 cudaError_t launch_paged_gather(const uint8_t *pool, const int32_t *page_table, const int32_t *topk, uint8_t *out,
                                 int B, int Hkv, int D, int page_size, int pages_per_req, int num_pages, int topk_n,
                                 unsigned *err, cudaStream_t stream);

@@ -1,51 +1,41 @@
-// gqa_paged.cu -- sparse paged FP8 decode kernel and its test hooks.
-#include "gqa_launch.h"
-#include "gqa_paged_kernel.cuh"
+// gqa_paged.cu -- sparse (top-K) paged FP8 decode kernel and its test hooks.
+#include "gqa_paged_impl.cuh"
 
 namespace gqa {
 
-template <int D, int NT, int HB>
-static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
-    using C = PagedCfg<D, NT, HB>;
-    auto kern = gqa_paged_fp8_kernel<D, NT, HB>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
+// Test hook: byte copy of the selected rows through the kernel's own index map.
+__global__ void gqa_paged_gather_kernel(const uint8_t *pool, const int32_t *page_table, const int32_t *topk,
+                                        uint8_t *out, int Hkv, int D, int page_size, int pages_per_req,
+                                        int num_pages, int topk_n, unsigned *err) {
+    const int k = blockIdx.x;
+    const int b = blockIdx.y;
+    bool bad = false;
+    const int t = topk[size_t(b) * topk_n + k];
+    const int row = paged_token_row(page_table, b, pages_per_req, page_size, num_pages, t, &bad);
+    if (bad && threadIdx.x == 0) flag_error(err, kErrIndex);
+    const int n16 = Hkv * D / 16;
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t(b) * topk_n + k) * Hkv * D);
+    for (int u = threadIdx.x; u < n16; u += blockDim.x) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row >= 0) v = *reinterpret_cast<const uint4 *>(pool + size_t(row) * Hkv * D + size_t(u) * 16);
+        dst[u] = v;
     }
-    // Programmatic dependent launch: the CTAs may be scheduled while the
-    // previous kernel in the stream drains; they wait for it before reading.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.Hkv + HB - 1) / HB, a.B);
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// Heads per CTA: the smallest power of two covering the KV heads, at most 8
-// (4 when each consumer holds two n-tiles of query rows).
-template <int D, int NT>
-static cudaError_t launch_paged_nt(const PagedArgs &a, cudaStream_t stream) {
-    const int cap = NT == 2 ? 4 : 8;
-    const int want = a.Hkv < cap ? a.Hkv : cap;
-    if (want <= 1) return launch_paged_inst<D, NT, 1>(a, stream);
-    if (want <= 2) return launch_paged_inst<D, NT, 2>(a, stream);
-    if (want <= 4 || NT == 2) return launch_paged_inst<D, NT, 4>(a, stream);
-    return launch_paged_inst<D, NT, (NT == 2 ? 4 : 8)>(a, stream);
+// Test hook: the kernel's E4M3FN -> f16 widening, reported as fp32.
+__global__ void gqa_fp8_to_f32_kernel(const uint8_t *codes, float *out, int n) {
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+    if (i >= n) return;
+    const uint16_t two = uint16_t(codes[i]) | (i + 1 < n ? uint16_t(codes[i + 1]) << 8 : uint16_t(0));
+    const uint32_t h2 = e4m3x2_to_f16x2(two);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+    out[i] = f.x;
+    if (i + 1 < n) out[i + 1] = f.y;
 }
 
-cudaError_t launch_paged_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
-    const bool two = a.G > 8;  // groups of 9..16 rows use two n-tiles of 8 rows
-    if (D == 64) return two ? launch_paged_nt<64, 2>(a, stream) : launch_paged_nt<64, 1>(a, stream);
-    if (D == 128) return two ? launch_paged_nt<128, 2>(a, stream) : launch_paged_nt<128, 1>(a, stream);
-    return cudaErrorInvalidValue;
+
+cudaError_t launch_paged_topk_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
+    return cudaError_t(paged_dispatch<true, false>(a, D, stream, 0));
 }
 
 cudaError_t launch_paged_gather(const uint8_t *pool, const int32_t *page_table, const int32_t *topk, uint8_t *out,

@@ -1,0 +1,74 @@
+// gqa_paged_impl.cuh -- launch templates of the paged kernel, shared by the
+// translation units that instantiate its forms (top-K FP8; whole-request FP8;
+// whole-request bf16).
+#pragma once
+
+#include "gqa_launch.h"
+#include "gqa_paged_kernel.cuh"
+
+namespace gqa {
+
+template <int D, int NT, int HB, bool KV8, bool RANGE>
+static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
+    using C = PagedCfg<D, NT, HB, KV8>;
+    auto kern = gqa_paged_kernel<D, NT, HB, KV8, RANGE>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    // Programmatic dependent launch: the CTAs may be scheduled while the
+    // previous kernel in the stream drains; they wait for it before reading.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.Hkv + HB - 1) / HB, a.B, RANGE ? a.num_splits : 1);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <int D, int NT, int HB, bool KV8, bool RANGE>
+static int paged_occupancy_inst() {
+    using C = PagedCfg<D, NT, HB, KV8>;
+    auto kern = gqa_paged_kernel<D, NT, HB, KV8, RANGE>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM_BYTES) != cudaSuccess) return 0;
+    return n;
+}
+
+// Dispatch over (n-tiles, heads per CTA).  op 0 launches, op 1 returns the
+// resident CTAs per SM of the chosen instance (as a cudaError_t-sized int).
+template <int D, int NT, bool KV8, bool RANGE>
+static long paged_dispatch_nt(const PagedArgs &a, cudaStream_t stream, int op) {
+    const int hb = paged_heads_per_cta(D, KV8, a.Mq, a.Hkv);
+#define GQA_PAGED_CASE(HBV)                                                                              \
+    if (hb == HBV)                                                                                       \
+        return op == 0 ? long(launch_paged_inst<D, NT, HBV, KV8, RANGE>(a, stream))                      \
+                       : long(paged_occupancy_inst<D, NT, HBV, KV8, RANGE>());
+    GQA_PAGED_CASE(1)
+    GQA_PAGED_CASE(2)
+    GQA_PAGED_CASE(4)
+    if constexpr (NT == 1 && (KV8 || D == 64)) {
+        GQA_PAGED_CASE(8)
+    }
+#undef GQA_PAGED_CASE
+    return op == 0 ? long(cudaErrorInvalidValue) : 0L;
+}
+
+template <bool KV8, bool RANGE>
+static long paged_dispatch(const PagedArgs &a, int D, cudaStream_t stream, int op) {
+    const bool two = a.Mq > 8;  // 9..16 rows use two n-tiles of 8 rows
+    if (D == 64) return two ? paged_dispatch_nt<64, 2, KV8, RANGE>(a, stream, op) : paged_dispatch_nt<64, 1, KV8, RANGE>(a, stream, op);
+    if (D == 128) return two ? paged_dispatch_nt<128, 2, KV8, RANGE>(a, stream, op) : paged_dispatch_nt<128, 1, KV8, RANGE>(a, stream, op);
+    return op == 0 ? long(cudaErrorInvalidValue) : 0L;
+}
+
+}  // namespace gqa

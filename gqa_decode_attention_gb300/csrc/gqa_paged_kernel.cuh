@@ -1,29 +1,35 @@
-// gqa_paged_kernel.cuh -- sparse paged GQA decode with an FP8 E4M3FN K/V pool
-// and a sigmoid output gate (sm_103a).
+// gqa_paged_kernel.cuh -- paged GQA decode over a shared K/V pool (sm_103a):
+// the sparse top-K form with an FP8 E4M3FN pool and a sigmoid output gate,
+// and the whole-request form (every token of each request up to its own
+// length) over a bf16 or FP8 pool.
 //
-// The operation is the one of "Sparse paged GQA decode attention with FP8 KV
-// cache on SM89", sections "Workload" and "Implementations": per request, a
-// list of top-K logical token indices is mapped through the request's page
-// table (page = table[t / page_size], slot = t % page_size) to rows of a
-// shared FP8 pool; attention runs over those rows only, with k_scale folded
-// into the score multiplier together with the softmax scale and log2(e)
-// (base-2 exponentials), v_scale applied once to the output, then
-// out = sigmoid(gate) * attn.
+// The sparse operation is the one of "Sparse paged GQA decode attention with
+// FP8 KV cache on SM89", sections "Workload" and "Implementations": per
+// request, a list of top-K logical token indices is mapped through the
+// request's page table (page = table[t / page_size], slot = t % page_size) to
+// rows of a shared FP8 pool; attention runs over those rows only, with
+// k_scale folded into the score multiplier together with the softmax scale
+// and log2(e) (base-2 exponentials), v_scale applied once to the output, then
+// out = sigmoid(gate) * attn.  The whole-request form walks tokens
+// 0 .. seq_len-1 of each request through the same page table (the serving
+// layout the pages leave open), masks query row i of S_q to tokens
+// t <= seq_len - S_q + i, and may split a request's tokens over several CTAs
+// whose fp32 partials (O / l, log2-domain LSE) the dense path's combine
+// kernel merges.
 //
-// Mapping: a CTA serves one request and a block of up to eight KV heads, one
-// consumer warp per head; each consumer owns its head's whole group of
-// G = Hq / Hkv query heads, so every selected K/V row is fetched from HBM
-// once for the group (the page's "Open problem": its grouped kernels
+// Mapping: a CTA serves one request (and one token split) and a block of HB
+// KV heads, one consumer warp per head; each consumer owns its head's whole
+// group of G * S_q query rows (at most 16), so every K/V row is fetched from
+// HBM once for the group (the page's "Open problem": its grouped kernels
 // requested every row once per query head).  A producer warp gathers the
-// selected token rows: per token one bulk asynchronous copy of the block's
-// contiguous K piece (heads x D bytes) and one of its V piece, into a ring
-// of shared-memory stages of 16 tokens completed on mbarriers.  The copy
-// engine moves whole row pieces, so the streaming rate does not depend on
-// per-lane load issue, and the ring's rows are padded so every fragment read
-// below is free of bank conflicts.
+// tokens: per token one bulk asynchronous copy of the block's contiguous K
+// piece (HB heads x D elements) and one of its V piece, into a ring of
+// shared-memory stages of 16 tokens completed on mbarriers.  The copy engine
+// moves whole row pieces, and the ring's rows are padded so every fragment
+// read below is free of bank conflicts.
 //
-// Per 16 selected tokens a consumer computes, on the tensor cores in f16
-// with fp32 accumulation,
+// Per 16 tokens a consumer computes, on the tensor cores with fp32
+// accumulation (f16 inputs for FP8 pools, bf16 for bf16 pools),
 //   S^T[16 tokens x 8 rows] = K[16 x D] . Q^T[D x 8]     (D/16 MMAs)
 //   O^T[D x 8 rows]        += V^T[D x 16] . P^T[16 x 8]  (D/16 MMAs)
 // with the query rows in the MMA's N dimension (8 rows per n-tile), so no
@@ -32,8 +38,8 @@
 // the output dimension is mapped back in the epilogue, which lets every lane
 // read whole 16-byte pieces of its K / V rows.  FP8 codes are widened to f16
 // with the packed cvt instruction -- exact, since every E4M3FN value is an
-// f16 value.  q is converted to f16 per row with a power-of-two row scale
-// folded back into the score multiplier, so no q value overflows.
+// f16 value -- and q is converted to f16 per row with a power-of-two row
+// scale folded back into the score multiplier, so no q value overflows.
 #pragma once
 
 #include "gqa_common.cuh"
@@ -64,44 +70,66 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-template <int D, int NT, int HB>
+template <int D, int NT, int HB, bool KV8>
 struct PagedCfg {
     static_assert(D == 64 || D == 128, "paged kernel supports D = 64 or 128");
     static_assert(HB >= 1 && HB <= kPagedMaxHeadsPerCta, "heads per CTA");
     static constexpr int T = kPagedStageTokens;
-    static constexpr int KU = D / 64;        // 16-byte K pieces per lane per token (the lane owns D/4 bytes)
-    static constexpr int KSTEPS = D / 16;    // MMA k-steps over the head dimension
-    static constexpr int VB = D / 8;         // V bytes per lane per token
-    static constexpr int DB = D / 16;        // output d-blocks of 16
-    static constexpr int PIECE = HB * D;     // bytes of a token row the CTA copies (its heads)
+    static constexpr int ELEM = KV8 ? 1 : 2;  // bytes per K/V element
+    static constexpr int ROWB = D * ELEM;     // bytes of one head's row
+    static constexpr int KU = ROWB / 64;      // 16-byte K pieces per lane per token (the lane owns ROWB/4 bytes)
+    static constexpr int KSTEPS = D / 16;     // MMA k-steps over the head dimension
+    static constexpr int VB = D / 8 * ELEM;   // V bytes per lane per token
+    static constexpr int VW = VB / 4;         // V words per lane per token
+    static constexpr int DB = D / 16;         // output d-blocks of 16
+    static constexpr int PIECE = HB * ROWB;   // bytes of a token row the CTA copies (its heads)
     // Row strides in the ring.  K: rows gi and gi + 1 of a quarter-warp must
     // sit 16 banks apart (stride = 64 mod 128 bytes); V: rows 2c of a
-    // quarter-warp must sit 8 banks apart (stride = 16 mod 128 bytes).
+    // quarter-warp must sit 8 banks apart (stride = 16 mod 64 bytes).
     static constexpr int KRS = PIECE + 64;
     static constexpr int VRS = PIECE + 16;
     static constexpr int STAGE_BYTES = T * (KRS + VRS);
-    static constexpr int STAGES = (96 * 1024) / STAGE_BYTES < 3 ? 3 : ((96 * 1024) / STAGE_BYTES > 8 ? 8 : (96 * 1024) / STAGE_BYTES);
-    static constexpr int WARPS = HB + 1;     // HB consumers, then the producer
+    static constexpr int STAGES_FIT = (96 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT < 3 ? 3 : (STAGES_FIT > 8 ? 8 : STAGES_FIT);
+    static constexpr int WARPS = HB + 1;      // HB consumers, then the producer
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;             // full[STAGES], empty[STAGES]
     static constexpr int MASK_OFF = BAR_OFF + 2 * STAGES * 8;        // valid-token mask per stage
     static constexpr int FLAG_OFF = MASK_OFF + STAGES * 4;           // abort flag
-    static constexpr int ROWS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;   // physical rows of the chunk
+    static constexpr int ROWS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;   // physical rows of the pass
     static constexpr int SMEM_BYTES = ROWS_OFF + kPagedChunk * 4;
     static constexpr int IPT = (kPagedChunk + THREADS - 1) / THREADS;  // index-map entries per thread
-    static constexpr int MIN_BLOCKS = (220 * 1024) / (SMEM_BYTES + 1024) < 1 ? 1 : ((220 * 1024) / (SMEM_BYTES + 1024) > 8 ? 8 : (220 * 1024) / (SMEM_BYTES + 1024));
+    static constexpr int MIN_BLOCKS_FIT = (220 * 1024) / (SMEM_BYTES + 1024);
+    static constexpr int MIN_BLOCKS = MIN_BLOCKS_FIT < 1 ? 1 : (MIN_BLOCKS_FIT > 8 ? 8 : MIN_BLOCKS_FIT);
     static_assert(STAGE_BYTES % 16 == 0 && KRS % 16 == 0 && VRS % 16 == 0, "bulk copy alignment");
 };
 
-// Lane (gi = lane/4, c = lane%4) holds, for k-step kk, head-dimension bytes
-// k_dbase(kk, c) .. +3 of its K rows: word kk%4 of its 16-byte piece kk/4,
-// which sits at byte (kk/4) * 64 + 16 c of the row.
-__device__ __forceinline__ int k_dbase(int kk, int c) { return (kk >> 2) * 64 + 16 * c + 4 * (kk & 3); }
+// Head-dimension element where lane (gi, c) holds, for k-step kk, the four
+// elements of its K row that feed the MMA's k = 2c, 2c+1 (first pair) and
+// k = 2c+8, 2c+9 (second pair); Q is loaded at the same elements.
+//  FP8: word kk%4 of the lane's 16-byte piece kk/4, at byte (kk/4)*64 + 16c.
+//  bf16: words 2(kk%2), 2(kk%2)+1 of the lane's piece kk/2, at byte (kk/2)*64 + 16c.
+template <bool KV8>
+__device__ __forceinline__ int k_dbase(int kk, int c) {
+    if constexpr (KV8) return (kk >> 2) * 64 + 16 * c + 4 * (kk & 3);
+    return (kk >> 1) * 32 + 8 * c + 4 * (kk & 1);
+}
 
-template <int D, int NT, int HB>
-__global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, HB>::MIN_BLOCKS)
-    gqa_paged_fp8_kernel(const PagedArgs a) {
-    using C = PagedCfg<D, NT, HB>;
+// Head-dimension element of output d-block t, half `hi` (0: accumulator row
+// gi, 1: row gi + 8) held by lane gi.
+//  FP8: the lane's V piece is bytes VB*gi .. VB*gi + VB-1; block t uses bytes 2t, 2t+1.
+//  bf16: the lane's V words are 16-byte chunks at elements 64m + 8gi; block t
+//  uses word t, i.e. chunk t/4, elements 2(t%4), 2(t%4)+1.
+template <int D, bool KV8>
+__device__ __forceinline__ int out_d(int t, int hi, int gi) {
+    if constexpr (KV8) return (D / 8) * gi + 2 * t + hi;
+    return 64 * (t >> 2) + 8 * gi + 2 * (t & 3) + hi;
+}
+
+template <int D, int NT, int HB, bool KV8, bool RANGE>
+__global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D, NT, HB, KV8>::MIN_BLOCKS)
+    gqa_paged_kernel(const PagedArgs a) {
+    using C = PagedCfg<D, NT, HB, KV8>;
     extern __shared__ __align__(128) uint8_t psmem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(psmem + C::BAR_OFF);
     uint64_t *empty = full + C::STAGES;
@@ -112,6 +140,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
+    const int split = blockIdx.z;
     const int hb0 = blockIdx.x * HB;
     const int nh = min(HB, a.Hkv - hb0);  // heads of this CTA
     const bool producer = warp == HB;
@@ -129,54 +158,91 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
         *abort_flag = 0;
         fence_mbarrier_init();
     }
+    __syncthreads();     // barriers and flag initialised before anyone reads them
     pdl_wait_primary();  // inputs may be written by the previous kernel in the stream
 
-    // ---- Q^T fragments (f16, per-row power-of-two scale).  Lane gi holds
-    // query row gi (+8 per n-tile) at head-dim bytes k_dbase(kk, c) .. +3.
+    // ---- the tokens of this CTA: the top-K list, or the request's own
+    // tokens [t_begin, t_end) of this split.
+    bool bad = false;
+    int n_tok = a.topk_n;
+    int t_begin = 0;
+    int seq_len = 0;
+    if constexpr (RANGE) {
+        seq_len = __ldg(a.seq_lens + b);
+        const int cap = a.pages_per_req * a.page_size;
+        if (seq_len < 0 || seq_len > cap) {
+            bad = true;
+            seq_len = seq_len < 0 ? 0 : cap;
+        }
+        t_begin = split * a.tokens_per_split;
+        n_tok = max(0, min(t_begin + a.tokens_per_split, seq_len) - t_begin);
+    }
+
+    // ---- Q^T fragments.  Lane gi holds query row gi (+8 per n-tile) at the
+    // elements k_dbase(kk, c) .. +3.  FP8 pools: f16 with a per-row
+    // power-of-two scale; bf16 pools: the bf16 values as they are.
     uint32_t qf[NT][C::KSTEPS][2];
     float alpha_s[NT][2];
     float m_run[NT][2], l_run[NT][2];
     float o[NT][C::DB][4];
+    int kmax[NT][2];  // last visible token of the rows this lane holds in S^T (S_q > 1)
     if (!producer) {
         float row_alpha[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int hl = gi + 8 * nt;
-            const bool real = active && hl < a.G;
-            float qv[C::KSTEPS][4];
-            float mx = 0.f;
+            const int r = gi + 8 * nt;  // row r = i * G + hl of the unit
+            const bool real = active && r < a.Mq;
+            const int i = real ? r / a.G : 0;
+            const int hl = real ? r % a.G : 0;
+            const __nv_bfloat16 *qrow = a.q + ((size_t(b) * a.Sq + i) * a.Hq + g * a.G + hl) * D;
+            if constexpr (KV8) {
+                float qv[C::KSTEPS][4];
+                float mx = 0.f;
 #pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                if (real) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(a.q + (size_t(b) * a.Hq + g * a.G + hl) * D +
-                                                                       k_dbase(kk, c));
-                    qv[kk][0] = __uint_as_float(raw.x << 16);
-                    qv[kk][1] = __uint_as_float(raw.x & 0xffff0000u);
-                    qv[kk][2] = __uint_as_float(raw.y << 16);
-                    qv[kk][3] = __uint_as_float(raw.y & 0xffff0000u);
-                } else {
-                    qv[kk][0] = qv[kk][1] = qv[kk][2] = qv[kk][3] = 0.f;
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    if (real) {
+                        const uint2 raw = *reinterpret_cast<const uint2 *>(qrow + k_dbase<KV8>(kk, c));
+                        qv[kk][0] = __uint_as_float(raw.x << 16);
+                        qv[kk][1] = __uint_as_float(raw.x & 0xffff0000u);
+                        qv[kk][2] = __uint_as_float(raw.y << 16);
+                        qv[kk][3] = __uint_as_float(raw.y & 0xffff0000u);
+                    } else {
+                        qv[kk][0] = qv[kk][1] = qv[kk][2] = qv[kk][3] = 0.f;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(qv[kk][e]));
                 }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504)
+                const int ex = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
+                const float down = ldexpf(1.f, -ex);
+                row_alpha[nt] = a.alpha * ldexpf(1.f, ex);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(qv[kk][e]));
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504)
-            const int ex = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
-            const float down = ldexpf(1.f, -ex);
-            row_alpha[nt] = a.alpha * ldexpf(1.f, ex);
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
+                    qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+                }
+            } else {
 #pragma unroll
-            for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
-                qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+                for (int kk = 0; kk < C::KSTEPS; ++kk) {
+                    uint2 raw = make_uint2(0u, 0u);
+                    if (real) raw = *reinterpret_cast<const uint2 *>(qrow + k_dbase<KV8>(kk, c));
+                    qf[nt][kk][0] = raw.x;  // k = 2c, 2c+1
+                    qf[nt][kk][1] = raw.y;  // k = 2c+8, 2c+9
+                }
+                row_alpha[nt] = a.alpha;
             }
         }
-        // score multipliers of the rows this lane holds in S^T: 8 nt + 2c + e
+        // score multipliers and visibility of the rows this lane holds in S^T: 8 nt + 2c + e
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) alpha_s[nt][e] = __shfl_sync(0xffffffffu, row_alpha[nt], 4 * (2 * c + e));
+            for (int e = 0; e < 2; ++e) {
+                alpha_s[nt][e] = __shfl_sync(0xffffffffu, row_alpha[nt], 4 * (2 * c + e));
+                const int r = 8 * nt + 2 * c + e;
+                kmax[nt][e] = seq_len - a.Sq + (r < a.Mq ? r / a.G : 0);
+            }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             m_run[nt][0] = m_run[nt][1] = -INFINITY;
@@ -185,17 +251,17 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
             for (int t = 0; t < C::DB; ++t) o[nt][t][0] = o[nt][t][1] = o[nt][t][2] = o[nt][t][3] = 0.f;
         }
     }
+    const bool causal = RANGE && a.Sq > 1;
 
-    const size_t row_bytes = size_t(a.Hkv) * D;
-    const uint32_t piece = uint32_t(nh) * D;
-    bool bad = false;
+    const size_t row_bytes = size_t(a.Hkv) * C::ROWB;
+    const uint32_t piece = uint32_t(nh) * C::ROWB;
     bool failed = false;
-    int gs0 = 0;     // global step index of the chunk's first step (mbarrier phases)
+    int gs0 = 0;     // global step index of the pass's first step (mbarrier phases)
     int issued = 0;  // producer: steps issued so far (all of 0 .. issued-1)
 
-    for (int base_k = 0; base_k < a.topk_n; base_k += kPagedChunk) {
-        const int cn = min(kPagedChunk, a.topk_n - base_k);
-        __syncthreads();  // previous chunk fully consumed (and, first time, barriers initialised)
+    for (int base_k = 0; base_k < n_tok; base_k += kPagedChunk) {
+        const int cn = min(kPagedChunk, n_tok - base_k);
+        __syncthreads();  // previous pass fully consumed
         if (*abort_flag) break;
         // Index map, batched so each thread has all its top-K loads and then
         // all its page-table loads in flight together.
@@ -203,7 +269,10 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
 #pragma unroll
         for (int u = 0; u < C::IPT; ++u) {
             const int k = threadIdx.x + u * C::THREADS;
-            tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + base_k + k) : -1;
+            if constexpr (RANGE)
+                tk[u] = k < cn ? t_begin + base_k + k : -1;
+            else
+                tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + base_k + k) : -1;
         }
 #pragma unroll
         for (int u = 0; u < C::IPT; ++u) {
@@ -218,7 +287,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
             // lanes 0..15 copy the K pieces of the stage's 16 tokens, lanes 16..31 the V pieces
             const int tok = lane & (C::T - 1);
             const bool is_v = lane >= C::T;
-            const uint8_t *pool = (is_v ? a.v_pool : a.k_pool) + size_t(hb0) * D;
+            const uint8_t *pool = (is_v ? a.v_pool : a.k_pool) + size_t(hb0) * C::ROWB;
             const uint32_t dst_off = is_v ? uint32_t(C::T * C::KRS + tok * C::VRS) : uint32_t(tok * C::KRS);
             for (int s = 0; s < steps && !failed; ++s) {
                 const int gs = gs0 + s;
@@ -246,7 +315,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
                               piece, full + st);
             }
         } else if (active) {
-            const uint32_t kcol = uint32_t(warp * D);
+            const uint32_t kcol = uint32_t(warp * C::ROWB);
             for (int s = 0; s < steps; ++s) {
                 const int gs = gs0 + s;
                 const int st = gs % C::STAGES;
@@ -261,6 +330,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
 
                 // token validity of the two tokens this lane holds in S^T (gi, gi + 8)
                 const bool tv0 = (mask >> gi) & 1u, tv1 = (mask >> (gi + 8)) & 1u;
+                const int tok0 = t_begin + base_k + s * C::T + gi;  // token index (whole-request form)
 
                 // ---- S^T = K . Q^T
                 uint4 kr[2][C::KU];
@@ -274,13 +344,27 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
                 for (int nt = 0; nt < NT; ++nt) st_[nt][0] = st_[nt][1] = st_[nt][2] = st_[nt][3] = 0.f;
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                    const int u = kk >> 2, w = kk & 3;
-                    const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
-                    const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
-                    const uint32_t af[4] = {e4m3x2_to_f16x2(uint16_t(w0 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(w1 & 0xffffu)),
-                                            e4m3x2_to_f16x2(uint16_t(w0 >> 16)), e4m3x2_to_f16x2(uint16_t(w1 >> 16))};
+                    uint32_t af[4];
+                    if constexpr (KV8) {
+                        const int u = kk >> 2, w = kk & 3;
+                        const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
+                        const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
+                        af[0] = e4m3x2_to_f16x2(uint16_t(w0 & 0xffffu));
+                        af[1] = e4m3x2_to_f16x2(uint16_t(w1 & 0xffffu));
+                        af[2] = e4m3x2_to_f16x2(uint16_t(w0 >> 16));
+                        af[3] = e4m3x2_to_f16x2(uint16_t(w1 >> 16));
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
+                        for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
+                    } else {
+                        const int u = kk >> 1;
+                        const bool hi = kk & 1;
+                        af[0] = hi ? kr[0][u].z : kr[0][u].x;
+                        af[1] = hi ? kr[1][u].z : kr[1][u].x;
+                        af[2] = hi ? kr[0][u].w : kr[0][u].y;
+                        af[3] = hi ? kr[1][u].w : kr[1][u].y;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
+                    }
                 }
 
                 // ---- online softmax over the 16 tokens, rows 8 nt + 2c + e
@@ -291,8 +375,13 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
                     float pv[4];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float t0 = tv0 ? st_[nt][e] * alpha_s[nt][e] : -INFINITY;
-                        const float t1 = tv1 ? st_[nt][2 + e] * alpha_s[nt][e] : -INFINITY;
+                        bool ok0 = tv0, ok1 = tv1;
+                        if (causal) {
+                            ok0 = ok0 && tok0 <= kmax[nt][e];
+                            ok1 = ok1 && tok0 + 8 <= kmax[nt][e];
+                        }
+                        const float t0 = ok0 ? st_[nt][e] * alpha_s[nt][e] : -INFINITY;
+                        const float t1 = ok1 ? st_[nt][2 + e] * alpha_s[nt][e] : -INFINITY;
                         float mx = fmaxf(t0, t1);
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -306,8 +395,8 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
                         l_run[nt][e] = l_run[nt][e] * corr[nt][e] + pv[e] + pv[2 + e];
                     }
                     // P^T B fragments: b0 = rows gi at tokens 2c, 2c+1; b1 = tokens 2c+8, 2c+9.
-                    const uint32_t pk_lo = pack_f16x2(pv[0], pv[1]);  // token gi,     rows 2c, 2c+1
-                    const uint32_t pk_hi = pack_f16x2(pv[2], pv[3]);  // token gi + 8, rows 2c, 2c+1
+                    const uint32_t pk_lo = KV8 ? pack_f16x2(pv[0], pv[1]) : pack_bf16x2(pv[0], pv[1]);  // token gi
+                    const uint32_t pk_hi = KV8 ? pack_f16x2(pv[2], pv[3]) : pack_bf16x2(pv[2], pv[3]);  // token gi + 8
                     const int src0 = 4 * (2 * c) + (gi >> 1), src1 = 4 * (2 * c + 1) + (gi >> 1);
                     const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;
                     pb[nt][0] = prmt(__shfl_sync(0xffffffffu, pk_lo, src0), __shfl_sync(0xffffffffu, pk_lo, src1), sel);
@@ -328,44 +417,61 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
                         }
                 }
 
-                // ---- O^T += V^T . P^T.  d-block t: rows m = gi (byte 2t) and gi + 8
-                // (byte 2t + 1) of the lane's VB-byte piece, tokens 2c, 2c+1 (a0, a1)
-                // and 2c+8, 2c+9 (a2, a3).  Rows of invalid tokens are zeroed here
-                // (their ring slots hold stale bytes, possibly NaN codes).
-                uint32_t vw[4][C::VB / 4];
+                // ---- V words of tokens 2c, 2c+1, 2c+8, 2c+9 (rows of padding
+                // tokens zeroed: their ring slots hold stale bytes), then the
+                // stage is released.
+                uint32_t vw[4][C::VW];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int tkn = 2 * c + (j & 1) + 8 * (j >> 1);
                     const bool ok = (mask >> tkn) & 1u;
-                    const uint8_t *src = vst + tkn * C::VRS + kcol + C::VB * gi;
-                    if constexpr (C::VB == 16) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(src);
+                    const uint8_t *vrow = vst + tkn * C::VRS + kcol;
+                    if constexpr (KV8 && C::VB == 8) {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(vrow + 8 * gi);
                         vw[j][0] = ok ? x.x : 0u;
                         vw[j][1] = ok ? x.y : 0u;
-                        vw[j][2] = ok ? x.z : 0u;
-                        vw[j][3] = ok ? x.w : 0u;
                     } else {
-                        const uint2 x = *reinterpret_cast<const uint2 *>(src);
-                        vw[j][0] = ok ? x.x : 0u;
-                        vw[j][1] = ok ? x.y : 0u;
+                        // 16-byte chunks: FP8 one at byte 16 gi; bf16 one per 64 elements at 128 m + 16 gi
+#pragma unroll
+                        for (int m = 0; m < C::VW / 4; ++m) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(vrow + 128 * m + 16 * gi);
+                            vw[j][4 * m + 0] = ok ? x.x : 0u;
+                            vw[j][4 * m + 1] = ok ? x.y : 0u;
+                            vw[j][4 * m + 2] = ok ? x.z : 0u;
+                            vw[j][4 * m + 3] = ok ? x.w : 0u;
+                        }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty + st);  // ring slot free for the producer
+
+                // ---- O^T += V^T . P^T, tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3)
+                if constexpr (KV8) {
+                    // d-block t: rows m = gi (byte 2t) and gi + 8 (byte 2t + 1) of the lane's piece
 #pragma unroll
-                for (int w = 0; w < C::VB / 4; ++w) {
-                    const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
-                    const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
-                    const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
-                    const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
-                    const uint32_t a_t0[4] = {e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
-                                              e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd01 >> 16))};
-                    const uint32_t a_t1[4] = {e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
-                                              e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd23 >> 16))};
+                    for (int w = 0; w < C::VW; ++w) {
+                        const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
+                        const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
+                        const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
+                        const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
+                        const uint32_t a_t0[4] = {e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
+                                                  e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd01 >> 16))};
+                        const uint32_t a_t1[4] = {e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
+                                                  e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd23 >> 16))};
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);
-                        mma_f16_16816(o[nt][2 * w + 1], a_t1, pb[nt][0], pb[nt][1]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);
+                            mma_f16_16816(o[nt][2 * w + 1], a_t1, pb[nt][0], pb[nt][1]);
+                        }
+                    }
+                } else {
+                    // d-block t = word t: rows m = gi (low half) and gi + 8 (high half)
+#pragma unroll
+                    for (int t = 0; t < C::DB; ++t) {
+                        const uint32_t a_t[4] = {prmt(vw[0][t], vw[1][t], 0x5410u), prmt(vw[0][t], vw[1][t], 0x7632u),
+                                                 prmt(vw[2][t], vw[3][t], 0x5410u), prmt(vw[2][t], vw[3][t], 0x7632u)};
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][t], a_t, pb[nt][0], pb[nt][1]);
                     }
                 }
             }
@@ -390,21 +496,10 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
     }
     if (!active || *abort_flag) return;
 
-    // ---- epilogue: v_scale, normalise, sigmoid gate, bf16.  Lane holds rows
-    // 8 nt + 2c + e at head-dim bytes VB*gi .. VB*gi + VB-1 (d-block t:
-    // 2t from o[t][e], 2t + 1 from o[t][2 + e]).  All gate words are loaded
-    // before the first store so they are in flight together.
-    uint32_t graw[NT][2][C::DB];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int hl = 8 * nt + 2 * c + e;
-            const size_t off = (size_t(b) * a.Hq + g * a.G + hl) * D + C::VB * gi;
-#pragma unroll
-            for (int t = 0; t < C::DB; ++t)
-                graw[nt][e][t] = hl < a.G ? __ldg(reinterpret_cast<const unsigned int *>(a.gate + off + 2 * t)) : 0u;
-        }
+    // ---- epilogue.  Lane holds rows r = 8 nt + 2c + e at the head-dim
+    // elements out_d(t, 0|1, gi) of o[nt][t][e] / o[nt][t][2 + e].
+    //  one split: out = gate ? sigmoid(gate) * v_scale * O / l : v_scale * O / l (bf16), LSE (natural log);
+    //  several: fp32 partials v_scale * O / l and the log2-domain LSE for the combine kernel.
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -413,57 +508,49 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB>::THREADS, PagedCfg<D, NT, 
             L += __shfl_xor_sync(0xffffffffu, L, 4);
             L += __shfl_xor_sync(0xffffffffu, L, 8);
             L += __shfl_xor_sync(0xffffffffu, L, 16);
-            const int hl = 8 * nt + 2 * c + e;
-            if (hl >= a.G) continue;
-            const int h = g * a.G + hl;
+            const int r = 8 * nt + 2 * c + e;
+            if (r >= a.Mq) continue;
+            const int i = r / a.G;
+            const int h = g * a.G + r % a.G;
             const float f = L > 0.f ? a.v_scale / L : 0.f;
-            const size_t off = (size_t(b) * a.Hq + h) * D + C::VB * gi;
-            uint32_t packed[C::VB / 2];
+            const float lse2 = L > 0.f ? m_run[nt][e] + log2f(L) : -INFINITY;
+            if (a.num_splits > 1) {
+                const size_t prow = ((size_t(b) * a.Hkv + g) * a.Mq + r) * a.num_splits + split;
+                float *dst = a.o_part + prow * D;
+#pragma unroll
+                for (int t = 0; t < C::DB; ++t)
+                    *reinterpret_cast<float2 *>(dst + out_d<D, KV8>(t, 0, gi)) =
+                        make_float2(o[nt][t][e] * f, o[nt][t][2 + e] * f);
+                if (gi == 0) a.lse_part[prow] = lse2;
+                continue;
+            }
+            const size_t off = ((size_t(b) * a.Sq + i) * a.Hq + h) * D;
+            uint32_t graw[C::DB];
+#pragma unroll
+            for (int t = 0; t < C::DB; ++t)
+                graw[t] = a.gate != nullptr
+                              ? __ldg(reinterpret_cast<const unsigned int *>(a.gate + off + out_d<D, KV8>(t, 0, gi)))
+                              : 0u;
+            uint32_t packed[C::DB];
 #pragma unroll
             for (int t = 0; t < C::DB; ++t) {
-                const float g0 = __uint_as_float(graw[nt][e][t] << 16);
-                const float g1 = __uint_as_float(graw[nt][e][t] & 0xffff0000u);
-                const float s0 = 1.f / (1.f + __expf(-g0));
-                const float s1 = 1.f / (1.f + __expf(-g1));
+                float s0 = 1.f, s1 = 1.f;
+                if (a.gate != nullptr) {
+                    const float g0 = __uint_as_float(graw[t] << 16);
+                    const float g1 = __uint_as_float(graw[t] & 0xffff0000u);
+                    s0 = 1.f / (1.f + __expf(-g0));
+                    s1 = 1.f / (1.f + __expf(-g1));
+                }
                 packed[t] = pack_bf16x2(o[nt][t][e] * f * s0, o[nt][t][2 + e] * f * s1);
             }
+            // output d-blocks 4q .. 4q+3 are 8 contiguous elements
 #pragma unroll
-            for (int t = 0; t < C::VB / 2; t += 4)
-                *reinterpret_cast<uint4 *>(a.out + off + 2 * t) =
-                    make_uint4(packed[t], packed[t + 1], packed[t + 2], packed[t + 3]);
+            for (int q4 = 0; q4 < C::DB / 4; ++q4)
+                *reinterpret_cast<uint4 *>(a.out + off + out_d<D, KV8>(4 * q4, 0, gi)) =
+                    make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
             if (a.lse != nullptr && gi == 0)
-                a.lse[size_t(b) * a.Hq + h] = L > 0.f ? (m_run[nt][e] + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+                a.lse[(size_t(b) * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
         }
-}
-
-// Test hook: byte copy of the selected rows through the kernel's own index map.
-__global__ void gqa_paged_gather_kernel(const uint8_t *pool, const int32_t *page_table, const int32_t *topk,
-                                        uint8_t *out, int Hkv, int D, int page_size, int pages_per_req,
-                                        int num_pages, int topk_n, unsigned *err) {
-    const int k = blockIdx.x;
-    const int b = blockIdx.y;
-    bool bad = false;
-    const int t = topk[size_t(b) * topk_n + k];
-    const int row = paged_token_row(page_table, b, pages_per_req, page_size, num_pages, t, &bad);
-    if (bad && threadIdx.x == 0) flag_error(err, kErrIndex);
-    const int n16 = Hkv * D / 16;
-    uint4 *dst = reinterpret_cast<uint4 *>(out + (size_t(b) * topk_n + k) * Hkv * D);
-    for (int u = threadIdx.x; u < n16; u += blockDim.x) {
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row >= 0) v = *reinterpret_cast<const uint4 *>(pool + size_t(row) * Hkv * D + size_t(u) * 16);
-        dst[u] = v;
-    }
-}
-
-// Test hook: the kernel's E4M3FN -> f16 widening, reported as fp32.
-__global__ void gqa_fp8_to_f32_kernel(const uint8_t *codes, float *out, int n) {
-    const int i = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
-    if (i >= n) return;
-    const uint16_t two = uint16_t(codes[i]) | (i + 1 < n ? uint16_t(codes[i + 1]) << 8 : uint16_t(0));
-    const uint32_t h2 = e4m3x2_to_f16x2(two);
-    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-    out[i] = f.x;
-    if (i + 1 < n) out[i + 1] = f.y;
 }
 
 }  // namespace gqa

@@ -38,15 +38,19 @@ struct DenseArgs {
 };
 
 struct PagedArgs {
-    const __nv_bfloat16 *q;
-    const __nv_bfloat16 *gate;
-    const uint8_t *k_pool;
+    const __nv_bfloat16 *q;     // [B, Sq, Hq, D]
+    const __nv_bfloat16 *gate;  // [B, Hq, D] or null (no gate)
+    const uint8_t *k_pool;      // [num_pages, page_size, Hkv, D] elements (FP8 codes or bf16)
     const uint8_t *v_pool;
-    const int32_t *page_table;
-    const int32_t *topk;
-    __nv_bfloat16 *out;
-    float *lse;
-    int B, Hq, Hkv, G, page_size, pages_per_req, num_pages, topk_n;
+    const int32_t *page_table;  // [B, pages_per_req]
+    const int32_t *topk;        // [B, topk_n] (top-K form)
+    const int32_t *seq_lens;    // [B] (whole-request form)
+    __nv_bfloat16 *out;         // [B, Sq, Hq, D]
+    float *lse;                 // [B, Hq, Sq] or null
+    float *o_part;              // [B*Hkv, Mq, num_splits, D] fp32 (num_splits > 1)
+    float *lse_part;            // [B*Hkv, Mq, num_splits] fp32, log2 domain (num_splits > 1)
+    int B, Sq, Hq, Hkv, G, Mq, page_size, pages_per_req, num_pages, topk_n;
+    int num_splits, tokens_per_split;  // whole-request form
     float alpha;    // scale * k_scale * log2(e)
     float v_scale;
     unsigned long long wait_limit_ns;

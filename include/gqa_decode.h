@@ -192,6 +192,64 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
                                 int num_pages, int topk, float scale, gqa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Paged decode over whole requests (no top-K selection), bf16 or FP8 pools.
+ *
+ * The serving layout of a paged KV cache: request b holds tokens
+ * t = 0 .. seq_lens[b]-1, token t stored at page page_table[b, t / page_size],
+ * slot t % page_size, of the shared pools (the page-table addressing of
+ * "Sparse paged GQA decode attention with FP8 KV cache on SM89", section
+ * "Workload", applied to every token instead of a top-K list).  For query row
+ * i < Sq of request b and query head h (KV head g = h // (Hq/Hkv)), the
+ * visible tokens are t <= seq_lens[b] - Sq + i (bottom-right alignment, as in
+ * gqa_decode), and
+ *   s_t = scale * q[b,i,h,:] . K^_t,  K^ = k * k_scale,  V^ = v * v_scale,
+ *   out[b,i,h,:] = softmax(s) V^,  lse[b,h,i] = ln sum_t exp(s_t).
+ * A row that sees no token gives out = 0 and lse = -inf.  Each request's
+ * tokens may be split over several CTAs; the fp32 partials are merged by the
+ * same LSE-weighted combine as gqa_decode's.
+ *
+ * q, out : device bf16 [B, Sq, Hq, D].  lse : device fp32 [B, Hq, Sq] or NULL.
+ * k_pool, v_pool : device [num_pages, page_size, Hkv, D] of bf16
+ *   (kv_dtype GQA_KV_BF16; k_scale and v_scale are ignored) or of E4M3FN
+ *   codes (GQA_KV_FP8_E4M3FN; k_scale, v_scale finite host fp32 scalars).
+ * page_table : device int32 [B, pages_per_req].  seq_lens : device int32 [B].
+ * Limits: D in {64, 128}; (Hq / Hkv) * Sq <= 16; pages_per_req * page_size
+ *   and num_pages * page_size < 2^31.  Pointers 16-byte aligned (q, out,
+ *   pools), 4-byte aligned (page_table, seq_lens, lse).
+ * Device-checked: a seq_lens[b] outside [0, pages_per_req * page_size] is
+ *   clamped into it, and a page id outside [0, num_pages) is skipped; both
+ *   flag GQA_ERR_DEVICE_INDEX in the device error word.
+ * Workspace: gqa_decode_paged allocates its split partials stream-ordered
+ *   from a library-owned pool; gqa_decode_paged_ex takes num_splits (0 =
+ *   automatic) and an optional caller workspace (256-byte aligned, at least
+ *   gqa_decode_paged_workspace_bytes; NULL = library pool).
+ * ------------------------------------------------------------------------ */
+typedef enum { GQA_KV_BF16 = 0, GQA_KV_FP8_E4M3FN = 1 } gqa_kv_dtype;
+
+gqa_status gqa_decode_paged(const void *q, const void *k_pool, const void *v_pool, int kv_dtype,
+                            float k_scale, float v_scale, const int32_t *page_table,
+                            const int32_t *seq_lens, void *out, float *lse,
+                            int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                            int pages_per_req, int num_pages, float scale, gqa_stream_t stream);
+
+gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_pool, int kv_dtype,
+                               float k_scale, float v_scale, const int32_t *page_table,
+                               const int32_t *seq_lens, void *out, float *lse,
+                               int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                               int pages_per_req, int num_pages, float scale, int num_splits,
+                               void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
+/* Token splits per request the automatic choice uses for this shape on the
+ * current device (negative gqa_status on invalid arguments). */
+int gqa_decode_paged_num_splits(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype,
+                                int page_size, int pages_per_req);
+
+/* Workspace bytes gqa_decode_paged_ex needs for num_splits (0 = automatic);
+ * 0 when no workspace is needed or the arguments are invalid. */
+size_t gqa_decode_paged_workspace_bytes(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype,
+                                        int page_size, int pages_per_req, int num_splits);
+
+/* ------------------------------------------------------------------------
  * Test hooks.  They run the paged kernel's own index mapping and FP8
  * conversion in isolation so those can be checked bit for bit.
  * ------------------------------------------------------------------------ */

@@ -115,6 +115,55 @@ def test_paged_rejects(lib, kw, status):
     assert _paged(lib, **kw) == status
 
 
+def _paged_kv(lib, q=A, kp=A, vp=A, kvd=0, ks=1.0, vs=1.0, pt=A, sl=A, out=A, lse=A, B=2, Sq=1, Hq=8, Hkv=2,
+              D=128, ps=16, ppr=4, num_pages=16, splits=0, ws=None, ws_bytes=0):
+    return lib.gqa_decode_paged_ex(q, kp, vp, kvd, ks, vs, pt, sl, out, lse, B, Sq, Hq, Hkv, D, ps, ppr,
+                                   num_pages, 0.0, splits, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(Hq=6, Hkv=4), 1),
+    (dict(Sq=0), 1),
+    (dict(ps=0), 1),
+    (dict(ppr=0), 1),
+    (dict(num_pages=0), 1),
+    (dict(kvd=2), 1),                # unknown pool type
+    (dict(splits=-1), 1),
+    (dict(D=96), 2),
+    (dict(D=256), 2),
+    (dict(Hq=64, Hkv=2), 2),         # group of 32 rows > 16
+    (dict(Hq=16, Hkv=2, Sq=3), 2),   # 8 heads x 3 decode rows > 16
+    (dict(kvd=1, ks=float("inf")), 1),
+    (dict(kvd=1, vs=float("nan")), 1),
+    (dict(kvd=0, ks=float("inf")), None),  # scales ignored for bf16 pools: not an argument error
+    (dict(q=0), 1),
+    (dict(sl=0), 1),
+    (dict(pt=0), 1),
+    (dict(kp=MIS), 3),
+    (dict(out=MIS), 3),
+    (dict(sl=A + 2), 3),
+    (dict(lse=A + 2), 3),
+])
+def test_paged_kv_rejects(lib, kw, status):
+    got = _paged_kv(lib, **kw)
+    if status is None:
+        assert got not in (1, 2, 3)
+    else:
+        assert got == status
+
+
+def test_paged_kv_sizes(lib):
+    # automatic split count and workspace reject bad shapes with a negative status / zero
+    assert lib.gqa_decode_paged_num_splits(2, 1, 8, 2, 96, 0, 16, 4) == -2
+    assert lib.gqa_decode_paged_num_splits(2, 1, 6, 4, 128, 0, 16, 4) == -1
+    assert lib.gqa_decode_paged_workspace_bytes(2, 1, 8, 2, 96, 0, 16, 4, 3) == 0
+    # explicit splits need no device: 2 requests x 2 heads x 4 rows x 3 splits
+    rows = 2 * 2 * 4 * 3
+    want = ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert lib.gqa_decode_paged_workspace_bytes(2, 1, 8, 2, 128, 0, 16, 64, 3) == want
+    assert lib.gqa_decode_paged_workspace_bytes(2, 1, 8, 2, 128, 0, 16, 64, 1) == 0
+
+
 def test_gather_and_convert_reject(lib):
     assert lib.gqa_paged_gather_fp8(A, A, A, A, 2, 2, 128, 16, 4, 16, 65, None) == 1
     assert lib.gqa_paged_gather_fp8(MIS, A, A, A, 2, 2, 128, 16, 4, 16, 32, None) == 3

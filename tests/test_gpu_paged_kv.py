@@ -1,0 +1,141 @@
+"""GPU parity of paged decode over whole requests (no top-K), bf16 and FP8
+pools, through the C ABI, against the fp64 oracle on the same stored bytes."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gqa_inputs
+from parity import assert_lse_close, assert_o_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gq():
+    from gqa_decode_attention_gb300 import build as gbuild
+    gbuild.build()
+    import gqa_decode_attention_gb300 as m
+    m.load_library()
+    assert torch.cuda.is_available()
+    return m
+
+
+def _cuda(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _run(gq, inp, **kw):
+    d = _cuda(inp)
+    out, lse = gq.gqa_decode_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"],
+                                   d["k_scale"], d["v_scale"], **kw)
+    torch.cuda.synchronize()
+    return out.cpu(), lse.cpu()
+
+
+def _ref(orc, inp, scale):
+    return orc.gqa_decode_paged(inp["q"], inp["k_pool"], inp["v_pool"], inp["page_table"], inp["seq_lens"],
+                                scale, inp["k_scale"], inp["v_scale"])
+
+
+def _check(out, lse, ref_o, ref_l, what):
+    # rows that see no token: exactly zero output, -inf LSE
+    empty = np.isneginf(ref_l)                     # [B, Hq, Sq]
+    if empty.any():
+        e = torch.from_numpy(empty)
+        assert torch.all(torch.isneginf(lse[e])), what
+        oe = out.float().permute(0, 2, 1, 3)[e]    # [n, D]
+        assert torch.all(oe == 0), what
+    ok = ~empty
+    o_ok = torch.from_numpy(ok).permute(0, 2, 1)   # [B, Sq, Hq]
+    assert_o_close(out[o_ok], ref_o[o_ok.numpy()], what)
+    assert_lse_close(lse[torch.from_numpy(ok)], ref_l[ok], what)
+
+
+# (B, Sq, Hq, Hkv, D, page_size, pages_per_req, kv, seq_lens)
+SMALL = [
+    (3, 1, 32, 8, 128, 16, 8, "bf16", (128, 77, 1)),
+    (3, 1, 32, 8, 128, 16, 8, "fp8", (128, 100, 17)),
+    (2, 2, 16, 4, 128, 1, 90, "bf16", (90, 33)),          # page size 1, two decode rows
+    (2, 4, 8, 2, 64, 64, 3, "fp8", (192, 5)),             # four decode rows, one request shorter than a page
+    (2, 3, 12, 3, 128, 16, 6, "bf16", (96, 2)),           # request shorter than S_q: rows without tokens
+    (2, 1, 16, 1, 64, 16, 10, "bf16", (160, 0)),          # an empty request
+    (1, 1, 96, 12, 64, 32, 4, "fp8", (111,)),             # 12 heads: a full and a partial head block
+    (2, 2, 64, 8, 128, 16, 12, "fp8", (190, 64)),         # 16 rows per KV head: two n-tiles
+    (1, 1, 16, 1, 128, 16, 300, "bf16", (4800,)),         # more tokens than one index-map pass
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "b{}_sq{}_h{}x{}_d{}_ps{}_ppr{}_{}".format(*s[:8]))
+@pytest.mark.parametrize("splits", [0, 1, 5])
+def test_paged_kv_small_vs_oracle(gq, orc, shape, splits):
+    B, Sq, Hq, Hkv, D, ps, ppr, kv, lens = shape
+    inp = gqa_inputs.paged_kv_inputs(B, Sq, Hq, Hkv, D, ps, ppr, B * ppr + 2, seed=sum(lens) + D + ps, kv_dtype=kv,
+                                     seq_lens=list(lens))
+    out, lse = _run(gq, inp, num_splits=splits)
+    ref_o, ref_l = _ref(orc, inp, 1.0 / math.sqrt(D))
+    _check(out, lse, ref_o, ref_l, f"paged kv {shape} splits={splits}")
+    assert gq.gqa_device_status() == 0
+
+
+def test_split_counts_agree(gq):
+    inp = gqa_inputs.paged_kv_inputs(4, 1, 32, 8, 128, 16, 64, 300, seed=41, kv_dtype="bf16")
+    ref, ref_l = _run(gq, inp, num_splits=1)
+    cap = 64 * 16
+    for s in (2, 3, 7, cap // 16):
+        out, lse = _run(gq, inp, num_splits=s)
+        assert torch.allclose(out.float(), ref.float(), atol=2e-2, rtol=2e-2), s
+        assert torch.allclose(lse, ref_l, atol=1e-3, rtol=0), s
+
+
+def test_page_permutation_and_caller_workspace(gq, orc):
+    """Moving every page elsewhere in the pool (and the table with it) changes
+    nothing; a caller workspace gives the same result as the library pool."""
+    inp = gqa_inputs.paged_kv_inputs(3, 1, 32, 8, 128, 16, 16, 60, seed=42, kv_dtype="fp8")
+    out, lse = _run(gq, inp, num_splits=4)
+    perm = torch.randperm(60, generator=torch.Generator().manual_seed(43))
+    inv = torch.argsort(perm)
+    moved = dict(inp, k_pool=inp["k_pool"][perm].contiguous(), v_pool=inp["v_pool"][perm].contiguous(),
+                 page_table=inv[inp["page_table"].long()].to(torch.int32).contiguous())
+    out2, lse2 = _run(gq, moved, num_splits=4)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    nbytes = gq.gqa_decode_paged_workspace_bytes(3, 1, 32, 8, 128, 1, 16, 16, 4)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out3, lse3 = _run(gq, inp, num_splits=4, workspace=ws)
+    assert torch.equal(out, out3) and torch.equal(lse, lse3)
+
+
+def test_sequence_length_out_of_range_flagged(gq):
+    inp = gqa_inputs.paged_kv_inputs(2, 1, 8, 2, 64, 16, 4, 9, seed=44, kv_dtype="bf16", seq_lens=[64, 10])
+    inp["seq_lens"][1] = 65                       # capacity is 64
+    _run(gq, inp)
+    assert gq.gqa_device_status() == 7
+    assert gq.gqa_device_status() == 0
+
+
+def test_wait_timeout_is_reported_not_hung(gq):
+    """The producer withholds the first stage of every CTA (test hook): the
+    bounded waits run out, the kernel returns and flags a timeout, and the
+    next call works."""
+    inp = gqa_inputs.paged_kv_inputs(2, 1, 32, 8, 128, 16, 8, 17, seed=45, kv_dtype="bf16")
+    d = _cuda(inp)
+    gq.gqa_set_wait_limit_ns(50_000_000)
+    gq.gqa_debug_set_fault_mode(1)
+    try:
+        gq.gqa_decode_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"], num_splits=1)
+        assert gq.gqa_device_status() == 6
+    finally:
+        gq.gqa_debug_set_fault_mode(0)
+        gq.gqa_set_wait_limit_ns(0)
+    out, lse = _run(gq, inp)
+    assert gq.gqa_device_status() == 0
+    assert torch.isfinite(lse).all()
+
+
+def test_automatic_splits_reported(gq):
+    n = gq.gqa_decode_paged_num_splits(4, 1, 32, 8, 128, 0, 16, 256)
+    assert n >= 1
+    assert gq.gqa_decode_paged_workspace_bytes(4, 1, 32, 8, 128, 0, 16, 256) == (
+        0 if n == 1 else gq.gqa_decode_paged_workspace_bytes(4, 1, 32, 8, 128, 0, 16, 256, n))
