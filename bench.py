@@ -39,7 +39,7 @@ import gqa_inputs  # noqa: E402
 METRIC = "GQA decode µs/call and KV-cache HBM GB/s (% of measured GB300 peak)"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gqa_dense_kernel.cuh", "gqa_dense_umma.cuh", "gqa_umma.cuh", "gqa_paged_kernel.cuh",
-                  "gqa_common.cuh", "gqa_params.h", "gqa_dense_impl.cuh"]
+                  "gqa_common.cuh", "gqa_params.h", "gqa_dense_impl.cuh", "gqa_paged_impl.cuh"]
 
 
 # ---------------------------------------------------------------------------
@@ -58,9 +58,16 @@ def paged_flops(B, Hq, topk, D) -> int:
     return 4 * B * topk * Hq * D
 
 
+def paged_kv_lens(cfg) -> list[int]:
+    return [int(x) for x in gqa_inputs.paged_kv_seq_lens(cfg.B, cfg.Sq, cfg.pages_per_req * cfg.page_size, cfg.seed)]
+
+
 def workload_kv_bytes(cfg) -> int:
     if isinstance(cfg, gqa_inputs.DenseConfig):
         return kv_bytes(cfg.B, cfg.Hkv, cfg.Skv, cfg.D, 2)
+    if isinstance(cfg, gqa_inputs.PagedKVConfig):
+        elem = 2 if cfg.kv_dtype == "bf16" else 1
+        return sum(kv_bytes(1, cfg.Hkv, n, cfg.D, elem) for n in paged_kv_lens(cfg))
     return kv_bytes(cfg.B, cfg.Hkv, cfg.topk, cfg.D, 1)
 
 
@@ -68,9 +75,28 @@ def workload_config(cfg) -> dict:
     if isinstance(cfg, gqa_inputs.DenseConfig):
         return {"workload": cfg.name, "B": cfg.B, "Sq": cfg.Sq, "Skv": cfg.Skv, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
                 "D": cfg.D, "kv_dtype": "bf16", "mask": "bottom-right causal" if cfg.Sq > 1 else "none"}
+    if isinstance(cfg, gqa_inputs.PagedKVConfig):
+        lens = paged_kv_lens(cfg)
+        cap = cfg.pages_per_req * cfg.page_size
+        return {"workload": cfg.name, "B": cfg.B, "Sq": cfg.Sq, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
+                "page_size": cfg.page_size, "pages_per_req": cfg.pages_per_req, "num_pages": cfg.num_pages,
+                "seq_lens": f"uniform in [{max(cfg.Sq, cap // 2)}, {cap}], total {sum(lens)} tokens",
+                "kv_dtype": "bf16" if cfg.kv_dtype == "bf16" else "fp8_e4m3fn"}
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
             "page_size": cfg.page_size, "pages_per_req": cfg.pages_per_req, "num_pages": cfg.num_pages,
             "topk": cfg.topk, "kv_dtype": "fp8_e4m3fn"}
+
+
+def workload_dtype(cfg) -> str:
+    if isinstance(cfg, gqa_inputs.DenseConfig) or (isinstance(cfg, gqa_inputs.PagedKVConfig) and cfg.kv_dtype == "bf16"):
+        return "bf16"
+    return "fp8_e4m3fn kv, bf16 q/out, f16 mma"
+
+
+def workload_kernel(cfg) -> str:
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        return "gqa_dense_umma_kernel" if cfg.D == 256 else "gqa_dense_split_kernel"
+    return "gqa_paged_kernel"
 
 
 def gbs(nbytes: float, ms: float) -> float:
@@ -253,6 +279,19 @@ def _make_call(gq, cfg, dev, seed_offset):
             gq.gqa_decode(q, k, v, out=out, lse=lse)
         splits = gq.gqa_decode_num_splits(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D)
         return call, dict(q=q, k=k, v=v, out=out, lse=lse), (2 if splits > 1 else 1), splits
+    if isinstance(cfg, gqa_inputs.PagedKVConfig):
+        inp = gqa_inputs.paged_kv_inputs(cfg.B, cfg.Sq, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
+                                         cfg.num_pages, cfg.seed + seed_offset, cfg.kv_dtype,
+                                         seq_lens=paged_kv_lens(cfg), device=dev)
+        out = torch.empty_like(inp["q"])
+        lse = torch.empty((cfg.B, cfg.Hq, cfg.Sq), dtype=torch.float32, device=dev)
+
+        def call():
+            gq.gqa_decode_paged(inp["q"], inp["k_pool"], inp["v_pool"], inp["page_table"], inp["seq_lens"],
+                                inp["k_scale"], inp["v_scale"], out=out, lse=lse)
+        splits = gq.gqa_decode_paged_num_splits(cfg.B, cfg.Sq, cfg.Hq, cfg.Hkv, cfg.D,
+                                                0 if cfg.kv_dtype == "bf16" else 1, cfg.page_size, cfg.pages_per_req)
+        return call, dict(inp, out=out, lse=lse), (2 if splits > 1 else 1), splits
     inp = gqa_inputs.paged_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
                                   cfg.num_pages, cfg.topk, cfg.seed + seed_offset, device=dev)
     out = torch.empty_like(inp["q"])
@@ -307,6 +346,9 @@ def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
             reps += 1
         sample = (f"{'all' if rows is None else len(rows)} of {nrows} query rows "
                   f"(the rows of whole KV-head groups), {reps} pass(es)")
+    elif isinstance(cfg, gqa_inputs.PagedKVConfig):
+        cpu = {n: (t.cpu() if hasattr(t, "cpu") else t) for n, t in tensors.items()}
+        return _paged_kv_oracle_timing(orc, cfg, cpu, max_seconds, min_seconds)
     else:
         cpu = {n: (t.cpu() if hasattr(t, "cpu") else t) for n, t in tensors.items()}
         nrows = cfg.B * cfg.Hq
@@ -329,6 +371,40 @@ def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
     return {"value": gbs(workload_kv_bytes(cfg) * frac, per_pass * 1e3), "unit": "GB/s",
             "cores": orc.num_threads(), "kind": "oracle", "sample": sample,
             "us_per_call_equiv": per_pass / frac * 1e6}
+
+
+def _paged_kv_oracle_timing(orc, cfg, cpu, max_seconds, min_seconds) -> dict:
+    """The oracle on whole-request paged inputs: rows of request 0 first (a
+    row sample when a pass would exceed max_seconds); bytes credited per row
+    as its share of its request's K/V."""
+    lens = [int(x) for x in cpu["seq_lens"]]
+    elem = 2 if cfg.kv_dtype == "bf16" else 1
+    nrows = cfg.B * cfg.Hq * cfg.Sq
+    G = cfg.Hq // cfg.Hkv
+
+    def row_bytes(r):  # row r = (b*Hq + h)*Sq + i reads 1/(G*Sq) of its KV head's bytes
+        b = r // (cfg.Hq * cfg.Sq)
+        return 2 * lens[b] * cfg.D * elem / (G * cfg.Sq)
+
+    def run(rows):
+        orc.gqa_decode_paged(cpu["q"], cpu["k_pool"], cpu["v_pool"], cpu["page_table"], cpu["seq_lens"],
+                             cfg.scale, cpu["k_scale"], cpu["v_scale"], rows=rows)
+
+    t0 = time.perf_counter()
+    run(list(range(8)))
+    per_row = (time.perf_counter() - t0) / 8
+    rows = None if per_row * nrows <= max_seconds else list(range(max(1, int(max_seconds / 3 / per_row))))
+    covered = sum(row_bytes(r) for r in (range(nrows) if rows is None else rows))
+    reps, elapsed = 0, 0.0
+    while elapsed < min_seconds and reps < 1000:
+        t0 = time.perf_counter()
+        run(rows)
+        elapsed += time.perf_counter() - t0
+        reps += 1
+    per_pass = elapsed / reps
+    sample = f"{'all' if rows is None else len(rows)} of {nrows} query rows, {reps} pass(es)"
+    return {"value": gbs(covered, per_pass * 1e3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+            "sample": sample, "seconds_per_pass": per_pass, "bytes_covered": covered}
 
 
 def run_gqa(args) -> int:
@@ -446,7 +522,7 @@ def run_gqa(args) -> int:
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16" if isinstance(cfg, gqa_inputs.DenseConfig) else "fp8_e4m3fn kv, bf16 q/out, f16 mma",
+            "dtype": workload_dtype(cfg),
             "data": "synthetic (seeded N(0,1), generated on the device)",
             "config": dict(workload_config(cfg),
                            l2=f"flushed before every step: {flush_bytes >> 20} MiB written, then {flush_bytes >> 20} MiB read",
@@ -461,8 +537,7 @@ def run_gqa(args) -> int:
             "frac_of_copy_peak_this_run": round(value / world / copy_peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(cfg.name),
-                         "kernel": ("gqa_dense_umma_kernel" if cfg.D == 256 else "gqa_dense_split_kernel")
-                         if isinstance(cfg, gqa_inputs.DenseConfig) else "gqa_paged_fp8_kernel",
+                         "kernel": workload_kernel(cfg),
                          "kernel_us": round(kern_avg * 1e3, 2),
                          "algorithmic_bytes_per_launch": nbytes},
             "cpu_baseline": cpu_base,
@@ -497,6 +572,27 @@ def run_reference(args) -> int:
 
         def step():
             orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
+    elif isinstance(cfg, gqa_inputs.PagedKVConfig):
+        inp = gqa_inputs.paged_kv_config_inputs(cfg, device="cpu")
+        budget_s = 150.0 / max(1, args.steps + args.warmup)
+        probe = _paged_kv_oracle_timing(orc, cfg, inp, max_seconds=budget_s, min_seconds=0.0)
+        ts = []
+        for _ in range(args.steps):
+            r = _paged_kv_oracle_timing(orc, cfg, inp, max_seconds=budget_s, min_seconds=0.0)
+            ts.append(r["seconds_per_pass"] * 1e3)
+        total = sum(ts)
+        value = gbs(args.steps * probe["bytes_covered"], total)
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(total / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), CPU)",
+            "config": workload_config(cfg), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": probe["sample"] + " per step"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return 0
     else:
         inp = gqa_inputs.paged_config_inputs(cfg, device="cpu")
         nrows = cfg.B * cfg.Hq

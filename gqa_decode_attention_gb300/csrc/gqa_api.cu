@@ -306,11 +306,11 @@ gqa_status check_paged(int B, int Hq, int Hkv, int D, int page_size, int pages_p
 }
 
 // ------------------------------------------------------------ paged, whole requests
-constexpr int kPagedMinSplitTokens = 256;
 
 struct PagedShape {
     int B, Sq, Hq, Hkv, D, G, Mq, ps, ppr, num_pages, cap;
     bool kv8;
+    bool topk_form;  // the sparse top-K form (FP8, gated) rather than whole requests
 };
 
 gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int page_size, int pages_per_req,
@@ -337,58 +337,74 @@ gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, i
     s->num_pages = num_pages;
     s->cap = pages_per_req * page_size;
     s->kv8 = kv_dtype == GQA_KV_FP8_E4M3FN;
+    s->topk_form = false;
     return GQA_OK;
 }
 
 // Resident CTAs per SM of the paged instance serving shape s (cached).
 int paged_occupancy(int dev, const PagedShape &s) {
-    static int cache[kMaxDevices][2][2][2][4];  // [dev][kv8][D][two n-tiles][log2 heads per CTA]
+    static int cache[kMaxDevices][3][2][2][4];  // [dev][form][D][two n-tiles][log2 heads per CTA]
     const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
     const int lh = hb == 1 ? 0 : hb == 2 ? 1 : hb == 4 ? 2 : 3;
+    const int form = s.topk_form ? 2 : s.kv8 ? 1 : 0;
     std::lock_guard<std::mutex> lk(g_mu);
-    int &slot = cache[dev][s.kv8][s.D == 128][s.Mq > 8][lh];
+    int &slot = cache[dev][form][s.D == 128][s.Mq > 8][lh];
     if (slot == 0) {
         PagedArgs a;
         std::memset(&a, 0, sizeof(a));
         a.Hkv = s.Hkv;
         a.Mq = s.Mq;
-        slot = s.kv8 ? paged_range_ctas_per_sm_fp8(a, s.D) : paged_range_ctas_per_sm_bf16(a, s.D);
+        slot = s.topk_form ? paged_topk_ctas_per_sm_fp8(a, s.D)
+               : s.kv8     ? paged_range_ctas_per_sm_fp8(a, s.D)
+                           : paged_range_ctas_per_sm_bf16(a, s.D);
     }
     return slot;
 }
 
-// Token splits of each request: one wave of resident CTAs when the requests
-// alone do not fill it, every split at least kPagedMinSplitTokens tokens of
-// the table's capacity, then evened out to multiples of 16 tokens.  Returns
-// the split count and sets *tps (tokens per split).
-int choose_paged_splits(const PagedShape &s, int requested, int dev, int *tps) {
-    int S;
-    const int max_s = (s.cap + kPagedMinSplitTokens - 1) / kPagedMinSplitTokens;
+// Workers per head block of the balanced schedule: one resident CTA slot
+// each (the kernel is bound by bytes in flight, so every slot should stream),
+// at least one.  The top-K form (equal lists) uses one worker per request as
+// soon as the requests fill half the slots: a request then never straddles
+// two workers and no merge pass is needed, which costs less than the idle
+// slots it leaves.
+int choose_paged_workers(const PagedShape &s, int requested, int dev) {
+    long W;
     if (requested > 0) {
-        S = requested;
+        W = requested;
     } else {
         const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
-        const long units = long(s.B) * ((s.Hkv + hb - 1) / hb);
+        const long nhb = (s.Hkv + hb - 1) / hb;
         const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
         const long occ = paged_occupancy(dev, s) > 0 ? paged_occupancy(dev, s) : 1;
-        const long slots = nsm * occ;
-        S = units >= slots ? 1 : int(slots / units);
-        if (S > max_s) S = max_s;
+        W = nsm * occ / nhb;
+        if (s.topk_form && 2 * long(s.B) * nhb >= nsm * occ) W = s.B;
     }
-    const int max_split = (s.cap + 15) / 16;
-    if (S > max_split) S = max_split;
-    if (S > kMaxSplits) S = kMaxSplits;
-    if (S < 1) S = 1;
-    int t = (s.cap + S - 1) / S;
-    t = (t + 15) / 16 * 16;
-    *tps = t;
-    return (s.cap + t - 1) / t;
+    if (W > 65535) W = 65535;
+    return W < 1 ? 1 : int(W);
 }
 
-size_t paged_workspace_bytes(const PagedShape &s, int splits) {
-    if (splits <= 1) return 0;
-    const size_t rows = size_t(s.B) * s.Hkv * s.Mq * splits;
-    return align256(rows * s.D * sizeof(float)) + align256(rows * sizeof(float));
+// Partials of the shared requests: per (head block, worker) two slots (the
+// worker's first and last segment) of HB heads x Mq rows.
+size_t paged_workspace_bytes(const PagedShape &s, int workers) {
+    if (workers <= 1) return 0;
+    const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
+    const size_t nhb = (s.Hkv + hb - 1) / hb;
+    const size_t rows = nhb * size_t(workers) * 2 * hb * s.Mq;
+    const size_t prefix = s.topk_form ? 0 : align256((size_t(s.B) + 1) * sizeof(long long));
+    return align256(rows * s.D * sizeof(float)) + align256(rows * sizeof(float)) + prefix;
+}
+
+// Points the kernel arguments at the partial buffers inside a workspace of
+// paged_workspace_bytes(s, workers) bytes.
+void paged_bind_workspace(const PagedShape &s, int workers, void *ws, PagedArgs *a) {
+    const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
+    const size_t rows = size_t((s.Hkv + hb - 1) / hb) * workers * 2 * hb * s.Mq;
+    char *p = static_cast<char *>(ws);
+    a->o_part = reinterpret_cast<float *>(p);
+    p += align256(rows * s.D * sizeof(float));
+    a->lse_part = reinterpret_cast<float *>(p);
+    p += align256(rows * sizeof(float));
+    a->step_prefix = s.topk_form ? nullptr : reinterpret_cast<long long *>(p);
 }
 
 }  // namespace
@@ -558,7 +574,6 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     a.topk_n = topk;
     a.Sq = 1;
     a.Mq = a.G;
-    a.num_splits = 1;
     a.alpha = resolve_scale(scale, D) * k_scale * 1.4426950408889634f;
     a.v_scale = v_scale;
     a.wait_limit_ns = g_wait_limit_ns.load();
@@ -567,10 +582,43 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     if (!current_device(&dev)) return GQA_ERR_CUDA;
     a.err = error_word(dev);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // Balanced schedule: one worker per resident CTA slot per head block.
+    PagedShape ps_;
+    std::memset(&ps_, 0, sizeof(ps_));
+    ps_.B = B;
+    ps_.Sq = 1;
+    ps_.Hq = Hq;
+    ps_.Hkv = Hkv;
+    ps_.D = D;
+    ps_.G = a.G;
+    ps_.Mq = a.G;
+    ps_.kv8 = true;
+    ps_.topk_form = true;
+    const int workers = choose_paged_workers(ps_, 0, dev);
+    a.num_splits = workers;
+    // Equal lists: a request is shared by two workers only when some worker
+    // boundary floor(w T / W) falls inside it.
+    bool shared = false;
+    {
+        const long steps = (long(topk) + kPagedStageTokens - 1) / kPagedStageTokens;
+        const long T = steps * B;
+        for (long w = 1; w < workers && steps > 0 && !shared; ++w) shared = (w * T / workers) % steps != 0;
+    }
+    const size_t need = shared ? paged_workspace_bytes(ps_, workers) : 0;
+    void *ws = nullptr;
+    if (need > 0) {
+        if (pool_alloc(&ws, need, dev, cs) != cudaSuccess) {
+            cudaGetLastError();
+            return GQA_ERR_NO_MEMORY;
+        }
+        paged_bind_workspace(ps_, workers, ws, &a);
+    }
     cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
     if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
     cudaError_t pe = launch_paged_topk_fp8(a, D, cs);
     if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
+    if (pe == cudaSuccess && shared) pe = launch_paged_topk_combine_fp8(a, D, cs);
+    if (ws != nullptr) cudaFreeAsync(ws, cs);
     if (pe != cudaSuccess) {
         cudaGetLastError();
         return GQA_ERR_CUDA;
@@ -596,9 +644,7 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
         return GQA_ERR_ALIGNMENT;
     int dev = 0;
     if (!current_device(&dev)) return GQA_ERR_CUDA;
-    int tps = 0;
-    const int splits = choose_paged_splits(s, num_splits, dev, &tps);
-    if (splits > 65535) return GQA_ERR_UNSUPPORTED;
+    const int splits = choose_paged_workers(s, num_splits, dev);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = paged_workspace_bytes(s, splits);
     void *ws = workspace;
@@ -624,11 +670,7 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
     a.seq_lens = seq_lens;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
-    if (need > 0) {
-        const size_t rows = size_t(s.B) * s.Hkv * s.Mq * splits;
-        a.o_part = static_cast<float *>(ws);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + align256(rows * s.D * sizeof(float)));
-    }
+    if (need > 0) paged_bind_workspace(s, splits, ws, &a);
     a.B = B;
     a.Sq = Sq;
     a.Hq = Hq;
@@ -639,7 +681,6 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
     a.pages_per_req = pages_per_req;
     a.num_pages = num_pages;
     a.num_splits = splits;
-    a.tokens_per_split = tps;
     a.alpha = resolve_scale(scale, D) * (s.kv8 ? k_scale : 1.0f) * 1.4426950408889634f;
     a.v_scale = s.kv8 ? v_scale : 1.0f;
     a.wait_limit_ns = g_wait_limit_ns.load();
@@ -650,7 +691,7 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
     cudaError_t e = s.kv8 ? launch_paged_range_fp8(a, D, cs) : launch_paged_range_bf16(a, D, cs);
     if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
     if (e == cudaSuccess && splits > 1)
-        e = launch_combine_partials(D, a.o_part, a.lse_part, a.out, lse, B, Sq, Hq, Hkv, s.G, s.Mq, splits, cs);
+        e = s.kv8 ? launch_paged_range_combine_fp8(a, D, cs) : launch_paged_range_combine_bf16(a, D, cs);
     if (owned) cudaFreeAsync(ws, cs);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -674,8 +715,7 @@ int gqa_decode_paged_num_splits(int B, int Sq, int Hq, int Hkv, int D, int kv_dt
     if (st != GQA_OK) return -int(st);
     int dev = 0;
     if (!current_device(&dev)) return -int(GQA_ERR_CUDA);
-    int tps = 0;
-    return choose_paged_splits(s, 0, dev, &tps);
+    return choose_paged_workers(s, 0, dev);
 }
 
 size_t gqa_decode_paged_workspace_bytes(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int page_size,
@@ -685,8 +725,7 @@ size_t gqa_decode_paged_workspace_bytes(int B, int Sq, int Hq, int Hkv, int D, i
         return 0;
     int dev = 0;
     if (num_splits == 0 && !current_device(&dev)) return 0;
-    int tps = 0;
-    return paged_workspace_bytes(s, choose_paged_splits(s, num_splits, dev, &tps));
+    return paged_workspace_bytes(s, choose_paged_workers(s, num_splits, dev));
 }
 
 gqa_status gqa_paged_gather_fp8(const uint8_t *pool, const int32_t *page_table, const int32_t *topk_idx, uint8_t *out,

@@ -72,10 +72,14 @@ inline int paged_heads_per_cta(int D, bool kv8, int Mq, int Hkv) {
     return hb;
 }
 cudaError_t launch_paged_topk_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+int paged_topk_ctas_per_sm_fp8(const PagedArgs &a, int D);
+cudaError_t launch_paged_topk_combine_fp8(const PagedArgs &a, int D, cudaStream_t stream);
 cudaError_t launch_paged_range_fp8(const PagedArgs &a, int D, cudaStream_t stream);
 cudaError_t launch_paged_range_bf16(const PagedArgs &a, int D, cudaStream_t stream);
 int paged_range_ctas_per_sm_fp8(const PagedArgs &a, int D);
 int paged_range_ctas_per_sm_bf16(const PagedArgs &a, int D);
+cudaError_t launch_paged_range_combine_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+cudaError_t launch_paged_range_combine_bf16(const PagedArgs &a, int D, cudaStream_t stream);
 cudaError_t launch_combine_d64(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
                                int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
 cudaError_t launch_combine_d128(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,

@@ -21,7 +21,8 @@ static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
     // Programmatic dependent launch: the CTAs may be scheduled while the
     // previous kernel in the stream drains; they wait for it before reading.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.Hkv + HB - 1) / HB, a.B, RANGE ? a.num_splits : 1);
+    // (head block, worker of the balanced schedule)
+    cfg.gridDim = dim3((a.Hkv + HB - 1) / HB, a.num_splits, 1);
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.stream = stream;
@@ -61,6 +62,22 @@ static long paged_dispatch_nt(const PagedArgs &a, cudaStream_t stream, int op) {
     }
 #undef GQA_PAGED_CASE
     return op == 0 ? long(cudaErrorInvalidValue) : 0L;
+}
+
+// Merge of the shared requests' partials (whole-request form, several workers).
+template <int D>
+static cudaError_t launch_paged_combine(const PagedArgs &a, int hb, cudaStream_t stream) {
+    const long rows = long(a.B) * a.Hkv * a.Mq;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gqa_paged_combine_kernel<D>, a, hb);
 }
 
 template <bool KV8, bool RANGE>

@@ -96,7 +96,8 @@ struct PagedCfg {
     static constexpr int BAR_OFF = STAGES * STAGE_BYTES;             // full[STAGES], empty[STAGES]
     static constexpr int MASK_OFF = BAR_OFF + 2 * STAGES * 8;        // valid-token mask per stage
     static constexpr int FLAG_OFF = MASK_OFF + STAGES * 4;           // abort flag
-    static constexpr int ROWS_OFF = (FLAG_OFF + 4 + 15) / 16 * 16;   // physical rows of the pass
+    static constexpr int SCHED_OFF = (FLAG_OFF + 4 + 7) / 8 * 8;     // balanced schedule (4 longs)
+    static constexpr int ROWS_OFF = (SCHED_OFF + 32 + 15) / 16 * 16; // physical rows of the pass
     static constexpr int SMEM_BYTES = ROWS_OFF + kPagedChunk * 4;
     static constexpr int IPT = (kPagedChunk + THREADS - 1) / THREADS;  // index-map entries per thread
     static constexpr int MIN_BLOCKS_FIT = (220 * 1024) / (SMEM_BYTES + 1024);
@@ -139,8 +140,6 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.y;
-    const int split = blockIdx.z;
     const int hb0 = blockIdx.x * HB;
     const int nh = min(HB, a.Hkv - hb0);  // heads of this CTA
     const bool producer = warp == HB;
@@ -161,22 +160,126 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
     __syncthreads();     // barriers and flag initialised before anyone reads them
     pdl_wait_primary();  // inputs may be written by the previous kernel in the stream
 
-    // ---- the tokens of this CTA: the top-K list, or the request's own
-    // tokens [t_begin, t_end) of this split.
     bool bad = false;
-    int n_tok = a.topk_n;
-    int t_begin = 0;
-    int seq_len = 0;
-    if constexpr (RANGE) {
-        seq_len = __ldg(a.seq_lens + b);
+    // ---- balanced schedule.  Request b holds len_b tokens (its top-K list,
+    // or its own tokens 0 .. seq_len-1), i.e. ceil(len_b / 16) steps; worker
+    // w = blockIdx.y of W = num_splits takes global steps
+    // [w T / W, (w+1) T / W) of the T steps of all requests, in request
+    // order, as segments of consecutive requests.
+    int seg_b = 0;   // request of the current segment
+    long seg_p = 0;  // its first global step
+    long w_begin = 0, w_end = 0;
+    if constexpr (!RANGE) {
+        // every list has topk_n entries: the schedule in closed form
+        const long steps = (a.topk_n + C::T - 1) / C::T;
+        const long T = steps * a.B;
+        const int W = a.num_splits;
+        w_begin = long(blockIdx.y) * T / W;
+        w_end = (long(blockIdx.y) + 1) * T / W;
+        seg_b = steps > 0 ? int(w_begin / steps) : 0;
+        seg_p = long(seg_b) * steps;
+    } else {
+        long* sched = reinterpret_cast<long *>(psmem + C::SCHED_OFF);
+        if (warp == 0) {
+            const int W = a.num_splits;
+            const int cap = a.pages_per_req * a.page_size;
+            long T = 0;
+            for (int b0 = 0; b0 < a.B; b0 += 32) {
+                const int bb = b0 + lane;
+                int len = bb >= a.B ? 0 : RANGE ? __ldg(a.seq_lens + bb) : a.topk_n;
+                len = len < 0 ? 0 : (len > cap ? cap : len);
+                long st = (len + C::T - 1) / C::T;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) st += __shfl_xor_sync(0xffffffffu, st, off);
+                T += st;
+            }
+            if (a.step_prefix != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
+                // every request's first global step, for the combine kernel
+                long Q = 0;
+                for (int b0 = 0; b0 < a.B; b0 += 32) {
+                    const int bb = b0 + lane;
+                    int len = bb < a.B ? __ldg(a.seq_lens + bb) : 0;
+                    len = len < 0 ? 0 : (len > cap ? cap : len);
+                    const long st = (len + C::T - 1) / C::T;
+                    long incl = st;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const long y = __shfl_up_sync(0xffffffffu, incl, off);
+                        if (lane >= off) incl += y;
+                    }
+                    if (bb < a.B) a.step_prefix[bb] = Q + incl - st;
+                    Q += __shfl_sync(0xffffffffu, incl, 31);
+                }
+                if (lane == 0) a.step_prefix[a.B] = Q;
+            }
+            const long start = long(blockIdx.y) * T / W, end = (long(blockIdx.y) + 1) * T / W;
+            // first request whose steps reach past `start`
+            long P = 0;
+            int first = a.B;
+            long first_p = T;
+            for (int b0 = 0; b0 < a.B && first == a.B; b0 += 32) {
+                const int bb = b0 + lane;
+                int len = bb >= a.B ? 0 : RANGE ? __ldg(a.seq_lens + bb) : a.topk_n;
+                len = len < 0 ? 0 : (len > cap ? cap : len);
+                const long st = (len + C::T - 1) / C::T;
+                long incl = st;  // inclusive prefix over the 32 requests of this chunk
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const long y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += y;
+                }
+                // An empty request at step P counts as reaching P + 1: it belongs to
+                // the worker whose range holds P (the last worker when P = T).
+                const bool hit = bb < a.B && P + incl - st + (st > 0 ? st : 1) > start;
+                const unsigned m = __ballot_sync(0xffffffffu, hit);
+                if (m != 0u) {
+                    const int l = __ffs(m) - 1;
+                    first = b0 + l;
+                    first_p = P + __shfl_sync(0xffffffffu, incl - st, l);
+                }
+                P += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) {
+                sched[0] = start;
+                sched[1] = end;
+                sched[2] = first;
+                sched[3] = first_p;
+            }
+        }
+        __syncthreads();
+        w_begin = sched[0];
+        w_end = sched[1];
+        seg_b = int(sched[2]);
+        seg_p = sched[3];
+    }
+    long seg_t = w_begin;  // global step where the current segment starts
+
+    const size_t row_bytes = size_t(a.Hkv) * C::ROWB;
+    const uint32_t piece = uint32_t(nh) * C::ROWB;
+    bool failed = false;
+    int gs0 = 0;     // global step index of the pass's first step (mbarrier phases)
+    int issued = 0;  // producer: steps issued so far (all of 0 .. issued-1)
+
+    const bool last_worker = int(blockIdx.y) == a.num_splits - 1;
+    while (seg_b < a.B && (seg_t < w_end || (last_worker && seg_t == w_end))) {
+    // ---- the current segment: tokens [t_begin, t_begin + n_tok) of request seg_b
+    const int b = seg_b;
+    int seq_len = RANGE ? __ldg(a.seq_lens + b) : a.topk_n;  // tokens of the request (list length in top-K form)
+    {
         const int cap = a.pages_per_req * a.page_size;
         if (seq_len < 0 || seq_len > cap) {
             bad = true;
             seq_len = seq_len < 0 ? 0 : cap;
         }
-        t_begin = split * a.tokens_per_split;
-        n_tok = max(0, min(t_begin + a.tokens_per_split, seq_len) - t_begin);
     }
+    const long steps_b = (seq_len + C::T - 1) / C::T;
+    const long seg_next = min(w_end, seg_p + steps_b);
+    const int t_begin = int(seg_t - seg_p) * C::T;  // first token (list entry) of the segment
+    const int n_tok = min(int(seg_next - seg_p) * C::T, seq_len) - t_begin;
+    // the segment is the whole request: write the final output; otherwise a
+    // partial in slot 0 (the worker's first segment) or 1 (its last)
+    const bool complete = seg_t == seg_p && seg_next == seg_p + steps_b;
+    const int slot = seg_t == w_begin ? 0 : 1;
 
     // ---- Q^T fragments.  Lane gi holds query row gi (+8 per n-tile) at the
     // elements k_dbase(kk, c) .. +3.  FP8 pools: f16 with a per-row
@@ -253,12 +356,6 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
     }
     const bool causal = RANGE && a.Sq > 1;
 
-    const size_t row_bytes = size_t(a.Hkv) * C::ROWB;
-    const uint32_t piece = uint32_t(nh) * C::ROWB;
-    bool failed = false;
-    int gs0 = 0;     // global step index of the pass's first step (mbarrier phases)
-    int issued = 0;  // producer: steps issued so far (all of 0 .. issued-1)
-
     for (int base_k = 0; base_k < n_tok; base_k += kPagedChunk) {
         const int cn = min(kPagedChunk, n_tok - base_k);
         __syncthreads();  // previous pass fully consumed
@@ -272,7 +369,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
             if constexpr (RANGE)
                 tk[u] = k < cn ? t_begin + base_k + k : -1;
             else
-                tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + base_k + k) : -1;
+                tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + t_begin + base_k + k) : -1;
         }
 #pragma unroll
         for (int u = 0; u < C::IPT; ++u) {
@@ -482,6 +579,75 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
         }
         gs0 += steps;
     }
+    // ---- epilogue of the segment.  Lane holds rows r = 8 nt + 2c + e at the
+    // head-dim elements out_d(t, 0|1, gi) of o[nt][t][e] / o[nt][t][2 + e].
+    //  whole request: out = [sigmoid(gate) *] v_scale * O / l (bf16), LSE (natural log);
+    //  shared request: fp32 partial v_scale * O / l and the log2-domain LSE in
+    //  the worker's slot, merged by the combine kernel.
+    if (active && !failed && !*abort_flag) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float L = l_run[nt][e];
+                L += __shfl_xor_sync(0xffffffffu, L, 4);
+                L += __shfl_xor_sync(0xffffffffu, L, 8);
+                L += __shfl_xor_sync(0xffffffffu, L, 16);
+                const int r = 8 * nt + 2 * c + e;
+                if (r >= a.Mq) continue;
+                const int i = r / a.G;
+                const int h = g * a.G + r % a.G;
+                const float f = L > 0.f ? a.v_scale / L : 0.f;
+                const float lse2 = L > 0.f ? m_run[nt][e] + log2f(L) : -INFINITY;
+                if (!complete) {
+                    const size_t prow =
+                        ((((size_t(blockIdx.x) * a.num_splits + blockIdx.y) * 2 + slot) * HB + warp) * a.Mq) + r;
+                    float *dst = a.o_part + prow * D;
+#pragma unroll
+                    for (int t = 0; t < C::DB; ++t)
+                        *reinterpret_cast<float2 *>(dst + out_d<D, KV8>(t, 0, gi)) =
+                            make_float2(o[nt][t][e] * f, o[nt][t][2 + e] * f);
+                    if (gi == 0) a.lse_part[prow] = lse2;
+                    continue;
+                }
+                const size_t off = ((size_t(b) * a.Sq + i) * a.Hq + h) * D;
+                uint32_t graw[C::DB];
+#pragma unroll
+                for (int t = 0; t < C::DB; ++t)
+                    graw[t] = a.gate != nullptr
+                                  ? __ldg(reinterpret_cast<const unsigned int *>(a.gate + off + out_d<D, KV8>(t, 0, gi)))
+                                  : 0u;
+                uint32_t packed[C::DB];
+#pragma unroll
+                for (int t = 0; t < C::DB; ++t) {
+                    float s0 = 1.f, s1 = 1.f;
+                    if (a.gate != nullptr) {
+                        const float g0 = __uint_as_float(graw[t] << 16);
+                        const float g1 = __uint_as_float(graw[t] & 0xffff0000u);
+                        s0 = __fdividef(1.f, 1.f + __expf(-g0));
+                        s1 = __fdividef(1.f, 1.f + __expf(-g1));
+                    }
+                    packed[t] = pack_bf16x2(o[nt][t][e] * f * s0, o[nt][t][2 + e] * f * s1);
+                }
+                // output d-blocks 4q .. 4q+3 are 8 contiguous elements
+#pragma unroll
+                for (int q4 = 0; q4 < C::DB / 4; ++q4)
+                    *reinterpret_cast<uint4 *>(a.out + off + out_d<D, KV8>(4 * q4, 0, gi)) =
+                        make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
+                if (a.lse != nullptr && gi == 0)
+                    a.lse[(size_t(b) * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
+            }
+    }
+    __syncthreads();  // every warp's view of the abort flag is the same below
+    if (*abort_flag) break;
+    // ---- next segment
+    if (seg_next == seg_p + steps_b) {  // request finished: on to the next one
+        seg_p = seg_next;
+        ++seg_b;
+    }
+    seg_t = seg_next;
+    }  // segment loop
+
     if (bad) flag_error(a.err, kErrIndex);
     if (producer) {
         // Every copy this CTA issued must land before its shared memory is
@@ -492,65 +658,101 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
             if (lane == 0 && !mbar_wait_bounded(full + st, (last / C::STAGES) & 1, a.wait_limit_ns, nullptr))
                 flag_error(a.err, kErrTimeout);
         }
-        return;
     }
-    if (!active || *abort_flag) return;
+}
 
-    // ---- epilogue.  Lane holds rows r = 8 nt + 2c + e at the head-dim
-    // elements out_d(t, 0|1, gi) of o[nt][t][e] / o[nt][t][2 + e].
-    //  one split: out = gate ? sigmoid(gate) * v_scale * O / l : v_scale * O / l (bf16), LSE (natural log);
-    //  several: fp32 partials v_scale * O / l and the log2-domain LSE for the combine kernel.
+
+// Merge of the partials of requests shared by several workers of the
+// balanced whole-request form.  One warp per output row (b, h, i): the warp
+// recomputes the schedule (T, the request's first step and step count, the
+// workers w_first .. w_last holding its steps), returns when the request lies
+// within one worker (that worker wrote the final output), and otherwise
+// merges the workers' partials with weights 2^(lse_w - max) (a partial that
+// saw no visible token has lse = -inf and weight 0).
+template <int D>
+__global__ void __launch_bounds__(128) gqa_paged_combine_kernel(const PagedArgs a, int HB) {
+    pdl_wait_primary();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned row = blockIdx.x * 4u + unsigned(warp);  // (b * Hkv + g) * Mq + r  (< 2^31)
+    if (row >= unsigned(a.B) * unsigned(a.Hkv) * unsigned(a.Mq)) return;
+    const unsigned unit = row / unsigned(a.Mq);
+    const int r = int(row - unit * unsigned(a.Mq));
+    const int b = int(unit / unsigned(a.Hkv));
+    const int g = int(unit - unsigned(b) * unsigned(a.Hkv));
+    long T, Pb, steps_b;
+    if (a.seq_lens == nullptr) {  // top-K form: every list has topk_n entries
+        const long steps = (a.topk_n + kPagedStageTokens - 1) / kPagedStageTokens;
+        T = steps * a.B;
+        Pb = steps * b;
+        steps_b = steps;
+    } else {  // whole-request form: the main kernel recorded every request's first step
+        Pb = a.step_prefix[b];
+        steps_b = a.step_prefix[b + 1] - Pb;
+        T = a.step_prefix[a.B];
+    }
+    if (steps_b == 0) return;  // written by the worker that walked it
+    const long W = a.num_splits;
+    // floor(x / y) for the schedule's products; 32-bit when they fit (the
+    // common case: 64-bit division is a long instruction sequence)
+    const bool narrow = (unsigned long long)(T + 1) * (unsigned long long)(W + 1) < (1ull << 32);
+    auto qdiv = [narrow](long x, long y) -> long {
+        return narrow ? long(unsigned(x) / unsigned(y)) : x / y;
+    };
+    // worker holding global step s: the largest w with floor(w T / W) <= s
+    const long w_first = qdiv((Pb + 1) * W - 1, T);
+    const long w_last = qdiv((Pb + steps_b) * W - 1, T);
+    if (w_first == w_last) return;
+    const int hb = g / HB, lh = g % HB;
+    constexpr int V = D / 32;  // values per lane
+    float m = -INFINITY, L = 0.f;
+    float acc[V];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            float L = l_run[nt][e];
-            L += __shfl_xor_sync(0xffffffffu, L, 4);
-            L += __shfl_xor_sync(0xffffffffu, L, 8);
-            L += __shfl_xor_sync(0xffffffffu, L, 16);
-            const int r = 8 * nt + 2 * c + e;
-            if (r >= a.Mq) continue;
-            const int i = r / a.G;
-            const int h = g * a.G + r % a.G;
-            const float f = L > 0.f ? a.v_scale / L : 0.f;
-            const float lse2 = L > 0.f ? m_run[nt][e] + log2f(L) : -INFINITY;
-            if (a.num_splits > 1) {
-                const size_t prow = ((size_t(b) * a.Hkv + g) * a.Mq + r) * a.num_splits + split;
-                float *dst = a.o_part + prow * D;
-#pragma unroll
-                for (int t = 0; t < C::DB; ++t)
-                    *reinterpret_cast<float2 *>(dst + out_d<D, KV8>(t, 0, gi)) =
-                        make_float2(o[nt][t][e] * f, o[nt][t][2 + e] * f);
-                if (gi == 0) a.lse_part[prow] = lse2;
-                continue;
-            }
-            const size_t off = ((size_t(b) * a.Sq + i) * a.Hq + h) * D;
-            uint32_t graw[C::DB];
-#pragma unroll
-            for (int t = 0; t < C::DB; ++t)
-                graw[t] = a.gate != nullptr
-                              ? __ldg(reinterpret_cast<const unsigned int *>(a.gate + off + out_d<D, KV8>(t, 0, gi)))
-                              : 0u;
-            uint32_t packed[C::DB];
-#pragma unroll
-            for (int t = 0; t < C::DB; ++t) {
-                float s0 = 1.f, s1 = 1.f;
-                if (a.gate != nullptr) {
-                    const float g0 = __uint_as_float(graw[t] << 16);
-                    const float g1 = __uint_as_float(graw[t] & 0xffff0000u);
-                    s0 = 1.f / (1.f + __expf(-g0));
-                    s1 = 1.f / (1.f + __expf(-g1));
-                }
-                packed[t] = pack_bf16x2(o[nt][t][e] * f * s0, o[nt][t][2 + e] * f * s1);
-            }
-            // output d-blocks 4q .. 4q+3 are 8 contiguous elements
-#pragma unroll
-            for (int q4 = 0; q4 < C::DB / 4; ++q4)
-                *reinterpret_cast<uint4 *>(a.out + off + out_d<D, KV8>(4 * q4, 0, gi)) =
-                    make_uint4(packed[4 * q4], packed[4 * q4 + 1], packed[4 * q4 + 2], packed[4 * q4 + 3]);
-            if (a.lse != nullptr && gi == 0)
-                a.lse[(size_t(b) * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    long w_start = qdiv(w_first * T, W);
+    for (long w = w_first; w <= w_last; ++w) {
+        const long w_next = qdiv((w + 1) * T, W);
+        const bool empty_range = w_start == w_next;  // a worker with no steps holds nothing
+        const int slot = (w == w_first && w_start < Pb) ? 1 : 0;
+        w_start = w_next;
+        if (empty_range) continue;
+        const size_t prow = ((((size_t(hb) * W + w) * 2 + slot) * HB + lh) * a.Mq) + r;
+        const float l2 = __ldg(a.lse_part + prow);
+        float x[V];
+        if constexpr (V == 4) {
+            const float4 x4 = __ldg(reinterpret_cast<const float4 *>(a.o_part + prow * D) + lane);
+            x[0] = x4.x;
+            x[1] = x4.y;
+            x[2] = x4.z;
+            x[3] = x4.w;
+        } else {
+            const float2 x2 = __ldg(reinterpret_cast<const float2 *>(a.o_part + prow * D) + lane);
+            x[0] = x2.x;
+            x[1] = x2.y;
         }
+        if (l2 == -INFINITY) continue;
+        const float mn = fmaxf(m, l2);
+        const float sc = fast_exp2(m - mn), wgt = fast_exp2(l2 - mn);
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = acc[v] * sc + wgt * x[v];
+        L = L * sc + wgt;
+        m = mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int i = r / a.G;
+    const int h = g * a.G + r % a.G;
+    const size_t off = ((size_t(b) * a.Sq + i) * a.Hq + h) * D + lane * V;
+#pragma unroll
+    for (int v = 0; v < V; v += 2) {
+        float s0 = 1.f, s1 = 1.f;
+        if (a.gate != nullptr) {  // sigmoid gate (top-K form)
+            const uint32_t graw = __ldg(reinterpret_cast<const unsigned int *>(a.gate + off + v));
+            s0 = __fdividef(1.f, 1.f + __expf(-__uint_as_float(graw << 16)));
+            s1 = __fdividef(1.f, 1.f + __expf(-__uint_as_float(graw & 0xffff0000u)));
+        }
+        *reinterpret_cast<uint32_t *>(a.out + off + v) = pack_bf16x2(acc[v] * inv * s0, acc[v + 1] * inv * s1);
+    }
+    if (a.lse != nullptr && lane == 0)
+        a.lse[(size_t(b) * a.Hq + h) * a.Sq + i] = L > 0.f ? (m + __log2f(L)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace gqa

@@ -47,10 +47,11 @@ struct PagedArgs {
     const int32_t *seq_lens;    // [B] (whole-request form)
     __nv_bfloat16 *out;         // [B, Sq, Hq, D]
     float *lse;                 // [B, Hq, Sq] or null
-    float *o_part;              // [B*Hkv, Mq, num_splits, D] fp32 (num_splits > 1)
-    float *lse_part;            // [B*Hkv, Mq, num_splits] fp32, log2 domain (num_splits > 1)
+    float *o_part;              // whole-request form, shared requests: [head block, worker, 2 slots, HB, Mq, D] fp32
+    float *lse_part;            // [head block, worker, 2 slots, HB, Mq] fp32, log2 domain
+    long long *step_prefix;     // whole-request form, several workers: [B + 1] first global step of each request
     int B, Sq, Hq, Hkv, G, Mq, page_size, pages_per_req, num_pages, topk_n;
-    int num_splits, tokens_per_split;  // whole-request form
+    int num_splits;             // whole-request form: workers per head block
     float alpha;    // scale * k_scale * log2(e)
     float v_scale;
     unsigned long long wait_limit_ns;

@@ -100,6 +100,14 @@ CONFIGS = {
     "paged_fp8_b256_h32x8_d128_top512_ps16": PagedConfig(
         "paged_fp8_b256_h32x8_d128_top512_ps16", B=256, Hq=32, Hkv=8, D=128, page_size=16,
         pages_per_req=32, num_pages=8192, topk=512, seed=1005),
+    # whole requests through page tables (the serving layout): the batched
+    # 32 x 32K shape, page size 16, lengths uniform in [16K, 32K]
+    "paged_bf16_b32_h64x8_d128_kv32k_ps16": PagedKVConfig(
+        "paged_bf16_b32_h64x8_d128_kv32k_ps16", B=32, Sq=1, Hq=64, Hkv=8, D=128, page_size=16,
+        pages_per_req=2048, kv_dtype="bf16", seed=1006),
+    "paged_fp8_b32_h64x8_d128_kv32k_ps16": PagedKVConfig(
+        "paged_fp8_b32_h64x8_d128_kv32k_ps16", B=32, Sq=1, Hq=64, Hkv=8, D=128, page_size=16,
+        pages_per_req=2048, kv_dtype="fp8", seed=1007),
 }
 
 # The configuration the headline throughput is quoted on (a long 128K cache,
@@ -218,11 +226,19 @@ def paged_kv_inputs(B, Sq, Hq, Hkv, D, page_size, pages_per_req, num_pages, seed
     perm = torch.randperm(num_pages, generator=g, device=device)[: B * pages_per_req]
     page_table = perm.view(B, pages_per_req).to(torch.int32).contiguous()
     if seq_lens is None:
-        lo = max(Sq, cap // 2)
-        seq_lens = torch.randint(lo, cap + 1, (B,), generator=g, device=device, dtype=torch.int64)
-    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32, device=device).contiguous()
+        seq_lens = paged_kv_seq_lens(B, Sq, cap, seed)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32).to(device).contiguous()
     return dict(q=q, k_pool=k_pool.contiguous(), v_pool=v_pool.contiguous(), k_scale=float(k_scale),
                 v_scale=float(v_scale), page_table=page_table, seq_lens=seq_lens, page_size=page_size)
+
+
+def paged_kv_seq_lens(B, Sq, cap, seed) -> torch.Tensor:
+    """Request lengths uniform in [max(Sq, cap / 2), cap], drawn on the CPU from
+    their own seed, so a configuration has the same lengths (and KV bytes) on
+    every device."""
+    g = torch.Generator().manual_seed(seed + 7919)
+    lo = max(Sq, cap // 2)
+    return torch.randint(lo, cap + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
 
 
 def paged_kv_config_inputs(cfg: PagedKVConfig, device="cpu"):

@@ -182,7 +182,11 @@ gqa_status gqa_decode_host(const void *q_host, const void *k_host, const void *v
  *         topk <= 65536; num_pages * page_size < 2^31.
  * Indices are trusted for speed; a t >= pages_per_req * page_size or a page
  * id outside [0, num_pages) is skipped and flags GQA_ERR_DEVICE_INDEX in the
- * device error word.  No workspace.
+ * device error word.  Small batches (requests filling less than half of the
+ * GPU's resident CTA slots) are spread over all slots by splitting lists
+ * between CTAs; their fp32 partials live in a workspace allocated
+ * stream-ordered from a library-owned pool and are merged (gate included) by
+ * a second kernel.  Larger batches use one CTA per request and no workspace.
  * ------------------------------------------------------------------------ */
 gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
                                 const uint8_t *k_pool, const uint8_t *v_pool,
@@ -204,9 +208,15 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
  * gqa_decode), and
  *   s_t = scale * q[b,i,h,:] . K^_t,  K^ = k * k_scale,  V^ = v * v_scale,
  *   out[b,i,h,:] = softmax(s) V^,  lse[b,h,i] = ln sum_t exp(s_t).
- * A row that sees no token gives out = 0 and lse = -inf.  Each request's
- * tokens may be split over several CTAs; the fp32 partials are merged by the
- * same LSE-weighted combine as gqa_decode's.
+ * A row that sees no token gives out = 0 and lse = -inf.
+ *
+ * Schedule: for each block of KV heads, W workers (CTAs) share the
+ * T = sum_b ceil(seq_lens[b] / 16) steps of 16 tokens of all requests
+ * equally -- worker w takes steps [w T / W, (w+1) T / W) in request order --
+ * so the load is balanced whatever the length mix.  A request covered by one
+ * worker is written directly; one spread over several workers leaves fp32
+ * partials (O / l, log2-domain LSE) that a merge kernel combines with
+ * LSE weights.  W defaults to one worker per resident CTA slot.
  *
  * q, out : device bf16 [B, Sq, Hq, D].  lse : device fp32 [B, Hq, Sq] or NULL.
  * k_pool, v_pool : device [num_pages, page_size, Hkv, D] of bf16
@@ -219,10 +229,11 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
  * Device-checked: a seq_lens[b] outside [0, pages_per_req * page_size] is
  *   clamped into it, and a page id outside [0, num_pages) is skipped; both
  *   flag GQA_ERR_DEVICE_INDEX in the device error word.
- * Workspace: gqa_decode_paged allocates its split partials stream-ordered
- *   from a library-owned pool; gqa_decode_paged_ex takes num_splits (0 =
- *   automatic) and an optional caller workspace (256-byte aligned, at least
- *   gqa_decode_paged_workspace_bytes; NULL = library pool).
+ * Workspace: gqa_decode_paged allocates the partials stream-ordered from a
+ *   library-owned pool; gqa_decode_paged_ex takes num_splits = W, the workers
+ *   per head block (0 = automatic), and an optional caller workspace
+ *   (256-byte aligned, at least gqa_decode_paged_workspace_bytes; NULL =
+ *   library pool).
  * ------------------------------------------------------------------------ */
 typedef enum { GQA_KV_BF16 = 0, GQA_KV_FP8_E4M3FN = 1 } gqa_kv_dtype;
 
@@ -239,7 +250,7 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
                                int pages_per_req, int num_pages, float scale, int num_splits,
                                void *workspace, size_t workspace_bytes, gqa_stream_t stream);
 
-/* Token splits per request the automatic choice uses for this shape on the
+/* Workers per head block the automatic choice uses for this shape on the
  * current device (negative gqa_status on invalid arguments). */
 int gqa_decode_paged_num_splits(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype,
                                 int page_size, int pages_per_req);

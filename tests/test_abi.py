@@ -157,9 +157,10 @@ def test_paged_kv_sizes(lib):
     assert lib.gqa_decode_paged_num_splits(2, 1, 8, 2, 96, 0, 16, 4) == -2
     assert lib.gqa_decode_paged_num_splits(2, 1, 6, 4, 128, 0, 16, 4) == -1
     assert lib.gqa_decode_paged_workspace_bytes(2, 1, 8, 2, 96, 0, 16, 4, 3) == 0
-    # explicit splits need no device: 2 requests x 2 heads x 4 rows x 3 splits
-    rows = 2 * 2 * 4 * 3
-    want = ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    # explicit worker counts need no device: 1 head block of 2 heads x 3 workers x
+    # 2 partial slots x 4 rows
+    rows = 1 * 3 * 2 * 2 * 4
+    want = ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256 + 256  # + step prefix of 3 longs
     assert lib.gqa_decode_paged_workspace_bytes(2, 1, 8, 2, 128, 0, 16, 64, 3) == want
     assert lib.gqa_decode_paged_workspace_bytes(2, 1, 8, 2, 128, 0, 16, 64, 1) == 0
 

@@ -79,11 +79,26 @@ def test_paged_kv_small_vs_oracle(gq, orc, shape, splits):
     assert gq.gqa_device_status() == 0
 
 
+@pytest.mark.parametrize("lens,workers", [((0, 0, 32), 31), ((0, 0, 0), 4), ((1, 0, 5, 0), 9),
+                                          ((700, 3, 0, 260), 200), ((64, 64), 3)])
+def test_balanced_schedule_edges(gq, orc, lens, workers):
+    """More workers than 16-token steps, empty requests between and after
+    shared ones, an all-empty batch."""
+    B = len(lens)
+    inp = gqa_inputs.paged_kv_inputs(B, 1, 16, 4, 64, 16, 48, B * 48 + 1, seed=50 + sum(lens), kv_dtype="bf16",
+                                     seq_lens=list(lens))
+    out, lse = _run(gq, inp, num_splits=workers)
+    ref_o, ref_l = _ref(orc, inp, 0.125)
+    _check(out, lse, ref_o, ref_l, f"balanced {lens} W={workers}")
+    assert gq.gqa_device_status() == 0
+
+
 def test_split_counts_agree(gq):
+    """Worker counts from one (every request whole in one CTA) to more workers
+    than steps agree within rounding."""
     inp = gqa_inputs.paged_kv_inputs(4, 1, 32, 8, 128, 16, 64, 300, seed=41, kv_dtype="bf16")
     ref, ref_l = _run(gq, inp, num_splits=1)
-    cap = 64 * 16
-    for s in (2, 3, 7, cap // 16):
+    for s in (2, 3, 7, 64, 300):
         out, lse = _run(gq, inp, num_splits=s)
         assert torch.allclose(out.float(), ref.float(), atol=2e-2, rtol=2e-2), s
         assert torch.allclose(lse, ref_l, atol=1e-3, rtol=0), s
@@ -139,3 +154,35 @@ def test_automatic_splits_reported(gq):
     assert n >= 1
     assert gq.gqa_decode_paged_workspace_bytes(4, 1, 32, 8, 128, 0, 16, 256) == (
         0 if n == 1 else gq.gqa_decode_paged_workspace_bytes(4, 1, 32, 8, 128, 0, 16, 256, n))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["paged_bf16_b32_h64x8_d128_kv32k_ps16", "paged_fp8_b32_h64x8_d128_kv32k_ps16"])
+def test_full_workload_sampled_rows(gq, orc, name):
+    """The benchmark workloads at full size, in the launch configuration the
+    benchmark times (automatic splits); sampled rows of three requests checked
+    against the oracle on a compact copy of just those requests' pages."""
+    cfg = gqa_inputs.CONFIGS[name]
+    inp = gqa_inputs.paged_kv_config_inputs(cfg, device="cuda")
+    out, lse = gq.gqa_decode_paged(inp["q"], inp["k_pool"], inp["v_pool"], inp["page_table"], inp["seq_lens"],
+                                   inp["k_scale"], inp["v_scale"])
+    torch.cuda.synchronize()
+    assert gq.gqa_device_status() == 0
+    reqs = [0, 17, cfg.B - 1]
+    pt = inp["page_table"][reqs].long()                       # [3, ppr] pool pages
+    kc = inp["k_pool"][pt.flatten()].cpu()                    # compact pools: request j's pages at j*ppr ..
+    vc = inp["v_pool"][pt.flatten()].cpu()
+    ppr = cfg.pages_per_req
+    ptc = torch.arange(len(reqs) * ppr, dtype=torch.int32).view(len(reqs), ppr)
+    sl = inp["seq_lens"][reqs].cpu()
+    qc = inp["q"][reqs].cpu()
+    rng = np.random.default_rng(7)
+    nrow = cfg.Hq * cfg.Sq
+    rows = sorted({0, len(reqs) * nrow - 1} | set(int(x) for x in rng.integers(0, len(reqs) * nrow, 40)))
+    ref_o, ref_l = orc.gqa_decode_paged(qc, kc, vc, ptc, sl, cfg.scale, inp["k_scale"], inp["v_scale"], rows=rows)
+    og = out[reqs].cpu()                                      # [3, Sq, Hq, D]
+    lg = lse[reqs].cpu()                                      # [3, Hq, Sq]
+    got_o = torch.stack([og[r // nrow, r % cfg.Sq, (r // cfg.Sq) % cfg.Hq] for r in rows])
+    got_l = torch.stack([lg[r // nrow, (r // cfg.Sq) % cfg.Hq, r % cfg.Sq] for r in rows])
+    assert_o_close(got_o, ref_o, name)
+    assert_lse_close(got_l, ref_l, name)
