@@ -630,6 +630,77 @@ def run_reference(args) -> int:
     return 0
 
 
+def run_latency_grid(args) -> int:
+    """Small-cache decode latency over the grid the portability study measured
+    (32/8 heads, d 128, bf16, Sq 1; batch 1 .. 32 x KV length 512 .. 16384):
+    per cell the automatic split count, device time per call (CUDA events,
+    L2 flushed, median of 20), and host time per call back to back, eager
+    and replayed from a captured CUDA graph.  One JSON line per cell."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from gqa_decode_attention_gb300 import build as gbuild
+    gbuild.build()
+    import gqa_decode_attention_gb300 as gq
+    gq.load_library()
+    flush_w = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones((512 << 20) // 8, dtype=torch.int64, device=dev)
+
+    def device_us(fn, n=20):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n):
+            flush_w.zero_()
+            flush_r.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    def host_us(fn, n=200):
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / n * 1e6
+
+    Hq, Hkv, D = 32, 8, 128
+    for B in (1, 8, 32):
+        for N in (512, 2048, 16384):
+            q, k, v = gqa_inputs.dense_inputs(B, 1, N, Hq, Hkv, D, 7, device=dev)
+            out = torch.empty_like(q)
+            lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
+
+            def call():
+                gq.gqa_decode(q, k, v, out=out, lse=lse)
+            d_us = device_us(call)
+            h_eager = host_us(call)
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                call()
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    call()
+            torch.cuda.current_stream().wait_stream(side)
+            h_graph = host_us(g.replay)
+            nbytes = kv_bytes(B, Hkv, N, D, 2)
+            print(json.dumps({"B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "D": D,
+                              "splits": gq.gqa_decode_num_splits(B, 1, N, Hq, Hkv, D),
+                              "device_us": round(d_us, 2), "gbs": round(gbs(nbytes, d_us * 1e-3), 1),
+                              "host_us_eager": round(h_eager, 2), "host_us_graph": round(h_graph, 2)}), flush=True)
+            del q, k, v, out, lse, g
+    return 0
+
+
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -642,6 +713,8 @@ def main(argv=None) -> int:
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--latency-grid", action="store_true",
+                   help="small-cache latency sweep (eager and CUDA graph) instead of the benchmark line")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
     if args.skv:
@@ -654,6 +727,8 @@ def main(argv=None) -> int:
         args.config = name
     if args.impl == "reference":
         return run_reference(args)
+    if args.latency_grid:
+        return run_latency_grid(args)
     return run_gqa(args)
 
 

@@ -244,3 +244,33 @@ def test_full_size_sampled_rows(gq, orc, cfg):
         assert_o_close(got_o, ref_o, f"{cfg.name} b={b} g={g}")
         assert_lse_close(got_l, ref_l, f"{cfg.name} b={b} g={g}")
         print(cfg.name, b, g, diagnostics(got_o, ref_o))
+
+
+def test_cuda_graph_capture_and_replay(gq, orc):
+    """The decode call (split kernel, programmatically dependent combine and
+    the stream-ordered workspace from the library pool) can be captured in a
+    CUDA graph; replays recompute from the current inputs."""
+    B, Sq, Skv, Hq, Hkv, D = 2, 1, 3000, 32, 8, 128
+    q, k, v = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=77, device="cuda")
+    assert gq.gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D) > 1
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        gq.gqa_decode(q, k, v, out=out, lse=lse)  # first call outside capture (pool, attributes)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            gq.gqa_decode(q, k, v, out=out, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    for seed in (78, 79):
+        q2, _, _ = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=seed, device="cuda")
+        q.copy_(q2)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        ref_o, ref_l = orc.gqa_decode(q.cpu(), k.cpu(), v.cpu(), 1.0 / math.sqrt(D))
+        assert_o_close(out.cpu(), ref_o, "graph replay")
+        assert_lse_close(lse.cpu(), ref_l, "graph replay lse")
+    assert gq.gqa_device_status() == 0
