@@ -17,8 +17,8 @@ library is benchmarked on):
   N(0, 1) with a per-tensor scale amax / 448;
 * paged decode over whole requests (the serving layout: no top-K, every
   token of each request up to its own length): q [B, Sq, Hq, D] bf16, K/V
-  pools [num_pages, page_size, Hkv, D] in bf16 (N(0, 1) rounded) or FP8
-  E4M3FN (quantised as above), each request's pages a random permutation of
+  pools [num_pages, page_size, Hkv, D] in bf16 (N(0, 1) rounded), FP8
+  E4M3FN (quantised as above) or int8 (symmetric per-tensor, scale amax/127), each request's pages a random permutation of
   the pool, sequence lengths drawn uniformly from [capacity / 2, capacity]
   (a length mix), or given.
 """
@@ -76,7 +76,7 @@ class PagedKVConfig:
     D: int
     page_size: int
     pages_per_req: int
-    kv_dtype: str  # "bf16" or "fp8"
+    kv_dtype: str  # "bf16", "fp8" or "int8"
     seed: int
 
     @property
@@ -158,6 +158,18 @@ def quantize_e4m3fn(x: torch.Tensor):
     return y.to(torch.float8_e4m3fn).view(torch.uint8), scale
 
 
+def quantize_int8(x: torch.Tensor):
+    """Per-tensor symmetric int8 codes of x with scale amax/127 (test data only).
+
+    Returns (codes int8, scale float); codes = round-to-nearest-even(x / scale)
+    clamped to [-127, 127].
+    """
+    amax = float(x.abs().max())
+    scale = amax / 127.0 if amax > 0 else 1.0
+    y = torch.round(x / scale).clamp_(-127, 127)
+    return y.to(torch.int8), scale
+
+
 def paged_inputs(B, Hq, Hkv, D, page_size, pages_per_req, num_pages, topk, seed,
                  device="cpu", pad_tail: int = 0):
     """Sparse paged FP8 inputs.
@@ -202,12 +214,13 @@ def paged_kv_inputs(B, Sq, Hq, Hkv, D, page_size, pages_per_req, num_pages, seed
     """Paged inputs over whole requests.
 
     Returns dict with q [B,Sq,Hq,D] bf16; k_pool, v_pool [num_pages,
-    page_size, Hkv, D] (bf16, or uint8 E4M3FN codes for kv_dtype "fp8");
+    page_size, Hkv, D] (bf16, uint8 E4M3FN codes for kv_dtype "fp8", or int8
+    codes for "int8");
     k_scale, v_scale floats (1.0 for bf16); page_table int32 [B, pages_per_req]
     (distinct pages from a random permutation of the pool); seq_lens int32 [B]
     (given, or uniform in [capacity / 2, capacity]).
     """
-    assert B * pages_per_req <= num_pages and kv_dtype in ("bf16", "fp8")
+    assert B * pages_per_req <= num_pages and kv_dtype in ("bf16", "fp8", "int8")
     cap = pages_per_req * page_size
     g = _gen(seed, device)
     q = _randn_bf16((B, Sq, Hq, D), g, device)
@@ -217,11 +230,12 @@ def paged_kv_inputs(B, Sq, Hq, Hkv, D, page_size, pages_per_req, num_pages, seed
         v_pool = _randn_bf16(shape, g, device)
         k_scale = v_scale = 1.0
     else:
+        quant = quantize_e4m3fn if kv_dtype == "fp8" else quantize_int8
         kx = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
-        k_pool, k_scale = quantize_e4m3fn(kx)
+        k_pool, k_scale = quant(kx)
         del kx
         vx = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
-        v_pool, v_scale = quantize_e4m3fn(vx)
+        v_pool, v_scale = quant(vx)
         del vx
     perm = torch.randperm(num_pages, generator=g, device=device)[: B * pages_per_req]
     page_table = perm.view(B, pages_per_req).to(torch.int32).contiguous()

@@ -27,8 +27,8 @@ attention):
   "Implementations": attention over the selected tokens with k_scale in the
   scores, v_scale on the values, then a sigmoid gate.
 * ``gqa_decode_paged`` -- the same page-table addressing without a top-K list:
-  every token of each request up to its own sequence length, bf16 or FP8
-  pools, the dense path's bottom-right mask per request (the serving layout
+  every token of each request up to its own sequence length, bf16, FP8 or
+  int8 pools, the dense path's bottom-right mask per request (the serving layout
   both pages leave as an open question).
 """
 from __future__ import annotations
@@ -88,6 +88,8 @@ def _as_u8(x) -> np.ndarray:
             t = t.view(torch.uint8)
         return np.ascontiguousarray(t.numpy())
     a = np.ascontiguousarray(x)
+    if a.dtype == np.int8:
+        a = a.view(np.uint8)
     assert a.dtype == np.uint8, a.dtype
     return a
 
@@ -225,20 +227,23 @@ class Oracle:
 
     # -- paged, whole requests -------------------------------------------
     def gqa_decode_paged(self, q, k_pool, v_pool, page_table, seq_lens, scale: float,
-                         k_scale: float = 1.0, v_scale: float = 1.0, rows=None):
+                         k_scale: float = 1.0, v_scale: float = 1.0, rows=None, kv_type=None):
         """Paged decode over every token of each request (no top-K).
 
-        q [B,Sq,Hq,D] bf16; pools [num_pages, ps, Hkv, D] of bf16 or E4M3FN
-        codes (uint8 / float8 tensors); page_table [B, ppr] int32; seq_lens [B]
-        int32.  Returns (O, LSE): O [B,Sq,Hq,D] and LSE [B,Hq,Sq] float64, or
+        q [B,Sq,Hq,D] bf16; pools [num_pages, ps, Hkv, D] of bf16, E4M3FN codes
+        (uint8 / float8 tensors) or int8 codes (int8 tensors); kv_type 0/1/2
+        overrides the inference from the pool dtype; page_table [B, ppr] int32;
+        seq_lens [B] int32.  Returns (O, LSE): O [B,Sq,Hq,D] and LSE [B,Hq,Sq] float64, or
         with ``rows`` (flattened ids (b*Hq + h)*Sq + i) O [n,D] and LSE [n].
         """
         qa = _as_u16(q)
-        kv_fp8 = not (hasattr(k_pool, "dtype") and str(k_pool.dtype) in ("torch.bfloat16", "uint16"))
-        if kv_fp8:
-            ka, va = _as_u8(k_pool), _as_u8(v_pool)
-        else:
+        dt = str(k_pool.dtype) if hasattr(k_pool, "dtype") else ""
+        if kv_type is None:
+            kv_type = 0 if dt in ("torch.bfloat16", "uint16") else 2 if dt in ("torch.int8", "int8") else 1
+        if kv_type == 0:
             ka, va = _as_u16(k_pool), _as_u16(v_pool)
+        else:
+            ka, va = _as_u8(k_pool), _as_u8(v_pool)
         pt, sl = _as_i32(page_table), _as_i32(seq_lens)
         B, Sq, Hq, D = qa.shape
         _, ps, Hkv, D2 = ka.shape
@@ -256,7 +261,7 @@ class Oracle:
         lse = np.zeros((n,), dtype=np.float64)
         self._lib.oracle_gqa_decode_paged(
             _p(qa, _u16_p), ka.ctypes.data_as(ctypes.c_void_p), va.ctypes.data_as(ctypes.c_void_p),
-            int(kv_fp8), float(k_scale), float(v_scale), _p(pt, _i32_p), _p(sl, _i32_p),
+            int(kv_type), float(k_scale), float(v_scale), _p(pt, _i32_p), _p(sl, _i32_p),
             B, Sq, Hq, Hkv, D, ps, ppr, float(scale), rp, n, _p(out, _dbl_p), _p(lse, _dbl_p))
         if rows is not None:
             return out, lse

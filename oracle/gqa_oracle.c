@@ -23,6 +23,11 @@
  *    request, up to its own sequence length) is the serving layout the
  *    kv-copies page's "Open questions" and the FP8 page's "Workload" point
  *    to; its masking follows the dense rule below, per request.
+ *  - "Profiling down to the register, then an extension that broke my
+ *    assumptions twice", paragraph "int8 KV-cache" and section "What's still
+ *    open": an int8 KV cache dequantised tile by tile inside the attention
+ *    kernel.  The format is not printed; the reading taken here is the
+ *    symmetric per-tensor one (value = int8 code * scale).
  *  - The masking rule for S_q > 1 is not printed on the pages; the reading
  *    taken here is bottom-right alignment: query row i of S_q sees keys
  *    j <= S_kv - S_q + i.
@@ -305,19 +310,24 @@ void oracle_gqa_decode_paged_fp8(const uint16_t *q, const uint16_t *gate,
 /* paged decode over whole requests (no top-K), bf16 or FP8 pools       */
 /* ------------------------------------------------------------------ */
 
-/* Value of element d of pool row `row` (byte offset of the row's first element
- * divided by the element size): a bf16 pattern, or an E4M3FN code. */
-static double pool_value(const void *pool, int kv_fp8, size_t row, int d)
+/* Value of element d of pool row `row` (offset of the row's first element):
+ * kv_type 0 = a bf16 pattern, 1 = an E4M3FN code, 2 = a two's-complement
+ * int8 code. */
+static double pool_value(const void *pool, int kv_type, size_t row, int d)
 {
-    if (kv_fp8)
+    if (kv_type == 1)
         return oracle_e4m3fn_value(((const uint8_t *)pool)[row + d]);
+    if (kv_type == 2) {
+        int8_t c = ((const int8_t *)pool)[row + d];
+        return PLANT(13) ? (double)(uint8_t)c : (double)c;
+    }
     return bf16_value(((const uint16_t *)pool)[row + d]);
 }
 
 /*
  * q : bf16 [B, Sq, Hq, D]
- * k_pool, v_pool : [num_pages, ps, Hkv, D] of bf16 patterns (kv_fp8 = 0) or
- *                  E4M3FN codes (kv_fp8 = 1)
+ * k_pool, v_pool : [num_pages, ps, Hkv, D] of bf16 patterns (kv_type 0),
+ *                  E4M3FN codes (kv_type 1) or int8 codes (kv_type 2)
  * page_table : int32 [B, ppr]      seq_lens : int32 [B], 0 <= seq_lens[b] <= ppr*ps
  * rows : optional list of flattened row ids r = (b*Hq + h)*Sq + i; NULL = all.
  * out : [n_rows, D] double        lse : [n_rows] double (natural log)
@@ -325,12 +335,14 @@ static double pool_value(const void *pool, int kv_fp8, size_t row, int d)
  * Request b holds tokens t = 0 .. seq_lens[b]-1, token t at page
  * page_table[b][t / ps], slot t % ps.  Query row i of Sq sees tokens
  * t <= seq_lens[b] - Sq + i (bottom-right alignment, as in the dense case).
- * K^ = val(k) * k_scale, V^ = val(v) * v_scale (pass 1 for bf16 pools),
+ * K^ = val(k) * k_scale, V^ = val(v) * v_scale (pass 1 for bf16 pools; an
+ * int8 code c has the value c, the per-tensor scale gives the dequantised
+ * value, the usual symmetric int8 cache format),
  * s_t = scale * q.K^_t, LSE = m + ln sum_t exp(s_t - m),
  * O = sum_t exp(s_t - LSE) V^_t.  A row that sees no token has O = 0 and
  * LSE = -inf.
  */
-void oracle_gqa_decode_paged(const uint16_t *q, const void *k_pool, const void *v_pool, int kv_fp8,
+void oracle_gqa_decode_paged(const uint16_t *q, const void *k_pool, const void *v_pool, int kv_type,
                              double k_scale, double v_scale,
                              const int32_t *page_table, const int32_t *seq_lens,
                              int B, int Sq, int Hq, int Hkv, int D, int ps, int ppr,
@@ -362,7 +374,7 @@ void oracle_gqa_decode_paged(const uint16_t *q, const void *k_pool, const void *
                 row_at[t] = pool_row(p, slot, g, ps, Hkv, D);
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d)
-                    dot += bf16_value(qrow[d]) * (pool_value(k_pool, kv_fp8, row_at[t], d) * ks);
+                    dot += bf16_value(qrow[d]) * (pool_value(k_pool, kv_type, row_at[t], d) * ks);
                 s[t] = scale * dot;
                 if (s[t] > m)
                     m = s[t];
@@ -377,7 +389,7 @@ void oracle_gqa_decode_paged(const uint16_t *q, const void *k_pool, const void *
             for (long t = 0; t <= last && t < len; ++t) {
                 double w = exp(s[t] - L);
                 for (int d = 0; d < D; ++d)
-                    o[d] += w * (pool_value(v_pool, kv_fp8, row_at[t], d) * vs);
+                    o[d] += w * (pool_value(v_pool, kv_type, row_at[t], d) * vs);
             }
             if (lse)
                 lse[n] = L;

@@ -430,6 +430,26 @@ def pin_paged_fp8_equals_bf16(orc):
     assert np.array_equal(O8, Ob) and np.array_equal(L8, Lb)
 
 
+def pin_paged_int8_equals_bf16(orc):
+    """An int8 pool with power-of-two k_scale != v_scale equals a bf16 pool that
+    holds the dequantised values (code * scale, exact in bf16 for |code| <= 128),
+    bit for bit; codes at both ends of the range (-128, 127) included."""
+    q, _, _, pt, sl = _paged_kv_small(2000)
+    g = torch.Generator().manual_seed(2001)
+    shape = (pt.numel() + 3, 4, 2, 16)
+    k8 = torch.randint(-128, 128, shape, generator=g, dtype=torch.int16).to(torch.int8)
+    v8 = torch.randint(-128, 128, shape, generator=g, dtype=torch.int16).to(torch.int8)
+    k8.view(-1)[:2] = torch.tensor([-128, 127], dtype=torch.int8)
+    v8.view(-1)[:2] = torch.tensor([127, -128], dtype=torch.int8)
+    ks, vs = 0.0078125, 0.25
+    kb = (k8.double() * ks).to(torch.bfloat16)
+    vb = (v8.double() * vs).to(torch.bfloat16)
+    assert torch.equal(kb.double(), k8.double() * ks) and torch.equal(vb.double(), v8.double() * vs)
+    O8, L8 = orc.gqa_decode_paged(q, k8, v8, pt, sl, 0.3, ks, vs)
+    Ob, Lb = orc.gqa_decode_paged(q, kb, vb, pt, sl, 0.3)
+    assert np.array_equal(O8, Ob) and np.array_equal(L8, Lb)
+
+
 def pin_paged_zero_keys_and_short_requests(orc):
     """K = 0: LSE = ln(#visible tokens) and O = the mean of the visible V rows
     (numpy over the fancy-indexed cache); a request shorter than S_q leaves its
@@ -457,5 +477,6 @@ DENSE_PINS = [pin_bruteforce_dense, pin_library_dense, pin_gqa_equals_expanded_m
               pin_zero_keys, pin_constant_v, pin_single_key, pin_zero_scale, pin_hardmax]
 PAGED_PINS = [pin_e4m3fn_table, pin_paged_gather, pin_bruteforce_paged, pin_paged_equals_dense,
               pin_topk_order_and_padding, pin_gate_and_scales]
-PAGED_KV_PINS = [pin_paged_requests_equal_dense, pin_paged_fp8_equals_bf16, pin_paged_zero_keys_and_short_requests]
+PAGED_KV_PINS = [pin_paged_requests_equal_dense, pin_paged_fp8_equals_bf16, pin_paged_int8_equals_bf16,
+                 pin_paged_zero_keys_and_short_requests]
 ALL_PINS = DENSE_PINS + PAGED_PINS + PAGED_KV_PINS

@@ -6,8 +6,8 @@ about (the two wrong head maps of the kv-copies-gqa head-map table) plus the
 plausible slips in each step: an off-by-one or top-left causal mask, a
 dropped log-sum in the LSE, a dropped softmax scale, page and slot swapped,
 an ungated (identity) gate, the wrong FP8 exponent bias, a dropped v_scale,
-and for whole-request paged decode an ignored sequence length or swapped
-K / V scales.
+and for whole-request paged decode an ignored sequence length, swapped
+K / V scales or int8 codes read as unsigned.
 """
 import os
 
@@ -29,6 +29,7 @@ MUTANTS = {
     10: "top-left causal alignment",
     11: "paged: per-request sequence length ignored",
     12: "paged: k_scale and v_scale swapped",
+    13: "paged: int8 codes read as unsigned",
 }
 
 
