@@ -81,7 +81,7 @@ def workload_config(cfg) -> dict:
         return {"workload": cfg.name, "B": cfg.B, "Sq": cfg.Sq, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
                 "page_size": cfg.page_size, "pages_per_req": cfg.pages_per_req, "num_pages": cfg.num_pages,
                 "seq_lens": f"uniform in [{max(cfg.Sq, cap // 2)}, {cap}], total {sum(lens)} tokens",
-                "kv_dtype": "bf16" if cfg.kv_dtype == "bf16" else "fp8_e4m3fn"}
+                "kv_dtype": {"bf16": "bf16", "fp8": "fp8_e4m3fn", "int8": "int8"}[cfg.kv_dtype]}
     return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D,
             "page_size": cfg.page_size, "pages_per_req": cfg.pages_per_req, "num_pages": cfg.num_pages,
             "topk": cfg.topk, "kv_dtype": "fp8_e4m3fn"}
@@ -90,6 +90,8 @@ def workload_config(cfg) -> dict:
 def workload_dtype(cfg) -> str:
     if isinstance(cfg, gqa_inputs.DenseConfig) or (isinstance(cfg, gqa_inputs.PagedKVConfig) and cfg.kv_dtype == "bf16"):
         return "bf16"
+    if isinstance(cfg, gqa_inputs.PagedKVConfig) and cfg.kv_dtype == "int8":
+        return "int8 kv, bf16 q/out, f16 mma"
     return "fp8_e4m3fn kv, bf16 q/out, f16 mma"
 
 
@@ -290,7 +292,8 @@ def _make_call(gq, cfg, dev, seed_offset):
             gq.gqa_decode_paged(inp["q"], inp["k_pool"], inp["v_pool"], inp["page_table"], inp["seq_lens"],
                                 inp["k_scale"], inp["v_scale"], out=out, lse=lse)
         splits = gq.gqa_decode_paged_num_splits(cfg.B, cfg.Sq, cfg.Hq, cfg.Hkv, cfg.D,
-                                                0 if cfg.kv_dtype == "bf16" else 1, cfg.page_size, cfg.pages_per_req)
+                                                {"bf16": 0, "fp8": 1, "int8": 2}[cfg.kv_dtype], cfg.page_size,
+                                                cfg.pages_per_req)
         return call, dict(inp, out=out, lse=lse), (2 if splits > 1 else 1), splits
     inp = gqa_inputs.paged_inputs(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
                                   cfg.num_pages, cfg.topk, cfg.seed + seed_offset, device=dev)

@@ -241,6 +241,7 @@ def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale,
 
 GQA_KV_BF16 = 0
 GQA_KV_FP8_E4M3FN = 1
+GQA_KV_INT8 = 2
 
 
 def _kv_dtype(k_pool) -> int:
@@ -248,15 +249,18 @@ def _kv_dtype(k_pool) -> int:
         return GQA_KV_BF16
     if k_pool.dtype == torch.uint8:
         return GQA_KV_FP8_E4M3FN
-    raise TypeError(f"k_pool: expected bfloat16 or uint8 (E4M3FN codes), got {k_pool.dtype}")
+    if k_pool.dtype == torch.int8:
+        return GQA_KV_INT8
+    raise TypeError(f"k_pool: expected bfloat16, uint8 (E4M3FN codes) or int8, got {k_pool.dtype}")
 
 
 def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_scale=1.0, out=None, lse=None,
                      scale=None, num_splits=0, workspace=None, stream=None, with_lse=True):
     """Paged decode over every token of each request (no top-K).
 
-    q [B,Sq,Hq,D] bf16; pools [num_pages, page_size, Hkv, D] of bf16, or of
-    uint8 E4M3FN codes (then k_scale / v_scale apply); page_table int32
+    q [B,Sq,Hq,D] bf16; pools [num_pages, page_size, Hkv, D] of bf16, of
+    uint8 E4M3FN codes or of int8 codes (for 8-bit codes k_scale / v_scale
+    apply); page_table int32
     [B, pages_per_req]; seq_lens int32 [B].  num_splits 0 = automatic;
     workspace: optional CUDA uint8 tensor of gqa_decode_paged_workspace_bytes.
     Returns (out [B,Sq,Hq,D] bf16, lse [B,Hq,Sq] fp32 or None).

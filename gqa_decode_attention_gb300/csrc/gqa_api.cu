@@ -309,7 +309,8 @@ gqa_status check_paged(int B, int Hq, int Hkv, int D, int page_size, int pages_p
 
 struct PagedShape {
     int B, Sq, Hq, Hkv, D, G, Mq, ps, ppr, num_pages, cap;
-    bool kv8;
+    int kvt;         // GQA_KV_BF16 / GQA_KV_FP8_E4M3FN / GQA_KV_INT8
+    bool kv8;        // 8-bit codes (FP8 or int8)
     bool topk_form;  // the sparse top-K form (FP8, gated) rather than whole requests
 };
 
@@ -318,7 +319,8 @@ gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, i
     if (B < 1 || Sq < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || pages_per_req < 1 || num_pages < 1)
         return GQA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
-    if (kv_dtype != GQA_KV_BF16 && kv_dtype != GQA_KV_FP8_E4M3FN) return GQA_ERR_INVALID_ARG;
+    if (kv_dtype != GQA_KV_BF16 && kv_dtype != GQA_KV_FP8_E4M3FN && kv_dtype != GQA_KV_INT8)
+        return GQA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
     const long G = Hq / Hkv;
     if (G * Sq > 16) return GQA_ERR_UNSUPPORTED;
@@ -336,17 +338,18 @@ gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, i
     s->ppr = pages_per_req;
     s->num_pages = num_pages;
     s->cap = pages_per_req * page_size;
-    s->kv8 = kv_dtype == GQA_KV_FP8_E4M3FN;
+    s->kvt = kv_dtype;
+    s->kv8 = kv_dtype != GQA_KV_BF16;
     s->topk_form = false;
     return GQA_OK;
 }
 
 // Resident CTAs per SM of the paged instance serving shape s (cached).
 int paged_occupancy(int dev, const PagedShape &s) {
-    static int cache[kMaxDevices][3][2][2][4];  // [dev][form][D][two n-tiles][log2 heads per CTA]
+    static int cache[kMaxDevices][4][2][2][4];  // [dev][form][D][two n-tiles][log2 heads per CTA]
     const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
     const int lh = hb == 1 ? 0 : hb == 2 ? 1 : hb == 4 ? 2 : 3;
-    const int form = s.topk_form ? 2 : s.kv8 ? 1 : 0;
+    const int form = s.topk_form ? 3 : s.kvt;
     std::lock_guard<std::mutex> lk(g_mu);
     int &slot = cache[dev][form][s.D == 128][s.Mq > 8][lh];
     if (slot == 0) {
@@ -354,9 +357,10 @@ int paged_occupancy(int dev, const PagedShape &s) {
         std::memset(&a, 0, sizeof(a));
         a.Hkv = s.Hkv;
         a.Mq = s.Mq;
-        slot = s.topk_form ? paged_topk_ctas_per_sm_fp8(a, s.D)
-               : s.kv8     ? paged_range_ctas_per_sm_fp8(a, s.D)
-                           : paged_range_ctas_per_sm_bf16(a, s.D);
+        slot = s.topk_form                  ? paged_topk_ctas_per_sm_fp8(a, s.D)
+               : s.kvt == GQA_KV_INT8        ? paged_range_ctas_per_sm_int8(a, s.D)
+               : s.kvt == GQA_KV_FP8_E4M3FN ? paged_range_ctas_per_sm_fp8(a, s.D)
+                                            : paged_range_ctas_per_sm_bf16(a, s.D);
     }
     return slot;
 }
@@ -592,6 +596,7 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     ps_.D = D;
     ps_.G = a.G;
     ps_.Mq = a.G;
+    ps_.kvt = GQA_KV_FP8_E4M3FN;
     ps_.kv8 = true;
     ps_.topk_form = true;
     const int workers = choose_paged_workers(ps_, 0, dev);
@@ -688,10 +693,14 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
     a.err = error_word(dev);
     cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
     if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
-    cudaError_t e = s.kv8 ? launch_paged_range_fp8(a, D, cs) : launch_paged_range_bf16(a, D, cs);
+    cudaError_t e = s.kvt == GQA_KV_INT8        ? launch_paged_range_int8(a, D, cs)
+                    : s.kvt == GQA_KV_FP8_E4M3FN ? launch_paged_range_fp8(a, D, cs)
+                                                 : launch_paged_range_bf16(a, D, cs);
     if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
     if (e == cudaSuccess && splits > 1)
-        e = s.kv8 ? launch_paged_range_combine_fp8(a, D, cs) : launch_paged_range_combine_bf16(a, D, cs);
+        e = s.kvt == GQA_KV_INT8        ? launch_paged_range_combine_int8(a, D, cs)
+            : s.kvt == GQA_KV_FP8_E4M3FN ? launch_paged_range_combine_fp8(a, D, cs)
+                                         : launch_paged_range_combine_bf16(a, D, cs);
     if (owned) cudaFreeAsync(ws, cs);
     if (e != cudaSuccess) {
         cudaGetLastError();

@@ -61,8 +61,9 @@ int dense_ctas_per_sm_d128(int cfg);
 int dense_ctas_per_sm_d256(int cfg);
 
 // Paged kernel.  Heads per CTA: the smallest power of two covering Hkv, at
-// most the number whose row pieces fit 1 KiB per token (8 FP8 heads of 128,
-// 4 bf16 heads of 128), and at most 4 when a consumer holds two n-tiles.
+// most the number whose row pieces fit 1 KiB per token (8 heads of 128 with
+// 8-bit codes, 4 bf16 heads of 128), and at most 4 when a consumer holds two
+// n-tiles.
 inline int paged_heads_per_cta(int D, bool kv8, int Mq, int Hkv) {
     int cap = 1024 / (D * (kv8 ? 1 : 2));
     if (cap > 8) cap = 8;
@@ -79,6 +80,9 @@ cudaError_t launch_paged_range_bf16(const PagedArgs &a, int D, cudaStream_t stre
 int paged_range_ctas_per_sm_fp8(const PagedArgs &a, int D);
 int paged_range_ctas_per_sm_bf16(const PagedArgs &a, int D);
 cudaError_t launch_paged_range_combine_fp8(const PagedArgs &a, int D, cudaStream_t stream);
+cudaError_t launch_paged_range_int8(const PagedArgs &a, int D, cudaStream_t stream);
+int paged_range_ctas_per_sm_int8(const PagedArgs &a, int D);
+cudaError_t launch_paged_range_combine_int8(const PagedArgs &a, int D, cudaStream_t stream);
 cudaError_t launch_paged_range_combine_bf16(const PagedArgs &a, int D, cudaStream_t stream);
 cudaError_t launch_combine_d64(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
                                int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);

@@ -35,9 +35,9 @@ __global__ void gqa_fp8_to_f32_kernel(const uint8_t *codes, float *out, int n) {
 
 
 cudaError_t launch_paged_topk_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
-    return cudaError_t(paged_dispatch<true, false>(a, D, stream, 0));
+    return cudaError_t(paged_dispatch<kKvFp8, false>(a, D, stream, 0));
 }
-int paged_topk_ctas_per_sm_fp8(const PagedArgs &a, int D) { return int(paged_dispatch<true, false>(a, D, nullptr, 1)); }
+int paged_topk_ctas_per_sm_fp8(const PagedArgs &a, int D) { return int(paged_dispatch<kKvFp8, false>(a, D, nullptr, 1)); }
 cudaError_t launch_paged_topk_combine_fp8(const PagedArgs &a, int D, cudaStream_t stream) {
     const int hb = paged_heads_per_cta(D, true, a.Mq, a.Hkv);
     return D == 64 ? launch_paged_combine<64>(a, hb, stream) : launch_paged_combine<128>(a, hb, stream);

@@ -8,10 +8,10 @@
 
 namespace gqa {
 
-template <int D, int NT, int HB, bool KV8, bool RANGE>
+template <int D, int NT, int HB, int KVT, bool RANGE>
 static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
-    using C = PagedCfg<D, NT, HB, KV8>;
-    auto kern = gqa_paged_kernel<D, NT, HB, KV8, RANGE>;
+    using C = PagedCfg<D, NT, HB, KVT != kKvBf16>;
+    auto kern = gqa_paged_kernel<D, NT, HB, KVT, RANGE>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -34,10 +34,10 @@ static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int D, int NT, int HB, bool KV8, bool RANGE>
+template <int D, int NT, int HB, int KVT, bool RANGE>
 static int paged_occupancy_inst() {
-    using C = PagedCfg<D, NT, HB, KV8>;
-    auto kern = gqa_paged_kernel<D, NT, HB, KV8, RANGE>;
+    using C = PagedCfg<D, NT, HB, KVT != kKvBf16>;
+    auto kern = gqa_paged_kernel<D, NT, HB, KVT, RANGE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;
@@ -47,13 +47,14 @@ static int paged_occupancy_inst() {
 
 // Dispatch over (n-tiles, heads per CTA).  op 0 launches, op 1 returns the
 // resident CTAs per SM of the chosen instance (as a cudaError_t-sized int).
-template <int D, int NT, bool KV8, bool RANGE>
+template <int D, int NT, int KVT, bool RANGE>
 static long paged_dispatch_nt(const PagedArgs &a, cudaStream_t stream, int op) {
+    constexpr bool KV8 = KVT != kKvBf16;
     const int hb = paged_heads_per_cta(D, KV8, a.Mq, a.Hkv);
 #define GQA_PAGED_CASE(HBV)                                                                              \
     if (hb == HBV)                                                                                       \
-        return op == 0 ? long(launch_paged_inst<D, NT, HBV, KV8, RANGE>(a, stream))                      \
-                       : long(paged_occupancy_inst<D, NT, HBV, KV8, RANGE>());
+        return op == 0 ? long(launch_paged_inst<D, NT, HBV, KVT, RANGE>(a, stream))                      \
+                       : long(paged_occupancy_inst<D, NT, HBV, KVT, RANGE>());
     GQA_PAGED_CASE(1)
     GQA_PAGED_CASE(2)
     GQA_PAGED_CASE(4)
@@ -80,11 +81,11 @@ static cudaError_t launch_paged_combine(const PagedArgs &a, int hb, cudaStream_t
     return cudaLaunchKernelEx(&cfg, gqa_paged_combine_kernel<D>, a, hb);
 }
 
-template <bool KV8, bool RANGE>
+template <int KVT, bool RANGE>
 static long paged_dispatch(const PagedArgs &a, int D, cudaStream_t stream, int op) {
     const bool two = a.Mq > 8;  // 9..16 rows use two n-tiles of 8 rows
-    if (D == 64) return two ? paged_dispatch_nt<64, 2, KV8, RANGE>(a, stream, op) : paged_dispatch_nt<64, 1, KV8, RANGE>(a, stream, op);
-    if (D == 128) return two ? paged_dispatch_nt<128, 2, KV8, RANGE>(a, stream, op) : paged_dispatch_nt<128, 1, KV8, RANGE>(a, stream, op);
+    if (D == 64) return two ? paged_dispatch_nt<64, 2, KVT, RANGE>(a, stream, op) : paged_dispatch_nt<64, 1, KVT, RANGE>(a, stream, op);
+    if (D == 128) return two ? paged_dispatch_nt<128, 2, KVT, RANGE>(a, stream, op) : paged_dispatch_nt<128, 1, KVT, RANGE>(a, stream, op);
     return op == 0 ? long(cudaErrorInvalidValue) : 0L;
 }
 

@@ -70,6 +70,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
+// Two int8 codes (low byte first) as f16x2, exactly: a code x biased to
+// x + 128 in [0, 255] becomes the mantissa of the f16 1024 + (x + 128)
+// (exponent 2^10, where f16 counts in units of one), and 1152 is subtracted.
+__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t two) {
+    const uint32_t h = prmt(uint32_t(two) ^ 0x8080u, 0x6464u, 0x5140u);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
+// K/V element types of the paged kernel.
+enum : int { kKvBf16 = 0, kKvFp8 = 1, kKvInt8 = 2 };
+
+// Two 8-bit codes (FP8 E4M3FN or int8) widened to f16x2, exactly.
+template <int KVT>
+__device__ __forceinline__ uint32_t widen8(uint16_t two) {
+    if constexpr (KVT == kKvInt8) return s8x2_to_f16x2(two);
+    return e4m3x2_to_f16x2(two);
+}
+
 template <int D, int NT, int HB, bool KV8>
 struct PagedCfg {
     static_assert(D == 64 || D == 128, "paged kernel supports D = 64 or 128");
@@ -127,9 +147,11 @@ __device__ __forceinline__ int out_d(int t, int hi, int gi) {
     return 64 * (t >> 2) + 8 * gi + 2 * (t & 3) + hi;
 }
 
-template <int D, int NT, int HB, bool KV8, bool RANGE>
-__global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D, NT, HB, KV8>::MIN_BLOCKS)
+template <int D, int NT, int HB, int KVT, bool RANGE>
+__global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
+                                  PagedCfg<D, NT, HB, KVT != kKvBf16>::MIN_BLOCKS)
     gqa_paged_kernel(const PagedArgs a) {
+    constexpr bool KV8 = KVT != kKvBf16;  // 8-bit codes (FP8 or int8) widened to f16; else bf16
     using C = PagedCfg<D, NT, HB, KV8>;
     extern __shared__ __align__(128) uint8_t psmem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(psmem + C::BAR_OFF);
@@ -446,10 +468,10 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
                         const int u = kk >> 2, w = kk & 3;
                         const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
                         const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
-                        af[0] = e4m3x2_to_f16x2(uint16_t(w0 & 0xffffu));
-                        af[1] = e4m3x2_to_f16x2(uint16_t(w1 & 0xffffu));
-                        af[2] = e4m3x2_to_f16x2(uint16_t(w0 >> 16));
-                        af[3] = e4m3x2_to_f16x2(uint16_t(w1 >> 16));
+                        af[0] = widen8<KVT>(uint16_t(w0 & 0xffffu));
+                        af[1] = widen8<KVT>(uint16_t(w1 & 0xffffu));
+                        af[2] = widen8<KVT>(uint16_t(w0 >> 16));
+                        af[3] = widen8<KVT>(uint16_t(w1 >> 16));
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
                     } else {
@@ -551,10 +573,10 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KV8>::THREADS, PagedCfg<D,
                         const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
                         const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
                         const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
-                        const uint32_t a_t0[4] = {e4m3x2_to_f16x2(uint16_t(ab01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab01 >> 16)),
-                                                  e4m3x2_to_f16x2(uint16_t(cd01 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd01 >> 16))};
-                        const uint32_t a_t1[4] = {e4m3x2_to_f16x2(uint16_t(ab23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(ab23 >> 16)),
-                                                  e4m3x2_to_f16x2(uint16_t(cd23 & 0xffffu)), e4m3x2_to_f16x2(uint16_t(cd23 >> 16))};
+                        const uint32_t a_t0[4] = {widen8<KVT>(uint16_t(ab01 & 0xffffu)), widen8<KVT>(uint16_t(ab01 >> 16)),
+                                                  widen8<KVT>(uint16_t(cd01 & 0xffffu)), widen8<KVT>(uint16_t(cd01 >> 16))};
+                        const uint32_t a_t1[4] = {widen8<KVT>(uint16_t(ab23 & 0xffffu)), widen8<KVT>(uint16_t(ab23 >> 16)),
+                                                  widen8<KVT>(uint16_t(cd23 & 0xffffu)), widen8<KVT>(uint16_t(cd23 >> 16))};
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);

@@ -108,6 +108,9 @@ CONFIGS = {
     "paged_fp8_b32_h64x8_d128_kv32k_ps16": PagedKVConfig(
         "paged_fp8_b32_h64x8_d128_kv32k_ps16", B=32, Sq=1, Hq=64, Hkv=8, D=128, page_size=16,
         pages_per_req=2048, kv_dtype="fp8", seed=1007),
+    "paged_int8_b32_h64x8_d128_kv32k_ps16": PagedKVConfig(
+        "paged_int8_b32_h64x8_d128_kv32k_ps16", B=32, Sq=1, Hq=64, Hkv=8, D=128, page_size=16,
+        pages_per_req=2048, kv_dtype="int8", seed=1008),
 }
 
 # The configuration the headline throughput is quoted on (a long 128K cache,

@@ -220,8 +220,12 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
  *
  * q, out : device bf16 [B, Sq, Hq, D].  lse : device fp32 [B, Hq, Sq] or NULL.
  * k_pool, v_pool : device [num_pages, page_size, Hkv, D] of bf16
- *   (kv_dtype GQA_KV_BF16; k_scale and v_scale are ignored) or of E4M3FN
- *   codes (GQA_KV_FP8_E4M3FN; k_scale, v_scale finite host fp32 scalars).
+ *   (kv_dtype GQA_KV_BF16; k_scale and v_scale are ignored), of E4M3FN codes
+ *   (GQA_KV_FP8_E4M3FN) or of two's-complement int8 codes (GQA_KV_INT8, the
+ *   int8 KV cache dequantised tile by tile inside the kernel that
+ *   "Profiling down to the register, then an extension that broke my
+ *   assumptions twice" leaves open: value = code * scale); for 8-bit codes
+ *   k_scale, v_scale are finite host fp32 per-tensor scales.
  * page_table : device int32 [B, pages_per_req].  seq_lens : device int32 [B].
  * Limits: D in {64, 128}; (Hq / Hkv) * Sq <= 16; pages_per_req * page_size
  *   and num_pages * page_size < 2^31.  Pointers 16-byte aligned (q, out,
@@ -235,7 +239,7 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
  *   (256-byte aligned, at least gqa_decode_paged_workspace_bytes; NULL =
  *   library pool).
  * ------------------------------------------------------------------------ */
-typedef enum { GQA_KV_BF16 = 0, GQA_KV_FP8_E4M3FN = 1 } gqa_kv_dtype;
+typedef enum { GQA_KV_BF16 = 0, GQA_KV_FP8_E4M3FN = 1, GQA_KV_INT8 = 2 } gqa_kv_dtype;
 
 gqa_status gqa_decode_paged(const void *q, const void *k_pool, const void *v_pool, int kv_dtype,
                             float k_scale, float v_scale, const int32_t *page_table,

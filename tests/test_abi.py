@@ -127,7 +127,8 @@ def _paged_kv(lib, q=A, kp=A, vp=A, kvd=0, ks=1.0, vs=1.0, pt=A, sl=A, out=A, ls
     (dict(ps=0), 1),
     (dict(ppr=0), 1),
     (dict(num_pages=0), 1),
-    (dict(kvd=2), 1),                # unknown pool type
+    (dict(kvd=3), 1),                # unknown pool type
+    (dict(kvd=2, vs=float("inf")), 1),  # int8 pools need finite scales
     (dict(splits=-1), 1),
     (dict(D=96), 2),
     (dict(D=256), 2),

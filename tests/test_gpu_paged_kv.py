@@ -64,6 +64,9 @@ SMALL = [
     (1, 1, 96, 12, 64, 32, 4, "fp8", (111,)),             # 12 heads: a full and a partial head block
     (2, 2, 64, 8, 128, 16, 12, "fp8", (190, 64)),         # 16 rows per KV head: two n-tiles
     (1, 1, 16, 1, 128, 16, 300, "bf16", (4800,)),         # more tokens than one index-map pass
+    (3, 1, 32, 8, 128, 16, 8, "int8", (128, 100, 17)),    # int8 pools
+    (2, 4, 8, 2, 64, 64, 3, "int8", (192, 5)),
+    (2, 2, 64, 8, 128, 16, 12, "int8", (190, 64)),
 ]
 
 
@@ -90,6 +93,22 @@ def test_balanced_schedule_edges(gq, orc, lens, workers):
     out, lse = _run(gq, inp, num_splits=workers)
     ref_o, ref_l = _ref(orc, inp, 0.125)
     _check(out, lse, ref_o, ref_l, f"balanced {lens} W={workers}")
+    assert gq.gqa_device_status() == 0
+
+
+def test_int8_extreme_codes(gq, orc):
+    """int8 pools holding every code, -128 and 127 included, against the oracle
+    (the quantiser of the workloads never emits -128)."""
+    inp = gqa_inputs.paged_kv_inputs(2, 1, 16, 4, 128, 16, 4, 9, seed=60, kv_dtype="int8", seq_lens=[64, 40])
+    g = torch.Generator().manual_seed(61)
+    for name in ("k_pool", "v_pool"):
+        codes = torch.randint(-128, 128, tuple(inp[name].shape), generator=g, dtype=torch.int16).to(torch.int8)
+        codes.view(-1)[:256] = torch.arange(-128, 128, dtype=torch.int16).to(torch.int8)
+        inp[name] = codes.contiguous()
+    inp["k_scale"], inp["v_scale"] = 0.01, 0.02
+    out, lse = _run(gq, inp)
+    ref_o, ref_l = _ref(orc, inp, 1.0 / math.sqrt(128))
+    _check(out, lse, ref_o, ref_l, "int8 extreme codes")
     assert gq.gqa_device_status() == 0
 
 
@@ -157,7 +176,8 @@ def test_automatic_splits_reported(gq):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["paged_bf16_b32_h64x8_d128_kv32k_ps16", "paged_fp8_b32_h64x8_d128_kv32k_ps16"])
+@pytest.mark.parametrize("name", ["paged_bf16_b32_h64x8_d128_kv32k_ps16", "paged_fp8_b32_h64x8_d128_kv32k_ps16",
+                                  "paged_int8_b32_h64x8_d128_kv32k_ps16"])
 def test_full_workload_sampled_rows(gq, orc, name):
     """The benchmark workloads at full size, in the launch configuration the
     benchmark times (automatic splits); sampled rows of three requests checked
