@@ -80,6 +80,23 @@ __device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t two) {
     return r;
 }
 
+// Biased f16x2 of two int8 codes picked from the bytes of (a, b) by the
+// permute selector `sel` (result bytes 0 and 2; bytes 1 and 3 are
+// overwritten): one lop3 flips each code's sign bit (code + 128 in
+// [0, 255]) and sets the f16 exponent of 1024, giving code + 1152 exactly.
+__device__ __forceinline__ uint32_t s8pair_biased(uint32_t a, uint32_t b, uint32_t sel) {
+    const uint32_t x = prmt(a, b, sel);
+    uint32_t r;
+    // per bit: c ? b : (a ^ b) with b = 0x64806480, c = 0xFF00FF00
+    asm("lop3.b32 %0, %1, %2, %3, 0x9C;" : "=r"(r) : "r"(x), "r"(0x64806480u), "r"(0xFF00FF00u));
+    return r;
+}
+__device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t h) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+
 // K/V element types of the paged kernel.
 enum : int { kKvBf16 = 0, kKvFp8 = 1, kKvInt8 = 2 };
 
@@ -311,6 +328,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
     float m_run[NT][2], l_run[NT][2];
     float o[NT][C::DB][4];
     int kmax[NT][2];  // last visible token of the rows this lane holds in S^T (S_q > 1)
+    float kbias[NT][2];  // int8: score offset of the biased K (1152 * sum of the row's q)
     if (!producer) {
         float row_alpha[NT];
 #pragma unroll
@@ -359,12 +377,33 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 row_alpha[nt] = a.alpha;
             }
         }
+        // int8 pools feed K to the MMA biased by +1152 (no subtraction per
+        // element); the scores are corrected by 1152 * sum_d q_d of the row,
+        // summed over the same f16 q values the MMA reads.
+        float qsum[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float sacc = 0.f;
+            if constexpr (KVT == kKvInt8) {
+#pragma unroll
+                for (int kk = 0; kk < C::KSTEPS; ++kk)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&qf[nt][kk][j]));
+                        sacc += f.x + f.y;
+                    }
+                sacc += __shfl_xor_sync(0xffffffffu, sacc, 1);
+                sacc += __shfl_xor_sync(0xffffffffu, sacc, 2);
+            }
+            qsum[nt] = sacc;
+        }
         // score multipliers and visibility of the rows this lane holds in S^T: 8 nt + 2c + e
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 alpha_s[nt][e] = __shfl_sync(0xffffffffu, row_alpha[nt], 4 * (2 * c + e));
+                kbias[nt][e] = 1152.f * __shfl_sync(0xffffffffu, qsum[nt], 4 * (2 * c + e));
                 const int r = 8 * nt + 2 * c + e;
                 kmax[nt][e] = seq_len - a.Sq + (r < a.Mq ? r / a.G : 0);
             }
@@ -468,10 +507,17 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                         const int u = kk >> 2, w = kk & 3;
                         const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
                         const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
-                        af[0] = widen8<KVT>(uint16_t(w0 & 0xffffu));
-                        af[1] = widen8<KVT>(uint16_t(w1 & 0xffffu));
-                        af[2] = widen8<KVT>(uint16_t(w0 >> 16));
-                        af[3] = widen8<KVT>(uint16_t(w1 >> 16));
+                        if constexpr (KVT == kKvInt8) {  // biased by +1152, corrected in the scores
+                            af[0] = s8pair_biased(w0, w0, 0x1100u);
+                            af[1] = s8pair_biased(w1, w1, 0x1100u);
+                            af[2] = s8pair_biased(w0, w0, 0x3322u);
+                            af[3] = s8pair_biased(w1, w1, 0x3322u);
+                        } else {
+                            af[0] = widen8<KVT>(uint16_t(w0 & 0xffffu));
+                            af[1] = widen8<KVT>(uint16_t(w1 & 0xffffu));
+                            af[2] = widen8<KVT>(uint16_t(w0 >> 16));
+                            af[3] = widen8<KVT>(uint16_t(w1 >> 16));
+                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) mma_f16_16816(st_[nt], af, qf[nt][kk][0], qf[nt][kk][1]);
                     } else {
@@ -499,8 +545,9 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                             ok0 = ok0 && tok0 <= kmax[nt][e];
                             ok1 = ok1 && tok0 + 8 <= kmax[nt][e];
                         }
-                        const float t0 = ok0 ? st_[nt][e] * alpha_s[nt][e] : -INFINITY;
-                        const float t1 = ok1 ? st_[nt][2 + e] * alpha_s[nt][e] : -INFINITY;
+                        const float kb = KVT == kKvInt8 ? kbias[nt][e] : 0.f;
+                        const float t0 = ok0 ? (st_[nt][e] - kb) * alpha_s[nt][e] : -INFINITY;
+                        const float t1 = ok1 ? (st_[nt][2 + e] - kb) * alpha_s[nt][e] : -INFINITY;
                         float mx = fmaxf(t0, t1);
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -569,14 +616,31 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                     // d-block t: rows m = gi (byte 2t) and gi + 8 (byte 2t + 1) of the lane's piece
 #pragma unroll
                     for (int w = 0; w < C::VW; ++w) {
-                        const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
-                        const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
-                        const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
-                        const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
-                        const uint32_t a_t0[4] = {widen8<KVT>(uint16_t(ab01 & 0xffffu)), widen8<KVT>(uint16_t(ab01 >> 16)),
-                                                  widen8<KVT>(uint16_t(cd01 & 0xffffu)), widen8<KVT>(uint16_t(cd01 >> 16))};
-                        const uint32_t a_t1[4] = {widen8<KVT>(uint16_t(ab23 & 0xffffu)), widen8<KVT>(uint16_t(ab23 >> 16)),
-                                                  widen8<KVT>(uint16_t(cd23 & 0xffffu)), widen8<KVT>(uint16_t(cd23 >> 16))};
+                        uint32_t a_t0[4], a_t1[4];
+                        if constexpr (KVT == kKvInt8) {
+                            // pair (token 2c, 2c+1) of byte k of word w: permute, lop3, exact -1152
+                            a_t0[0] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x4400u));
+                            a_t0[1] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x5511u));
+                            a_t0[2] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x4400u));
+                            a_t0[3] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x5511u));
+                            a_t1[0] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x6622u));
+                            a_t1[1] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x7733u));
+                            a_t1[2] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x6622u));
+                            a_t1[3] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x7733u));
+                        } else {
+                            const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
+                            const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
+                            const uint32_t cd01 = prmt(vw[2][w], vw[3][w], 0x5140u);
+                            const uint32_t cd23 = prmt(vw[2][w], vw[3][w], 0x7362u);
+                            a_t0[0] = widen8<KVT>(uint16_t(ab01 & 0xffffu));
+                            a_t0[1] = widen8<KVT>(uint16_t(ab01 >> 16));
+                            a_t0[2] = widen8<KVT>(uint16_t(cd01 & 0xffffu));
+                            a_t0[3] = widen8<KVT>(uint16_t(cd01 >> 16));
+                            a_t1[0] = widen8<KVT>(uint16_t(ab23 & 0xffffu));
+                            a_t1[1] = widen8<KVT>(uint16_t(ab23 >> 16));
+                            a_t1[2] = widen8<KVT>(uint16_t(cd23 & 0xffffu));
+                            a_t1[3] = widen8<KVT>(uint16_t(cd23 >> 16));
+                        }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             mma_f16_16816(o[nt][2 * w], a_t0, pb[nt][0], pb[nt][1]);
