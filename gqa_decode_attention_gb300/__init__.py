@@ -35,7 +35,7 @@ EXPORTS = [
     "gqa_status_string", "gqa_version", "gqa_decode", "gqa_decode_num_splits",
     "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
     "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged", "gqa_decode_paged_ex",
-    "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes",
+    "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes", "gqa_decode_paged_dev_scales",
     "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
     "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events",
 ]
@@ -83,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_paged.argtypes = [vp, vp, vp, i, f, f, vp, vp, vp, vp] + [i] * 8 + [f, vp]
     lib.gqa_decode_paged_ex.restype = st
     lib.gqa_decode_paged_ex.argtypes = [vp, vp, vp, i, f, f, vp, vp, vp, vp] + [i] * 8 + [f, i, vp, sz, vp]
+    lib.gqa_decode_paged_dev_scales.restype = st
+    lib.gqa_decode_paged_dev_scales.argtypes = [vp, vp, vp, i, vp, vp, i, vp, vp, vp, vp] + [i] * 8 + [f, i, vp, sz, vp]
     lib.gqa_decode_paged_num_splits.restype = i
     lib.gqa_decode_paged_num_splits.argtypes = [i] * 8
     lib.gqa_decode_paged_workspace_bytes.restype = sz
@@ -255,7 +257,8 @@ def _kv_dtype(k_pool) -> int:
 
 
 def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_scale=1.0, out=None, lse=None,
-                     scale=None, num_splits=0, workspace=None, stream=None, with_lse=True):
+                     scale=None, num_splits=0, workspace=None, stream=None, with_lse=True, k_scales=None,
+                     v_scales=None):
     """Paged decode over every token of each request (no top-K).
 
     q [B,Sq,Hq,D] bf16; pools [num_pages, page_size, Hkv, D] of bf16, of
@@ -263,6 +266,8 @@ def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_sca
     apply); page_table int32
     [B, pages_per_req]; seq_lens int32 [B].  num_splits 0 = automatic;
     workspace: optional CUDA uint8 tensor of gqa_decode_paged_workspace_bytes.
+    k_scales / v_scales: optional CUDA fp32 tensors of 1 or Hkv device-side
+    scales (8-bit pools; replace k_scale / v_scale).
     Returns (out [B,Sq,Hq,D] bf16, lse [B,Hq,Sq] fp32 or None).
     """
     lib = load_library()
@@ -281,6 +286,16 @@ def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_sca
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    if k_scales is not None or v_scales is not None:
+        _need(k_scales, "k_scales", torch.float32, "cuda")
+        _need(v_scales, "v_scales", torch.float32, "cuda")
+        st = lib.gqa_decode_paged_dev_scales(_ptr(q), _ptr(k_pool), _ptr(v_pool), kvd, _ptr(k_scales),
+                                             _ptr(v_scales), k_scales.numel(), _ptr(page_table), _ptr(seq_lens),
+                                             _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D, page_size,
+                                             page_table.shape[1], num_pages, _scale_arg(scale), int(num_splits),
+                                             ws_ptr, ws_bytes, _stream(stream))
+        _check(st, "gqa_decode_paged_dev_scales")
+        return out, lse
     st = lib.gqa_decode_paged_ex(_ptr(q), _ptr(k_pool), _ptr(v_pool), kvd, float(k_scale), float(v_scale),
                                  _ptr(page_table), _ptr(seq_lens), _ptr(out), _ptr(lse), B, Sq, Hq, Hkv, D,
                                  page_size, page_table.shape[1], num_pages, _scale_arg(scale), int(num_splits),

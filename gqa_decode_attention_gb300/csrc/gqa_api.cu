@@ -631,16 +631,22 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     return GQA_OK;
 }
 
-gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_pool, int kv_dtype, float k_scale,
-                               float v_scale, const int32_t *page_table, const int32_t *seq_lens, void *out,
-                               float *lse, int B, int Sq, int Hq, int Hkv, int D, int page_size, int pages_per_req,
-                               int num_pages, float scale, int num_splits, void *workspace,
-                               size_t workspace_bytes_, gqa_stream_t stream) {
+namespace {
+gqa_status run_paged_kv(const void *q, const void *k_pool, const void *v_pool, int kv_dtype, float k_scale,
+                        float v_scale, const float *k_scales, const float *v_scales, int n_scales,
+                        const int32_t *page_table, const int32_t *seq_lens, void *out, float *lse, int B, int Sq,
+                        int Hq, int Hkv, int D, int page_size, int pages_per_req, int num_pages, float scale,
+                        int num_splits, void *workspace, size_t workspace_bytes_, gqa_stream_t stream) {
     PagedShape s;
     gqa_status st = check_paged_kv(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req, num_pages, &s);
     if (st != GQA_OK) return st;
     if (num_splits < 0) return GQA_ERR_INVALID_ARG;
     if (s.kv8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale))) return GQA_ERR_INVALID_ARG;
+    if (k_scales != nullptr || v_scales != nullptr) {
+        if (k_scales == nullptr || v_scales == nullptr || (n_scales != 1 && n_scales != Hkv))
+            return GQA_ERR_INVALID_ARG;
+        if (!aligned(k_scales, 4) || !aligned(v_scales, 4)) return GQA_ERR_ALIGNMENT;
+    }
     if (q == nullptr || k_pool == nullptr || v_pool == nullptr || page_table == nullptr || seq_lens == nullptr ||
         out == nullptr)
         return GQA_ERR_INVALID_ARG;
@@ -688,6 +694,9 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
     a.num_splits = splits;
     a.alpha = resolve_scale(scale, D) * (s.kv8 ? k_scale : 1.0f) * 1.4426950408889634f;
     a.v_scale = s.kv8 ? v_scale : 1.0f;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.n_scales = n_scales;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.fault_mode = g_fault_mode.load();
     a.err = error_word(dev);
@@ -707,6 +716,29 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
         return GQA_ERR_CUDA;
     }
     return GQA_OK;
+}
+}  // namespace
+
+gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_pool, int kv_dtype, float k_scale,
+                               float v_scale, const int32_t *page_table, const int32_t *seq_lens, void *out,
+                               float *lse, int B, int Sq, int Hq, int Hkv, int D, int page_size, int pages_per_req,
+                               int num_pages, float scale, int num_splits, void *workspace,
+                               size_t workspace_bytes_, gqa_stream_t stream) {
+    return run_paged_kv(q, k_pool, v_pool, kv_dtype, k_scale, v_scale, nullptr, nullptr, 0, page_table, seq_lens,
+                        out, lse, B, Sq, Hq, Hkv, D, page_size, pages_per_req, num_pages, scale, num_splits,
+                        workspace, workspace_bytes_, stream);
+}
+
+gqa_status gqa_decode_paged_dev_scales(const void *q, const void *k_pool, const void *v_pool, int kv_dtype,
+                                       const float *k_scales, const float *v_scales, int n_scales,
+                                       const int32_t *page_table, const int32_t *seq_lens, void *out, float *lse,
+                                       int B, int Sq, int Hq, int Hkv, int D, int page_size, int pages_per_req,
+                                       int num_pages, float scale, int num_splits, void *workspace,
+                                       size_t workspace_bytes_, gqa_stream_t stream) {
+    if (kv_dtype == GQA_KV_BF16 || k_scales == nullptr || v_scales == nullptr) return GQA_ERR_INVALID_ARG;
+    return run_paged_kv(q, k_pool, v_pool, kv_dtype, 1.0f, 1.0f, k_scales, v_scales, n_scales, page_table,
+                        seq_lens, out, lse, B, Sq, Hq, Hkv, D, page_size, pages_per_req, num_pages, scale,
+                        num_splits, workspace, workspace_bytes_, stream);
 }
 
 gqa_status gqa_decode_paged(const void *q, const void *k_pool, const void *v_pool, int kv_dtype, float k_scale,

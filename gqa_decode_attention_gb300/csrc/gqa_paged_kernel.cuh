@@ -293,6 +293,15 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
     }
     long seg_t = w_begin;  // global step where the current segment starts
 
+    // this warp's KV head's dequantisation scales: the host scalars, times the
+    // device-side per-tensor or per-head values when given
+    float alpha_w = a.alpha, vscale_w = a.v_scale;
+    if (a.k_scales != nullptr && active) {
+        const int si = a.n_scales > 1 ? g : 0;
+        alpha_w *= __ldg(a.k_scales + si);
+        vscale_w *= __ldg(a.v_scales + si);
+    }
+
     const size_t row_bytes = size_t(a.Hkv) * C::ROWB;
     const uint32_t piece = uint32_t(nh) * C::ROWB;
     bool failed = false;
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 // 2^e with mx * 2^-e < 2^15: no overflow in f16 (max 65504)
                 const int ex = mx >= 32768.f ? ilogbf(mx) - 14 : 0;
                 const float down = ldexpf(1.f, -ex);
-                row_alpha[nt] = a.alpha * ldexpf(1.f, ex);
+                row_alpha[nt] = alpha_w * ldexpf(1.f, ex);
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
                     qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                     qf[nt][kk][0] = raw.x;  // k = 2c, 2c+1
                     qf[nt][kk][1] = raw.y;  // k = 2c+8, 2c+9
                 }
-                row_alpha[nt] = a.alpha;
+                row_alpha[nt] = alpha_w;
             }
         }
         // int8 pools feed K to the MMA biased by +1152 (no subtraction per
@@ -683,7 +692,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 if (r >= a.Mq) continue;
                 const int i = r / a.G;
                 const int h = g * a.G + r % a.G;
-                const float f = L > 0.f ? a.v_scale / L : 0.f;
+                const float f = L > 0.f ? vscale_w / L : 0.f;
                 const float lse2 = L > 0.f ? m_run[nt][e] + log2f(L) : -INFINITY;
                 if (!complete) {
                     const size_t prow =

@@ -54,6 +54,11 @@ struct PagedArgs {
     int num_splits;             // whole-request form: workers per head block
     float alpha;    // scale * k_scale * log2(e)
     float v_scale;
+    // Device-side scales (null: the host scalars above apply): n_scales = 1
+    // per tensor or Hkv per KV head; multiply alpha and v_scale.
+    const float *k_scales;
+    const float *v_scales;
+    int n_scales;
     unsigned long long wait_limit_ns;
     int fault_mode;  // test hook: 1 = the producer never issues the first stage
     unsigned *err;   // device error word

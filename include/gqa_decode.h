@@ -254,6 +254,21 @@ gqa_status gqa_decode_paged_ex(const void *q, const void *k_pool, const void *v_
                                int pages_per_req, int num_pages, float scale, int num_splits,
                                void *workspace, size_t workspace_bytes, gqa_stream_t stream);
 
+/* gqa_decode_paged_ex for 8-bit pools (GQA_KV_FP8_E4M3FN, GQA_KV_INT8) with
+ * the dequantisation scales in device memory: k_scales and v_scales each
+ * point to n_scales fp32 values, n_scales = 1 (per tensor) or Hkv (per KV
+ * head: KV head g uses [g]).  The kernel reads them when it starts, so
+ * earlier work in the stream may write them.  GQA_ERR_INVALID_ARG for a bf16
+ * pool, null scale pointers or another n_scales; GQA_ERR_ALIGNMENT unless
+ * 4-byte aligned. */
+gqa_status gqa_decode_paged_dev_scales(const void *q, const void *k_pool, const void *v_pool, int kv_dtype,
+                                       const float *k_scales, const float *v_scales, int n_scales,
+                                       const int32_t *page_table, const int32_t *seq_lens,
+                                       void *out, float *lse,
+                                       int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                                       int pages_per_req, int num_pages, float scale, int num_splits,
+                                       void *workspace, size_t workspace_bytes, gqa_stream_t stream);
+
 /* Workers per head block the automatic choice uses for this shape on the
  * current device (negative gqa_status on invalid arguments). */
 int gqa_decode_paged_num_splits(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype,

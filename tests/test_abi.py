@@ -153,6 +153,17 @@ def test_paged_kv_rejects(lib, kw, status):
         assert got == status
 
 
+def test_paged_dev_scales_rejects(lib):
+    def call(kvd=1, ks=A, vs=A, n=1, Hkv=2):
+        return lib.gqa_decode_paged_dev_scales(A, A, A, kvd, ks, vs, n, A, A, A, A, 2, 1, 8, Hkv, 128, 16, 4, 16,
+                                               0.0, 0, None, 0, None)
+    assert call(kvd=0) == 1          # bf16 pools take no scales
+    assert call(ks=None) == 1
+    assert call(n=3) == 1            # neither per tensor nor per head
+    assert call(ks=MIS) == 3
+    assert call(n=2) not in (1, 2, 3)  # per head: valid arguments
+
+
 def test_paged_kv_sizes(lib):
     # automatic split count and workspace reject bad shapes with a negative status / zero
     assert lib.gqa_decode_paged_num_splits(2, 1, 8, 2, 96, 0, 16, 4) == -2

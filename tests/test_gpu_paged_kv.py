@@ -112,6 +112,38 @@ def test_int8_extreme_codes(gq, orc):
     assert gq.gqa_device_status() == 0
 
 
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+def test_device_scales_per_head_and_per_tensor(gq, orc, kv):
+    """Device-side scales: per KV head (power-of-two scales, so the
+    dequantised pool is exact in bf16 and the oracle runs on that bf16 pool)
+    and per tensor (the same as the host scalars)."""
+    B, Hq, Hkv, D = 3, 32, 8, 128
+    inp = gqa_inputs.paged_kv_inputs(B, 1, Hq, Hkv, D, 16, 8, B * 8 + 1, seed=70, kv_dtype=kv, seq_lens=[128, 77, 9])
+    ks = torch.tensor([2.0 ** -(e % 4 + 5) for e in range(Hkv)], dtype=torch.float32)
+    vs = torch.tensor([2.0 ** -((3 * e) % 5 + 4) for e in range(Hkv)], dtype=torch.float32)
+    d = _cuda(inp)
+    out, lse = gq.gqa_decode_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"],
+                                   k_scales=ks.cuda(), v_scales=vs.cuda())
+    torch.cuda.synchronize()
+    assert gq.gqa_device_status() == 0
+    codes_k = inp["k_pool"].view(torch.float8_e4m3fn).double() if kv == "fp8" else inp["k_pool"].double()
+    codes_v = inp["v_pool"].view(torch.float8_e4m3fn).double() if kv == "fp8" else inp["v_pool"].double()
+    kb = (codes_k * ks.double().view(1, 1, Hkv, 1)).to(torch.bfloat16)
+    vb = (codes_v * vs.double().view(1, 1, Hkv, 1)).to(torch.bfloat16)
+    assert torch.equal(kb.double(), codes_k * ks.double().view(1, 1, Hkv, 1))
+    ref_o, ref_l = orc.gqa_decode_paged(inp["q"], kb, vb, inp["page_table"], inp["seq_lens"], 1.0 / math.sqrt(D))
+    _check(out.cpu(), lse.cpu(), ref_o, ref_l, f"{kv} per-head device scales")
+    # per tensor on the device == the host scalars
+    o1, l1 = gq.gqa_decode_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"],
+                                 k_scales=torch.tensor([inp["k_scale"]], device="cuda"),
+                                 v_scales=torch.tensor([inp["v_scale"]], device="cuda"))
+    o2, l2 = gq.gqa_decode_paged(d["q"], d["k_pool"], d["v_pool"], d["page_table"], d["seq_lens"],
+                                 inp["k_scale"], inp["v_scale"])
+    torch.cuda.synchronize()
+    assert torch.allclose(o1.float(), o2.float(), atol=1e-3, rtol=1e-2)
+    assert torch.allclose(l1, l2, atol=1e-5, rtol=0)
+
+
 def test_split_counts_agree(gq):
     """Worker counts from one (every request whole in one CTA) to more workers
     than steps agree within rounding."""
