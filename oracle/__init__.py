@@ -26,6 +26,9 @@ attention):
 * ``gqa_decode_paged_fp8`` -- same page, sections "Workload" and
   "Implementations": attention over the selected tokens with k_scale in the
   scores, v_scale on the values, then a sigmoid gate.
+* ``gqa_decode_dv`` -- the dense decode with a score head size (q, K) that
+  differs from the value head size (V, O): the kv-copies page's d192x128
+  flavour ("Limits, and what I'd do next").
 * ``gqa_decode_paged`` -- the same page-table addressing without a top-K list:
   every token of each request up to its own sequence length, bf16, FP8 or
   int8 pools, the dense path's bottom-right mask per request (the serving layout
@@ -122,6 +125,9 @@ class Oracle:
             _u16_p, _u16_p, _u16_p,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, _i32_p, ctypes.c_int, _dbl_p, _dbl_p]
+        lib.oracle_gqa_decode_dv.restype = None
+        lib.oracle_gqa_decode_dv.argtypes = [
+            _u16_p, _u16_p, _u16_p] + [ctypes.c_int] * 7 + [ctypes.c_double, _i32_p, ctypes.c_int, _dbl_p, _dbl_p]
         lib.oracle_paged_gather.restype = None
         lib.oracle_paged_gather.argtypes = [
             _u8_p, _i32_p, _i32_p] + [ctypes.c_int] * 6 + [_u8_p]
@@ -174,6 +180,32 @@ class Oracle:
         if rows is not None:
             return out, lse
         o = out.reshape(B, Hq, Sq, D).transpose(0, 2, 1, 3).copy()
+        return o, lse.reshape(B, Hq, Sq)
+
+    def gqa_decode_dv(self, q, k, v, scale: float, rows=None):
+        """Dense decode with Dqk != Dv.  q [B,Sq,Hq,Dqk], k [B,Skv,Hkv,Dqk],
+        v [B,Skv,Hkv,Dv] (bf16).  Returns (O [B,Sq,Hq,Dv], LSE [B,Hq,Sq]) or,
+        with ``rows``, (O [n,Dv], LSE [n])."""
+        qa, ka, va = _as_u16(q), _as_u16(k), _as_u16(v)
+        B, Sq, Hq, Dqk = qa.shape
+        _, Skv, Hkv, _ = ka.shape
+        Dv = va.shape[3]
+        assert ka.shape == (B, Skv, Hkv, Dqk) and va.shape == (B, Skv, Hkv, Dv)
+        if rows is None:
+            n = B * Hq * Sq
+            rp = None
+        else:
+            ra = _as_i32(np.asarray(rows, dtype=np.int32))
+            n = ra.size
+            rp = _p(ra, _i32_p)
+        out = np.zeros((n, Dv), dtype=np.float64)
+        lse = np.zeros((n,), dtype=np.float64)
+        self._lib.oracle_gqa_decode_dv(
+            _p(qa, _u16_p), _p(ka, _u16_p), _p(va, _u16_p),
+            B, Sq, Skv, Hq, Hkv, Dqk, Dv, float(scale), rp, n, _p(out, _dbl_p), _p(lse, _dbl_p))
+        if rows is not None:
+            return out, lse
+        o = out.reshape(B, Hq, Sq, Dv).transpose(0, 2, 1, 3).copy()
         return o, lse.reshape(B, Hq, Sq)
 
     # -- paged FP8 -----------------------------------------------------

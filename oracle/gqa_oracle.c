@@ -182,6 +182,61 @@ void oracle_gqa_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
 }
 
+/*
+ * Dense decode with different head sizes for the scores and the values
+ * ("When the K/V copy costs more than the attention", section "Limits, and
+ * what I'd do next": the d192x128 flavour): q, k : bf16 [.., Dqk],
+ * v : bf16 [B, Skv, Hkv, Dv], out : [n_rows, Dv].  Otherwise exactly
+ * oracle_gqa_decode (same rows, mask, scale, LSE).
+ */
+void oracle_gqa_decode_dv(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv, double scale,
+                          const int32_t *rows, int n_rows, double *out, double *lse)
+{
+    long total = rows ? n_rows : (long)B * Hq * Sq;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Skv > 0 ? Skv : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long n = 0; n < total; ++n) {
+            long r = rows ? rows[n] : n;
+            int i = (int)(r % Sq);
+            int h = (int)((r / Sq) % Hq);
+            int b = (int)(r / ((long)Sq * Hq));
+            int g = oracle_kv_head(h, Hq, Hkv);
+            long last = last_visible_key(i, Sq, Skv);
+            const uint16_t *qrow = q + (((size_t)b * Sq + i) * Hq + h) * Dqk;
+            int dot_len = PLANT(14) ? Dv : Dqk;
+            double m = -INFINITY;
+            for (long j = 0; j <= last && j < Skv; ++j) {
+                const uint16_t *krow = k + (((size_t)b * Skv + j) * Hkv + g) * Dqk;
+                double dot = 0.0;
+                for (int d = 0; d < dot_len; ++d)
+                    dot += bf16_value(qrow[d]) * bf16_value(krow[d]);
+                s[j] = scale * dot;
+                if (s[j] > m)
+                    m = s[j];
+            }
+            double sum = 0.0;
+            for (long j = 0; j <= last && j < Skv; ++j)
+                sum += exp(s[j] - m);
+            double L = m + log(sum);
+            double *o = out + (size_t)n * Dv;
+            for (int d = 0; d < Dv; ++d)
+                o[d] = 0.0;
+            for (long j = 0; j <= last && j < Skv; ++j) {
+                double w = exp(s[j] - L);
+                const uint16_t *vrow = v + (((size_t)b * Skv + j) * Hkv + g) * Dv;
+                for (int d = 0; d < Dv; ++d)
+                    o[d] += w * bf16_value(vrow[d]);
+            }
+            if (lse)
+                lse[n] = L;
+        }
+        free(s);
+    }
+}
+
 /* ------------------------------------------------------------------ */
 /* sparse paged FP8 decode with sigmoid gate                            */
 /* ------------------------------------------------------------------ */

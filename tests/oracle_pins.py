@@ -473,10 +473,50 @@ def pin_paged_zero_keys_and_short_requests(orc):
                 _assert_close(O[b, i, h], mean, 1e-13, 1e-13, "paged mean of visible V")
 
 
+# ----------------------------------------------------------------------
+# Dqk != Dv
+# ----------------------------------------------------------------------
+def pin_dv_equals_padded_v(orc):
+    """Dqk = 192, Dv = 128 equals the dense oracle run with V zero-padded to
+    192 columns: the first 128 output columns and the LSE bit for bit (the
+    padded columns come out exactly 0); Sq = 1 and 3 (causal)."""
+    for ci, (B, Sq, Skv, Hq, Hkv) in enumerate([(2, 1, 37, 8, 2), (1, 3, 20, 4, 4)]):
+        q = _bf16((B, Sq, Hq, 192), 2100 + ci)
+        k = _bf16((B, Skv, Hkv, 192), 2110 + ci)
+        v = _bf16((B, Skv, Hkv, 128), 2120 + ci)
+        vp = torch.cat([v, torch.zeros((B, Skv, Hkv, 64), dtype=torch.bfloat16)], dim=3).contiguous()
+        O, L = orc.gqa_decode_dv(q, k, v, 0.07)
+        Op, Lp = orc.gqa_decode(q, k, vp, 0.07)
+        assert np.array_equal(O, Op[..., :128]) and np.all(Op[..., 128:] == 0.0)
+        assert np.array_equal(L, Lp)
+
+
+def pin_bruteforce_dv(orc):
+    """Tiny Dqk != Dv case at 50 digits, no max subtraction."""
+    mpmath.mp.dps = 50
+    B, Sq, Skv, Hq, Hkv, Dqk, Dv = 1, 2, 5, 4, 2, 6, 3
+    q, k, v = _bf16((B, Sq, Hq, Dqk), 2200), _bf16((B, Skv, Hkv, Dqk), 2201), _bf16((B, Skv, Hkv, Dv), 2202)
+    O, L = orc.gqa_decode_dv(q, k, v, 0.4)
+    qn, kn, vn = _f64(q), _f64(k), _f64(v)
+    vis = _visible_mask(Sq, Skv)
+    for i in range(Sq):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            ws = [mpmath.e ** (mpmath.mpf(0.4) * mpmath.fsum(mpmath.mpf(qn[0, i, h, d]) * mpmath.mpf(kn[0, j, g, d])
+                                                          for d in range(Dqk))) if vis[i, j] else mpmath.mpf(0)
+                  for j in range(Skv)]
+            Z = mpmath.fsum(ws)
+            assert abs(L[0, h, i] - float(mpmath.log(Z))) <= 1e-12
+            for d in range(Dv):
+                ref = float(mpmath.fsum(w * mpmath.mpf(vn[0, j, g, d]) for j, w in enumerate(ws)) / Z)
+                assert abs(O[0, i, h, d] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
 DENSE_PINS = [pin_bruteforce_dense, pin_library_dense, pin_gqa_equals_expanded_mha, pin_head_map_table,
               pin_zero_keys, pin_constant_v, pin_single_key, pin_zero_scale, pin_hardmax]
 PAGED_PINS = [pin_e4m3fn_table, pin_paged_gather, pin_bruteforce_paged, pin_paged_equals_dense,
               pin_topk_order_and_padding, pin_gate_and_scales]
 PAGED_KV_PINS = [pin_paged_requests_equal_dense, pin_paged_fp8_equals_bf16, pin_paged_int8_equals_bf16,
                  pin_paged_zero_keys_and_short_requests]
-ALL_PINS = DENSE_PINS + PAGED_PINS + PAGED_KV_PINS
+DV_PINS = [pin_dv_equals_padded_v, pin_bruteforce_dv]
+ALL_PINS = DENSE_PINS + PAGED_PINS + PAGED_KV_PINS + DV_PINS

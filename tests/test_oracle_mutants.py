@@ -30,6 +30,7 @@ MUTANTS = {
     11: "paged: per-request sequence length ignored",
     12: "paged: k_scale and v_scale swapped",
     13: "paged: int8 codes read as unsigned",
+    14: "Dqk != Dv: scores summed over the value head size",
 }
 
 
