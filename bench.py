@@ -64,7 +64,8 @@ def paged_kv_lens(cfg) -> list[int]:
 
 def workload_kv_bytes(cfg) -> int:
     if isinstance(cfg, gqa_inputs.DenseConfig):
-        return kv_bytes(cfg.B, cfg.Hkv, cfg.Skv, cfg.D, 2)
+        # K rows of D dims and V rows of Dv dims (kv_bytes counts 2 x D per key)
+        return cfg.B * cfg.Hkv * cfg.Skv * (cfg.D + cfg.dv) * 2
     if isinstance(cfg, gqa_inputs.PagedKVConfig):
         elem = 2 if cfg.kv_dtype == "bf16" else 1
         return sum(kv_bytes(1, cfg.Hkv, n, cfg.D, elem) for n in paged_kv_lens(cfg))
@@ -73,8 +74,11 @@ def workload_kv_bytes(cfg) -> int:
 
 def workload_config(cfg) -> dict:
     if isinstance(cfg, gqa_inputs.DenseConfig):
-        return {"workload": cfg.name, "B": cfg.B, "Sq": cfg.Sq, "Skv": cfg.Skv, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
-                "D": cfg.D, "kv_dtype": "bf16", "mask": "bottom-right causal" if cfg.Sq > 1 else "none"}
+        c = {"workload": cfg.name, "B": cfg.B, "Sq": cfg.Sq, "Skv": cfg.Skv, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+             "D": cfg.D, "kv_dtype": "bf16", "mask": "bottom-right causal" if cfg.Sq > 1 else "none"}
+        if cfg.dv != cfg.D:
+            c["Dv"] = cfg.dv
+        return c
     if isinstance(cfg, gqa_inputs.PagedKVConfig):
         lens = paged_kv_lens(cfg)
         cap = cfg.pages_per_req * cfg.page_size
@@ -273,13 +277,16 @@ def _make_call(gq, cfg, dev, seed_offset):
     import torch
     if isinstance(cfg, gqa_inputs.DenseConfig):
         q, k, v = gqa_inputs.dense_inputs(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D,
-                                          cfg.seed + seed_offset, device=dev)
-        out = torch.empty_like(q)
+                                          cfg.seed + seed_offset, device=dev, Dv=cfg.dv)
+        out = torch.empty((cfg.B, cfg.Sq, cfg.Hq, cfg.dv), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((cfg.B, cfg.Hq, cfg.Sq), dtype=torch.float32, device=dev)
-
-        def call():
-            gq.gqa_decode(q, k, v, out=out, lse=lse)
-        splits = gq.gqa_decode_num_splits(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D)
+        if cfg.dv == cfg.D:
+            def call():
+                gq.gqa_decode(q, k, v, out=out, lse=lse)
+        else:
+            def call():
+                gq.gqa_decode_dv(q, k, v, out=out, lse=lse)
+        splits = gq.gqa_decode_dv_num_splits(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D, cfg.dv)
         return call, dict(q=q, k=k, v=v, out=out, lse=lse), (2 if splits > 1 else 1), splits
     if isinstance(cfg, gqa_inputs.PagedKVConfig):
         inp = gqa_inputs.paged_kv_inputs(cfg.B, cfg.Sq, cfg.Hq, cfg.Hkv, cfg.D, cfg.page_size, cfg.pages_per_req,
@@ -337,14 +344,14 @@ def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
         q, k, v = (tensors[n].cpu() for n in ("q", "k", "v"))
         nrows = cfg.B * cfg.Hq * cfg.Sq
         t0 = time.perf_counter()
-        orc.gqa_decode(q, k, v, cfg.scale, rows=list(range(min(nrows, 8))))
+        dense_oracle(orc, cfg, q, k, v, rows=list(range(min(nrows, 8))))
         per_row = (time.perf_counter() - t0) / min(nrows, 8)
         rows = None if per_row * nrows <= max_seconds else list(range(max(1, int(max_seconds / 3 / per_row))))
         frac = 1.0 if rows is None else len(rows) / nrows
         reps, elapsed = 0, 0.0
         while elapsed < min_seconds and reps < 1000:
             t0 = time.perf_counter()
-            orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
+            dense_oracle(orc, cfg, q, k, v, rows=rows)
             elapsed += time.perf_counter() - t0
             reps += 1
         sample = (f"{'all' if rows is None else len(rows)} of {nrows} query rows "
@@ -374,6 +381,13 @@ def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
     return {"value": gbs(workload_kv_bytes(cfg) * frac, per_pass * 1e3), "unit": "GB/s",
             "cores": orc.num_threads(), "kind": "oracle", "sample": sample,
             "us_per_call_equiv": per_pass / frac * 1e6}
+
+
+def dense_oracle(orc, cfg, q, k, v, rows=None):
+    """The oracle's dense decode for a dense workload (Dqk != Dv included)."""
+    if cfg.dv == cfg.D:
+        return orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
+    return orc.gqa_decode_dv(q, k, v, cfg.scale, rows=rows)
 
 
 def _paged_kv_oracle_timing(orc, cfg, cpu, max_seconds, min_seconds) -> dict:
@@ -487,7 +501,37 @@ def run_gqa(args) -> int:
 
     # ---- end to end through the host-buffer entry point (dense path)
     e2e = None
-    if not args.no_e2e and isinstance(cfg, gqa_inputs.DenseConfig):
+    if not args.no_e2e and isinstance(cfg, gqa_inputs.DenseConfig) and cfg.dv != cfg.D:
+        # no host-buffer entry point for this flavour: pinned host -> device
+        # copies, the device call and the device -> host copies of out / lse,
+        # all inside the timed call
+        qh, kh, vh = (tensors[n].cpu().pin_memory() for n in ("q", "k", "v"))
+        oh = torch.empty(tuple(tensors["out"].shape), dtype=torch.bfloat16).pin_memory()
+        lh = torch.empty(tuple(tensors["lse"].shape), dtype=torch.float32).pin_memory()
+        qd, kd, vd = (torch.empty_like(t, device=dev) for t in (qh, kh, vh))
+        od, ld = torch.empty_like(oh, device=dev), torch.empty_like(lh, device=dev)
+
+        def e2e_call():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            gq.gqa_decode_dv(qd, kd, vd, out=od, lse=ld)
+            oh.copy_(od, non_blocking=True)
+            lh.copy_(ld, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        e2e_call()  # warm-up
+        ts = []
+        for _ in range(max(1, args.e2e_steps)):
+            t0 = time.perf_counter()
+            e2e_call()
+            ts.append((time.perf_counter() - t0) * 1e3)
+        (e2e_ms,) = reduce_over_ranks([statistics.mean(ts)], "max")
+        e2e = {"value": gbs(world * nbytes, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": (qh.numel() + kh.numel() + vh.numel()) * 2,
+               "d2h_bytes_per_step": oh.numel() * 2 + lh.numel() * 4,
+               "api": "gqa_decode_dv with pinned host copies in the timed call"}
+        del qh, kh, vh, oh, lh, qd, kd, vd, od, ld
+    elif not args.no_e2e and isinstance(cfg, gqa_inputs.DenseConfig):
         qh = tensors["q"].cpu().pin_memory()
         kh = tensors["k"].cpu().pin_memory()
         vh = tensors["v"].cpu().pin_memory()
@@ -568,13 +612,13 @@ def run_reference(args) -> int:
         q, k, v = gqa_inputs.dense_config_inputs(cfg, device="cpu")
         nrows = cfg.B * cfg.Hq * cfg.Sq
         t0 = time.perf_counter()
-        orc.gqa_decode(q, k, v, cfg.scale, rows=list(range(min(8, nrows))))
+        dense_oracle(orc, cfg, q, k, v, rows=list(range(min(8, nrows))))
         per_row = (time.perf_counter() - t0) / min(8, nrows)
         budget_s = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
         rows = None if per_row * nrows <= budget_s else list(range(max(1, int(budget_s / per_row))))
 
         def step():
-            orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
+            dense_oracle(orc, cfg, q, k, v, rows=rows)
     elif isinstance(cfg, gqa_inputs.PagedKVConfig):
         inp = gqa_inputs.paged_kv_config_inputs(cfg, device="cpu")
         budget_s = 150.0 / max(1, args.steps + args.warmup)

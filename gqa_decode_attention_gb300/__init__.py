@@ -33,7 +33,9 @@ GQA_OK = 0
 # Every symbol the headers in include/ declare.
 EXPORTS = [
     "gqa_status_string", "gqa_version", "gqa_decode", "gqa_decode_num_splits",
-    "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
+    "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_dv", "gqa_decode_dv_num_splits",
+    "gqa_decode_dv_workspace_bytes",
+    "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
     "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged", "gqa_decode_paged_ex",
     "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes", "gqa_decode_paged_dev_scales",
     "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
@@ -71,6 +73,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_workspace_bytes.argtypes = [i] * 7
     lib.gqa_decode_ex.restype = st
     lib.gqa_decode_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.gqa_decode_dv.restype = st
+    lib.gqa_decode_dv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
+    lib.gqa_decode_dv_num_splits.restype = i
+    lib.gqa_decode_dv_num_splits.argtypes = [i] * 7
+    lib.gqa_decode_dv_workspace_bytes.restype = sz
+    lib.gqa_decode_dv_workspace_bytes.argtypes = [i] * 8
     lib.gqa_decode_noalloc.restype = st
     lib.gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
     lib.gqa_decode_noalloc_scratch_bytes.restype = sz
@@ -165,6 +173,44 @@ def gqa_decode_ex(q, k, v, out=None, lse=None, scale=None, num_splits=0, workspa
                            _scale_arg(scale), int(num_splits), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "gqa_decode_ex")
     return out, lse
+
+
+def gqa_decode_dv(q, k, v, out=None, lse=None, scale=None, num_splits=0, workspace=None, stream=None,
+                  with_lse=True):
+    """Dense decode with a score head size Dqk (q, k) different from the value
+    head size Dv (v, out): q [B,Sq,Hq,Dqk], k [B,Skv,Hkv,Dqk], v [B,Skv,Hkv,Dv].
+
+    Returns (out [B,Sq,Hq,Dv] bf16, lse [B,Hq,Sq] fp32 or None)."""
+    lib = load_library()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, "cuda")
+    B, Sq, Hq, Dqk = q.shape
+    _, Skv, Hkv, _ = k.shape
+    Dv = v.shape[-1]
+    if tuple(v.shape[:3]) != (B, Skv, Hkv) or tuple(k.shape) != (B, Skv, Hkv, Dqk):
+        raise ValueError("gqa_decode_dv: k must be [B,Skv,Hkv,Dqk] and v [B,Skv,Hkv,Dv]")
+    if out is None:
+        out = torch.empty((B, Sq, Hq, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and with_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    st = lib.gqa_decode_dv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Skv, Hq, Hkv, Dqk, Dv,
+                           _scale_arg(scale), int(num_splits), ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "gqa_decode_dv")
+    return out, lse
+
+
+def gqa_decode_dv_num_splits(B, Sq, Skv, Hq, Hkv, Dqk, Dv) -> int:
+    n = load_library().gqa_decode_dv_num_splits(B, Sq, Skv, Hq, Hkv, Dqk, Dv)
+    if n < 0:
+        raise GQAError(-n, "gqa_decode_dv_num_splits")
+    return n
+
+
+def gqa_decode_dv_workspace_bytes(B, Sq, Skv, Hq, Hkv, Dqk, Dv, num_splits=0) -> int:
+    return int(load_library().gqa_decode_dv_workspace_bytes(B, Sq, Skv, Hq, Hkv, Dqk, Dv, int(num_splits)))
 
 
 def gqa_decode_noalloc(q, k, v, out, lse=None, scale=None, num_splits=0, stream=None):

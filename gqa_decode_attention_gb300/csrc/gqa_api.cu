@@ -36,7 +36,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------ device facts
 std::mutex g_mu;
 int g_sm_count[kMaxDevices];
-int g_occ[kMaxDevices][3][kDenseCfgs];
+int g_occ[kMaxDevices][4][kDenseCfgs];
 
 bool current_device(int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return false;
@@ -53,7 +53,7 @@ int sm_count(int dev) {
     return g_sm_count[dev];
 }
 
-int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : D == 192 ? 3 : 2; }
 
 unsigned *g_err_ptr[kMaxDevices];
 
@@ -101,7 +101,10 @@ int dense_occupancy(int dev, int D, int cfg) {
     std::lock_guard<std::mutex> lk(g_mu);
     int &slot = g_occ[dev][d_index(D)][cfg];
     if (slot == 0) {
-        slot = D == 64 ? dense_ctas_per_sm_d64(cfg) : D == 128 ? dense_ctas_per_sm_d128(cfg) : dense_ctas_per_sm_d256(cfg);
+        slot = D == 64    ? dense_ctas_per_sm_d64(cfg)
+               : D == 128 ? dense_ctas_per_sm_d128(cfg)
+               : D == 192 ? dense_ctas_per_sm_d192x128(cfg)
+                          : dense_ctas_per_sm_d256(cfg);
     }
     return slot;
 }
@@ -127,12 +130,17 @@ EncodeTiledFn encode_fn() {
 // ------------------------------------------------------------ dense shapes
 struct DenseShape {
     int B, Sq, Skv, Hq, Hkv, D, G, Mq, cfg, qrows, row_groups, n_blocks;  // blocks of kSplitKeys keys
+    int Dv;  // value head size (= D except for the d192x128 flavour)
 };
 
-gqa_status check_dense(int B, int Sq, int Skv, int Hq, int Hkv, int D, DenseShape *s) {
+// D: score head size (q, K); Dv: value head size (V, out).  Supported:
+// D = Dv in {64, 128, 256}, and D = 192 with Dv = 128.
+gqa_status check_dense_dv(int B, int Sq, int Skv, int Hq, int Hkv, int D, int Dv, DenseShape *s) {
     if (B < 1 || Sq < 1 || Skv < 1 || Hq < 1 || Hkv < 1) return GQA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0 || Sq > Skv) return GQA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128 && D != 256) return GQA_ERR_UNSUPPORTED;
+    const bool same = D == Dv && (D == 64 || D == 128 || D == 256);
+    if (!same && !(D == 192 && Dv == 128)) return GQA_ERR_UNSUPPORTED;
+    s->Dv = Dv;
     const long G = Hq / Hkv;
     const long Mq = G * Sq;
     if (Mq > kMaxGroupRows) return GQA_ERR_UNSUPPORTED;
@@ -152,6 +160,10 @@ gqa_status check_dense(int B, int Sq, int Skv, int Hq, int Hkv, int D, DenseShap
     if (long(Hkv) * s->row_groups > 65535) return GQA_ERR_UNSUPPORTED;
     s->n_blocks = (Skv + kSplitKeys - 1) / kSplitKeys;
     return GQA_OK;
+}
+
+gqa_status check_dense(int B, int Sq, int Skv, int Hq, int Hkv, int D, DenseShape *s) {
+    return check_dense_dv(B, Sq, Skv, Hq, Hkv, D, D, s);
 }
 
 // Split count.  The kernel is HBM-bound once about kCtasPerSmTarget CTAs are
@@ -207,7 +219,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 size_t workspace_bytes(const DenseShape &s, int splits) {
     if (splits <= 1) return 0;
     const size_t rows = size_t(s.B) * s.Hkv * splits * s.Mq;
-    return align256(rows * s.D * sizeof(float)) + align256(rows * sizeof(float));
+    return align256(rows * s.Dv * sizeof(float)) + align256(rows * sizeof(float));
 }
 
 // key blocks per split as the kernel sees it for a split count
@@ -247,7 +259,7 @@ gqa_status run_dense(const void *q, const void *k, const void *v, void *out, flo
     if (need > 0) {
         const size_t rows = size_t(s.B) * s.Hkv * splits * s.Mq;
         a.o_part = static_cast<float *>(ws);
-        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + align256(rows * s.D * sizeof(float)));
+        a.lse_part = reinterpret_cast<float *>(static_cast<char *>(ws) + align256(rows * s.Dv * sizeof(float)));
     }
     a.B = s.B;
     a.Sq = s.Sq;
@@ -271,7 +283,10 @@ gqa_status run_dense(const void *q, const void *k, const void *v, void *out, flo
     L.stream = stream;
     L.ev_before = g_ev_before.load();
     L.ev_after = g_ev_after.load();
-    cudaError_t e = s.D == 64 ? launch_dense_d64(L) : s.D == 128 ? launch_dense_d128(L) : launch_dense_d256(L);
+    cudaError_t e = s.D == 64    ? launch_dense_d64(L)
+                    : s.D == 128 ? launch_dense_d128(L)
+                    : s.D == 192 ? launch_dense_d192x128(L)
+                                 : launch_dense_d256(L);
     if (owned) cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -473,14 +488,41 @@ gqa_status gqa_decode_ex(const void *q, const void *k, const void *v, void *out,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
+gqa_status gqa_decode_dv(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Sq, int Skv,
+                         int Hq, int Hkv, int Dqk, int Dv, float scale, int num_splits, void *workspace,
+                         size_t workspace_bytes_, gqa_stream_t stream) {
+    DenseShape s;
+    gqa_status st = check_dense_dv(B, Sq, Skv, Hq, Hkv, Dqk, Dv, &s);
+    if (st != GQA_OK) return st;
+    if (num_splits < 0) return GQA_ERR_INVALID_ARG;
+    st = check_dense_ptrs(q, k, v, out, lse);
+    if (st != GQA_OK) return st;
+    return run_dense(q, k, v, out, lse, s, resolve_scale(scale, Dqk), num_splits, workspace, workspace_bytes_,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gqa_decode_dv_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv, int num_splits) {
+    DenseShape s;
+    if (check_dense_dv(B, Sq, Skv, Hq, Hkv, Dqk, Dv, &s) != GQA_OK || num_splits < 0) return 0;
+    int dev = 0;
+    if (num_splits == 0 && !current_device(&dev)) return 0;
+    const int splits = choose_splits(s, num_splits, dev);
+    const int tps = blocks_per_split(s, splits);
+    return workspace_bytes(s, (s.n_blocks + tps - 1) / tps);
+}
+
 gqa_status gqa_decode(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Sq, int Skv,
                       int Hq, int Hkv, int D, float scale, gqa_stream_t stream) {
     return gqa_decode_ex(q, k, v, out, lse, B, Sq, Skv, Hq, Hkv, D, scale, 0, nullptr, 0, stream);
 }
 
 int gqa_decode_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int D) {
+    return gqa_decode_dv_num_splits(B, Sq, Skv, Hq, Hkv, D, D);
+}
+
+int gqa_decode_dv_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv) {
     DenseShape s;
-    gqa_status st = check_dense(B, Sq, Skv, Hq, Hkv, D, &s);
+    gqa_status st = check_dense_dv(B, Sq, Skv, Hq, Hkv, Dqk, Dv, &s);
     if (st != GQA_OK) return -int(st);
     int dev = 0;
     if (!current_device(&dev)) return -int(GQA_ERR_CUDA);

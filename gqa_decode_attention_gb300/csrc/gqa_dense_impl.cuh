@@ -8,18 +8,19 @@
 
 namespace gqa {
 
-template <int D, int CFG>
+// D: score head size (q, K); DV: value head size (V, O).
+template <int D, int DV, int CFG>
 struct DenseInst {
     static constexpr int RB = 1 << CFG;
     static constexpr int T = dense_tile_keys(D, CFG);
     static constexpr int S = dense_stages(D, CFG);
-    using C = DenseCfg<D, RB, T, S>;
-    static constexpr auto kernel() { return gqa_dense_split_kernel<D, RB, T, S>; }
+    using C = DenseCfg<D, DV, RB, T, S>;
+    static constexpr auto kernel() { return gqa_dense_split_kernel<D, DV, RB, T, S>; }
 };
 
-template <int D, int CFG>
+template <int D, int DV, int CFG>
 static cudaError_t launch_split_cfg(const DenseLaunch &L) {
-    using I = DenseInst<D, CFG>;
+    using I = DenseInst<D, DV, CFG>;
     using C = typename I::C;
     auto kern = I::kernel();
     static bool attr_set = false;  // per process; the attribute is per function
@@ -30,7 +31,7 @@ static cudaError_t launch_split_cfg(const DenseLaunch &L) {
     }
     CUtensorMap tk, tv;
     if (!make_kv_tensor_map(&tk, L.k, L.args.B, L.args.Skv, L.args.Hkv, D, I::T) ||
-        !make_kv_tensor_map(&tv, L.v, L.args.B, L.args.Skv, L.args.Hkv, D, I::T))
+        !make_kv_tensor_map(&tv, L.v, L.args.B, L.args.Skv, L.args.Hkv, DV, I::T))
         return cudaErrorInvalidValue;
     const dim3 grid(L.args.Hkv * L.args.row_groups, L.args.num_splits, L.args.B);
     const bool timed = L.ev_before != nullptr && L.ev_after != nullptr;
@@ -40,9 +41,9 @@ static cudaError_t launch_split_cfg(const DenseLaunch &L) {
     return cudaGetLastError();
 }
 
-template <int D, int CFG>
+template <int D, int DV, int CFG>
 static int occupancy_cfg() {
-    using I = DenseInst<D, CFG>;
+    using I = DenseInst<D, DV, CFG>;
     using C = typename I::C;
     auto kern = I::kernel();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
@@ -123,26 +124,26 @@ static int umma_occupancy() {
     return n;
 }
 
-template <int D>
+template <int D, int DV = D>
 static cudaError_t launch_dense(const DenseLaunch &L) {
     cudaError_t e;
     switch (L.cfg) {
-        case 0: e = launch_split_cfg<D, 0>(L); break;
-        case 1: e = launch_split_cfg<D, 1>(L); break;
-        case 2: e = launch_split_cfg<D, 2>(L); break;
-        default: e = launch_split_cfg<D, 3>(L); break;
+        case 0: e = launch_split_cfg<D, DV, 0>(L); break;
+        case 1: e = launch_split_cfg<D, DV, 1>(L); break;
+        case 2: e = launch_split_cfg<D, DV, 2>(L); break;
+        default: e = launch_split_cfg<D, DV, 3>(L); break;
     }
     if (e != cudaSuccess || L.args.num_splits == 1) return e;
-    return launch_combine<D>(L);
+    return launch_combine<DV>(L);
 }
 
-template <int D>
+template <int D, int DV = D>
 static int dense_occupancy(int cfg) {
     switch (cfg) {
-        case 0: return occupancy_cfg<D, 0>();
-        case 1: return occupancy_cfg<D, 1>();
-        case 2: return occupancy_cfg<D, 2>();
-        default: return occupancy_cfg<D, 3>();
+        case 0: return occupancy_cfg<D, DV, 0>();
+        case 1: return occupancy_cfg<D, DV, 1>();
+        case 2: return occupancy_cfg<D, DV, 2>();
+        default: return occupancy_cfg<D, DV, 3>();
     }
 }
 

@@ -36,14 +36,16 @@ constexpr int kStepKeys = 16;
 // Shape of one kernel instance: RB consumer warps (16 rows each), TMA tiles of
 // T keys, STAGES ring slots.  Chosen per (head dim, row count) so small-group
 // CTAs are small and many fit on an SM.
-template <int D, int RB, int T, int STAGES_>
+template <int D, int DV, int RB, int T, int STAGES_>
 struct DenseCfg {
     static constexpr int NC = RB;
     static constexpr int THREADS = 32 * (NC + 1);
     static constexpr int STAGES = STAGES_;
-    static constexpr int CHUNKS = D / 64;  // 128-byte swizzle atoms per row
-    static constexpr int TILE_BYTES = T * D * 2;
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int K_CHUNKS = D / 64;   // 128-byte swizzle atoms per K row (D = score head size)
+    static constexpr int V_CHUNKS = DV / 64;  // ... per V row (DV = value head size)
+    static constexpr int K_TILE_BYTES = T * D * 2;
+    static constexpr int V_TILE_BYTES = T * DV * 2;
+    static constexpr int STAGE_BYTES = K_TILE_BYTES + V_TILE_BYTES;
     static constexpr int QROWS = RB * 16;
     static constexpr int Q_BYTES = QROWS * D * 2;
     static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
@@ -54,11 +56,11 @@ struct DenseCfg {
     static_assert(kSplitKeys % T == 0 && T % kStepKeys == 0, "tile must divide the split granule");
 };
 
-template <int D, int RB, int T, int STAGES_>
-__global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg<D, RB, T, STAGES_>::MIN_BLOCKS)
+template <int D, int DV, int RB, int T, int STAGES_>
+__global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, DenseCfg<D, DV, RB, T, STAGES_>::MIN_BLOCKS)
     gqa_dense_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            const DenseArgs a) {
-    using C = DenseCfg<D, RB, T, STAGES_>;
+    using C = DenseCfg<D, DV, RB, T, STAGES_>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem;
@@ -108,13 +110,13 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
                     continue;  // test hook: this stage never fills
                 }
                 uint8_t *ks = ring + st * C::STAGE_BYTES;
-                uint8_t *vs = ks + C::TILE_BYTES;
+                uint8_t *vs = ks + C::K_TILE_BYTES;
                 const int j0 = key_begin + it * T;
                 mbar_arrive_expect_tx(&full[st], C::STAGE_BYTES);
 #pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c) tma_load_4d(ks + c * T * 128, &tmK, &full[st], c * 64, g, j0, b);
+                for (int c = 0; c < C::K_CHUNKS; ++c) tma_load_4d(ks + c * T * 128, &tmK, &full[st], c * 64, g, j0, b);
 #pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c) tma_load_4d(vs + c * T * 128, &tmV, &full[st], c * 64, g, j0, b);
+                for (int c = 0; c < C::V_CHUNKS; ++c) tma_load_4d(vs + c * T * 128, &tmV, &full[st], c * 64, g, j0, b);
                 issued = it + 1;
             }
             if (!ok) {
@@ -167,9 +169,9 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
 
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
-    float o[D / 8][4];
+    float o[DV / 8][4];
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    for (int nt = 0; nt < DV / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
     const uint32_t q_base = smem_u32(qs);
     const uint32_t ring_base = smem_u32(ring);
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
             break;
         }
         const uint32_t kb = ring_base + st * C::STAGE_BYTES;
-        const uint32_t vb = kb + C::TILE_BYTES;
+        const uint32_t vb = kb + C::K_TILE_BYTES;
 #pragma unroll 1
         for (int sub = 0; sub < T / kStepKeys; ++sub) {
             const int krow0 = sub * kStepKeys;  // first key row of this step in the tile
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
                                     pack_bf16x2(s[1][0], s[1][1]), pack_bf16x2(s[1][2], s[1][3])};
             if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt) {
+                for (int nt = 0; nt < DV / 8; ++nt) {
                     o[nt][0] *= corr[0];
                     o[nt][1] *= corr[0];
                     o[nt][2] *= corr[1];
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
             // ---- O += P V
             const int vrow = krow0 + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
+            for (int dp = 0; dp < DV / 16; ++dp) {
                 const int unit = dp * 2 + (lane >> 4);
                 const uint32_t addr = vb + (unit >> 3) * (T * 128) + swz128(vrow, unit & 7);
                 uint32_t b0, b1, b2, b3;
@@ -302,18 +304,18 @@ __global__ void __launch_bounds__(DenseCfg<D, RB, T, STAGES_>::THREADS, DenseCfg
         const int i = r / a.G;
         const int h = g * a.G + (r % a.G);
         if (a.num_splits == 1) {
-            __nv_bfloat16 *dst = a.out + ((size_t(b) * a.Sq + i) * a.Hq + h) * D + (lane & 3) * 2;
+            __nv_bfloat16 *dst = a.out + ((size_t(b) * a.Sq + i) * a.Hq + h) * DV + (lane & 3) * 2;
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt)
+            for (int nt = 0; nt < DV / 8; ++nt)
                 *reinterpret_cast<uint32_t *>(dst + nt * 8) =
                     pack_bf16x2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
             if (a.lse != nullptr && (lane & 3) == 0)
                 a.lse[(size_t(b) * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
         } else {
             const size_t prow = (size_t(unit) * a.Mq + r) * a.num_splits + split;
-            float *dst = a.o_part + prow * D + (lane & 3) * 2;
+            float *dst = a.o_part + prow * DV + (lane & 3) * 2;
 #pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt)
+            for (int nt = 0; nt < DV / 8; ++nt)
                 *reinterpret_cast<float2 *>(dst + nt * 8) = make_float2(o[nt][2 * hr] * inv, o[nt][2 * hr + 1] * inv);
             if ((lane & 3) == 0) a.lse_part[prow] = lse2;
         }

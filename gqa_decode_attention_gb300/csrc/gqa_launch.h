@@ -28,12 +28,16 @@ inline int dense_rows_per_cta(int D, int cfg) { return D == 256 ? 128 : dense_cf
 #ifndef GQA_D128_R16_STAGES
 #define GQA_D128_R16_STAGES 3
 #endif
+// (D is the score head size; the d192x128 flavour uses the D = 192 row.)
 constexpr int dense_tile_keys(int D, int cfg) {
     return D == 64 ? (cfg == 0 ? 32 : 64) : D == 128 ? (cfg == 0 ? GQA_D128_R16_TILE : cfg == 1 ? 32 : 64)
-                                                     : (cfg <= 1 ? 16 : cfg == 2 ? 32 : 64);
+         : D == 192 ? (cfg <= 1 ? 16 : 32)
+                    : (cfg <= 1 ? 16 : cfg == 2 ? 32 : 64);
 }
 constexpr int dense_stages(int D, int cfg) {
-    return D == 64 ? (cfg <= 1 ? 3 : 4) : D == 128 ? (cfg == 0 ? GQA_D128_R16_STAGES : 3) : (cfg == 1 ? 4 : cfg == 3 ? 2 : 3);
+    return D == 64 ? (cfg <= 1 ? 3 : 4) : D == 128 ? (cfg == 0 ? GQA_D128_R16_STAGES : 3)
+         : D == 192 ? 3
+                    : (cfg == 1 ? 4 : cfg == 3 ? 2 : 3);
 }
 
 struct DenseLaunch {
@@ -55,6 +59,9 @@ bool make_kv_tensor_map(CUtensorMap *map, const void *base, int B, int Skv, int 
 cudaError_t launch_dense_d64(const DenseLaunch &L);
 cudaError_t launch_dense_d128(const DenseLaunch &L);
 cudaError_t launch_dense_d256(const DenseLaunch &L);
+// Score head size 192, value head size 128 (mma.sync engine).
+cudaError_t launch_dense_d192x128(const DenseLaunch &L);
+int dense_ctas_per_sm_d192x128(int cfg);
 // Resident CTAs per SM of the dense split kernel for (D, cfg); 0 on error.
 int dense_ctas_per_sm_d64(int cfg);
 int dense_ctas_per_sm_d128(int cfg);

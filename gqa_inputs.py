@@ -42,10 +42,15 @@ class DenseConfig:
     Hkv: int
     D: int
     seed: int
+    Dv: int = 0  # value head size; 0 = D
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.D)
+
+    @property
+    def dv(self) -> int:
+        return self.Dv or self.D
 
 
 @dataclasses.dataclass(frozen=True)
@@ -97,6 +102,10 @@ CONFIGS = {
         "dense_b32_h64x8_d128_sq1_kv32k", B=32, Sq=1, Skv=32768, Hq=64, Hkv=8, D=128, seed=1003),
     "dense_b8_h32x2_d256_sq8_kv128k": DenseConfig(
         "dense_b8_h32x2_d256_sq8_kv128k", B=8, Sq=8, Skv=131072, Hq=32, Hkv=2, D=256, seed=1004),
+    # the d192x128 head flavour (scores over 192 dims, values of 128) on the
+    # headline's long-cache shape
+    "dense_b1_h64x8_d192x128_sq2_kv128k": DenseConfig(
+        "dense_b1_h64x8_d192x128_sq2_kv128k", B=1, Sq=2, Skv=131072, Hq=64, Hkv=8, D=192, Dv=128, seed=1009),
     "paged_fp8_b256_h32x8_d128_top512_ps16": PagedConfig(
         "paged_fp8_b256_h32x8_d128_top512_ps16", B=256, Hq=32, Hkv=8, D=128, page_size=16,
         pages_per_req=32, num_pages=8192, topk=512, seed=1005),
@@ -136,17 +145,18 @@ def _randn_bf16(shape, g: torch.Generator, device, chunk_elems: int = 1 << 28) -
     return out.view(*shape)
 
 
-def dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed, device="cpu"):
-    """q [B,Sq,Hq,D], k, v [B,Skv,Hkv,D], all bf16 ~ N(0,1)."""
+def dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed, device="cpu", Dv=None):
+    """q [B,Sq,Hq,D], k [B,Skv,Hkv,D], v [B,Skv,Hkv,Dv] (Dv defaults to D),
+    all bf16 ~ N(0,1)."""
     g = _gen(seed, device)
     q = _randn_bf16((B, Sq, Hq, D), g, device)
     k = _randn_bf16((B, Skv, Hkv, D), g, device)
-    v = _randn_bf16((B, Skv, Hkv, D), g, device)
+    v = _randn_bf16((B, Skv, Hkv, D if Dv is None else Dv), g, device)
     return q, k, v
 
 
 def dense_config_inputs(cfg: DenseConfig, device="cpu"):
-    return dense_inputs(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D, cfg.seed, device)
+    return dense_inputs(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D, cfg.seed, device, Dv=cfg.dv)
 
 
 def quantize_e4m3fn(x: torch.Tensor):

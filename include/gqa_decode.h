@@ -122,6 +122,33 @@ gqa_status gqa_decode_ex(const void *q, const void *k, const void *v, void *out,
                          int num_splits, void *workspace, size_t workspace_bytes,
                          gqa_stream_t stream);
 
+/* Dense decode whose score head size differs from its value head size.
+ * The page "When the K/V copy costs more than the attention", section
+ * "Limits, and what I'd do next", lists a d192x128 head flavour beside d64
+ * and d128: q and K carry Dqk = 192 dims, V and the output Dv = 128.  The
+ * operation is gqa_decode's with the dot product over Dqk dims and the
+ * weighted sum over Dv dims:
+ *   out[b,i,h,:] = sum_j softmax_j(scale * q[b,i,h,:] . k[b,j,g,:]) v[b,j,g,:]
+ * Layouts: q [B, Sq, Hq, Dqk], k [B, Skv, Hkv, Dqk], v [B, Skv, Hkv, Dv],
+ * out [B, Sq, Hq, Dv] bf16; lse [B, Hq, Sq] fp32 or NULL.
+ * Supported (Dqk, Dv): (192, 128), and Dqk == Dv in {64, 128, 256}, which
+ * runs exactly what gqa_decode_ex runs.  Other pairs: GQA_ERR_UNSUPPORTED.
+ * scale <= 0 or NaN selects 1 / sqrt(Dqk).  num_splits, workspace and every
+ * other limit and convention are gqa_decode_ex's; the workspace holds fp32
+ * partials of Dv dims per row. */
+gqa_status gqa_decode_dv(const void *q, const void *k, const void *v, void *out, float *lse,
+                         int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv, float scale,
+                         int num_splits, void *workspace, size_t workspace_bytes,
+                         gqa_stream_t stream);
+
+/* Split count gqa_decode_dv would use (>= 1), or a negative gqa_status. */
+int gqa_decode_dv_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv);
+
+/* Bytes of workspace gqa_decode_dv needs for `num_splits` (0 = automatic);
+ * 0 when a single split is used or on invalid arguments. */
+size_t gqa_decode_dv_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv,
+                                     int num_splits);
+
 /* Allocation-free dense decode.  The pages have no counterpart to this entry
  * point; it exists for callers that cannot allocate device memory while they
  * decode (a memory budget fixed at start-up, real-time loops where an

@@ -87,6 +87,30 @@ def test_dense_ex_rejects(lib):
     assert lib.gqa_decode_num_splits(1, 1, 64, 8, 2, 96) == -2
 
 
+def test_dense_dv_rejects(lib):
+    def dv(Dqk=192, Dv=128, splits=0, B=1, Sq=1, Skv=64, Hq=8, Hkv=2, q=A, v=A, ws_bytes=0):
+        return lib.gqa_decode_dv(q, A, v, A, A, B, Sq, Skv, Hq, Hkv, Dqk, Dv, 0.0, splits, None, ws_bytes, None)
+    assert dv(Dqk=128, Dv=192) == 2      # only (192, 128) and equal sizes
+    assert dv(Dqk=192, Dv=192) == 2
+    assert dv(Dqk=192, Dv=64) == 2
+    assert dv(Dqk=96, Dv=96) == 2
+    assert dv(Hq=6, Hkv=4) == 1
+    assert dv(Sq=3, Skv=2) == 1
+    assert dv(splits=-1) == 1
+    assert dv(q=0) == 1
+    assert dv(v=MIS) == 3
+    assert lib.gqa_decode_dv_workspace_bytes(1, 1, 64, 8, 2, 128, 192, 0) == 0
+    # explicit split count needs no device: 2 splits of the 2 blocks of 64 keys,
+    # rows = B * Hkv * splits * (G * Sq), fp32 partials of Dv dims plus one LSE each
+    rows = 1 * 2 * 2 * 4
+    want = ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert lib.gqa_decode_dv_workspace_bytes(1, 1, 128, 8, 2, 192, 128, 2) == want
+    assert lib.gqa_decode_dv_workspace_bytes(1, 1, 128, 8, 2, 192, 128, 1) == 0
+    # equal sizes report what the dense entry point reports
+    assert (lib.gqa_decode_dv_workspace_bytes(1, 1, 300, 8, 2, 128, 128, 3)
+            == lib.gqa_decode_workspace_bytes(1, 1, 300, 8, 2, 128, 3))
+
+
 def _paged(lib, q=A, gate=A, kp=A, vp=A, pt=A, tk=A, ks=1.0, vs=1.0, out=A, lse=A, B=2, Hq=8, Hkv=2, D=128,
            ps=16, ppr=4, num_pages=16, topk=32):
     return lib.gqa_decode_paged_fp8(q, gate, kp, vp, pt, tk, ks, vs, out, lse, B, Hq, Hkv, D, ps, ppr,

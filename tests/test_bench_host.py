@@ -48,6 +48,8 @@ def test_workload_bytes():
     assert bench.workload_kv_bytes(c["dense_b8_h32x2_d256_sq8_kv128k"]) == 2 << 30
     assert bench.workload_kv_bytes(c["paged_fp8_b256_h32x8_d128_top512_ps16"]) == 256 << 20
     assert bench.workload_kv_bytes(c["dense_b1_h8x1_d64_sq1_kv1k"]) == 256 << 10
+    # 131072 keys x 8 KV heads x (192 K dims + 128 V dims) x 2 bytes
+    assert bench.workload_kv_bytes(c["dense_b1_h64x8_d192x128_sq2_kv128k"]) == 640 << 20
 
 
 CLOCKS = """index, clocks.current.sm [MHz], clocks.max.sm [MHz], power.draw [W], clocks_event_reasons.active, clocks_event_reasons.hw_slowdown, clocks_event_reasons.hw_thermal_slowdown, clocks_event_reasons.sw_thermal_slowdown, clocks_event_reasons.sw_power_cap
