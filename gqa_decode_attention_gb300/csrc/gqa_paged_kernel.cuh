@@ -499,13 +499,45 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 const bool tv0 = (mask >> gi) & 1u, tv1 = (mask >> (gi + 8)) & 1u;
                 const int tok0 = t_begin + base_k + s * C::T + gi;  // token index (whole-request form)
 
-                // ---- S^T = K . Q^T
+                // ---- K words of tokens gi and gi + 8
                 uint4 kr[2][C::KU];
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int u = 0; u < C::KU; ++u)
                         kr[j][u] = *reinterpret_cast<const uint4 *>(kst + (gi + 8 * j) * C::KRS + kcol + u * 64 + 16 * c);
+                // ---- V words of tokens 2c, 2c+1, 2c+8, 2c+9 (rows of padding
+                // tokens zeroed: their ring slots hold stale bytes).  Read with
+                // the K words, before any arithmetic, so the stage goes back to
+                // the producer as early as possible: the stream is bound by the
+                // bytes in flight, and a stage held through the step's compute
+                // is a stage not loading.
+                uint32_t vw[4][C::VW];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int tkn = 2 * c + (j & 1) + 8 * (j >> 1);
+                    const bool ok = (mask >> tkn) & 1u;
+                    const uint8_t *vrow = vst + tkn * C::VRS + kcol;
+                    if constexpr (KV8 && C::VB == 8) {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(vrow + 8 * gi);
+                        vw[j][0] = ok ? x.x : 0u;
+                        vw[j][1] = ok ? x.y : 0u;
+                    } else {
+                        // 16-byte chunks: FP8 one at byte 16 gi; bf16 one per 64 elements at 128 m + 16 gi
+#pragma unroll
+                        for (int m = 0; m < C::VW / 4; ++m) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(vrow + 128 * m + 16 * gi);
+                            vw[j][4 * m + 0] = ok ? x.x : 0u;
+                            vw[j][4 * m + 1] = ok ? x.y : 0u;
+                            vw[j][4 * m + 2] = ok ? x.z : 0u;
+                            vw[j][4 * m + 3] = ok ? x.w : 0u;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + st);  // ring slot free for the producer
+
+                // ---- S^T = K . Q^T
                 float st_[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) st_[nt][0] = st_[nt][1] = st_[nt][2] = st_[nt][3] = 0.f;
@@ -592,33 +624,6 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                         }
                 }
 
-                // ---- V words of tokens 2c, 2c+1, 2c+8, 2c+9 (rows of padding
-                // tokens zeroed: their ring slots hold stale bytes), then the
-                // stage is released.
-                uint32_t vw[4][C::VW];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tkn = 2 * c + (j & 1) + 8 * (j >> 1);
-                    const bool ok = (mask >> tkn) & 1u;
-                    const uint8_t *vrow = vst + tkn * C::VRS + kcol;
-                    if constexpr (KV8 && C::VB == 8) {
-                        const uint2 x = *reinterpret_cast<const uint2 *>(vrow + 8 * gi);
-                        vw[j][0] = ok ? x.x : 0u;
-                        vw[j][1] = ok ? x.y : 0u;
-                    } else {
-                        // 16-byte chunks: FP8 one at byte 16 gi; bf16 one per 64 elements at 128 m + 16 gi
-#pragma unroll
-                        for (int m = 0; m < C::VW / 4; ++m) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(vrow + 128 * m + 16 * gi);
-                            vw[j][4 * m + 0] = ok ? x.x : 0u;
-                            vw[j][4 * m + 1] = ok ? x.y : 0u;
-                            vw[j][4 * m + 2] = ok ? x.z : 0u;
-                            vw[j][4 * m + 3] = ok ? x.w : 0u;
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty + st);  // ring slot free for the producer
 
                 // ---- O^T += V^T . P^T, tokens 2c, 2c+1 (a0, a1) and 2c+8, 2c+9 (a2, a3)
                 if constexpr (KV8) {
