@@ -184,6 +184,12 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
 }
 
 // Programmatic dependent launch controls.
+// 16-byte asynchronous global -> shared copy that bypasses L1; the issuing
+// thread sees it after cp_async_wait_all().
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

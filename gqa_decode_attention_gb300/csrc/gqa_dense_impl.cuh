@@ -60,7 +60,7 @@ static cudaError_t launch_combine_rows(const float *o_part, const float *lse_par
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(rows));
     cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = (size_t((S + 3) & ~3) + size_t(kCombineThreads) * 4) * sizeof(float);
+    cfg.dynamicSmemBytes = (size_t(combine_staged_splits<D>(S)) * (D / 4) + kCombineThreads) * sizeof(float4);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -77,7 +77,7 @@ static cudaError_t launch_combine(const DenseLaunch &L) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(rows));
     cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = (size_t((a.num_splits + 3) & ~3) + size_t(kCombineThreads) * 4) * sizeof(float);
+    cfg.dynamicSmemBytes = (size_t(combine_staged_splits<D>(a.num_splits)) * (D / 4) + kCombineThreads) * sizeof(float4);
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

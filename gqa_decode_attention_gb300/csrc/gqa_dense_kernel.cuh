@@ -324,85 +324,79 @@ __global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, Dens
 
 // LSE-weighted combine of the split partials.  One CTA per output row
 // (b, h, i): the split LSEs give weights w_s = 2^(lse_s - max) (a split that
-// saw no visible key has lse_s = -inf and weight exactly 0), then the CTA's
-// threads split the (split, head-dim) plane, accumulate w_s * O_s with many
-// loads in flight, and reduce across splits through shared memory.
+// saw no visible key has lse_s = -inf and weight exactly 0), and
+// O = sum_s w_s O_s / sum_s w_s.  The kernel is latency-bound (a few KiB per
+// row, read from L2), so it is laid out for few dependent round trips: every
+// thread first starts asynchronous copies of all its partial rows into shared
+// memory (no registers held), each warp then reduces the row maximum and the
+// weight sum over all splits by itself (shuffles, no block barrier), and the
+// only block-wide step is the final sum across the threads that hold
+// different splits of the same head-dim values.  The first SC splits are
+// staged; any beyond that (very long caches) are read directly.
 constexpr int kCombineThreads = 256;
+constexpr int kCombineStageBytes = 44 * 1024;  // staged partial rows per CTA (with the sums: <= 48 KiB)
+
+template <int D>
+__host__ __device__ constexpr int combine_staged_splits(int S) {
+    return S < kCombineStageBytes / (D * 4) ? S : kCombineStageBytes / (D * 4);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) gqa_combine_kernel(const float *__restrict__ o_part,
                                                                       const float *__restrict__ lse_part,
                                                                       __nv_bfloat16 *out, float *lse, int Sq,
                                                                       int Hq, int Hkv, int G, int Mq, int S) {
-    constexpr int C4 = D / 4;                    // float4 chunks per row
-    constexpr int SL = kCombineThreads / C4;     // split lanes
-    extern __shared__ float sm[];                // [S] weights, then [SL][D] partial sums
-    float *w_s = sm;
-    float4 *red = reinterpret_cast<float4 *>(sm + ((S + 3) & ~3));
-    __shared__ float warp_red[kCombineThreads / 32];
-    __shared__ float bcast[2];
+    constexpr int C4 = D / 4;                 // float4 chunks per row
+    constexpr int SL = kCombineThreads / C4;  // split lanes
+    extern __shared__ float4 cmb_smem[];      // [SC][C4] staged partial rows, then [SL][C4] sums
+    const int SC = combine_staged_splits<D>(S);
+    float4 *stage = cmb_smem;
+    float4 *red = cmb_smem + size_t(SC) * C4;
 
     pdl_wait_primary();
     const int tid = threadIdx.x;
-    const long row = blockIdx.x;                 // (unit * Mq + r)
+    const int lane = tid & 31;
+    const long row = blockIdx.x;  // (unit * Mq + r)
     const int r = int(row % Mq);
     const long unit = row / Mq;
     const int g = int(unit % Hkv);
     const int b = int(unit / Hkv);
     const float *lp = lse_part + size_t(row) * S;
     const float *op = o_part + size_t(row) * S * D;
+    const int c = tid % C4;
+    const int sl = tid / C4;
 
-    // 1. max over splits
+    // 1. this thread's splits s = sl + k SL: copies of the partial rows in flight
+    for (int s = sl; s < SC; s += SL) cp_async16(stage + s * C4 + c, op + size_t(s) * D + c * 4);
+
+    // 2. row maximum and weight sum over all splits, per warp
     float M = -INFINITY;
-    for (int s = tid; s < S; s += kCombineThreads) M = fmaxf(M, lp[s]);
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lp + s));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if ((tid & 31) == 0) warp_red[tid >> 5] = M;
-    __syncthreads();
-    if (tid == 0) {
-        float m = warp_red[0];
-        for (int w = 1; w < kCombineThreads / 32; ++w) m = fmaxf(m, warp_red[w]);
-        bcast[0] = m;
-    }
-    __syncthreads();
-    M = bcast[0];
     const float Mu = (M == -INFINITY) ? 0.f : M;
-
-    // 2. weights and their sum
     float L = 0.f;
-    for (int s = tid; s < S; s += kCombineThreads) {
-        const float l2 = lp[s];
-        const float w = (l2 == -INFINITY) ? 0.f : fast_exp2(l2 - Mu);
-        w_s[s] = w;
-        L += w;
+    for (int s = lane; s < S; s += 32) {
+        const float l2 = __ldg(lp + s);
+        L += (l2 == -INFINITY) ? 0.f : fast_exp2(l2 - Mu);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    __syncthreads();  // w_s complete; warp_red free again
-    if ((tid & 31) == 0) warp_red[tid >> 5] = L;
-    __syncthreads();
-    if (tid == 0) {
-        float l = 0.f;
-        for (int w = 0; w < kCombineThreads / 32; ++w) l += warp_red[w];
-        bcast[1] = l;
-    }
 
     // 3. weighted sum over this thread's splits for its 4 head-dim values
-    const int c = tid % C4;
-    const int sl = tid / C4;
+    cp_async_wait_all();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
     for (int s = sl; s < S; s += SL) {
-        const float w = w_s[s];
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(op + size_t(s) * D) + c);
+        const float l2 = __ldg(lp + s);
+        const float w = (l2 == -INFINITY) ? 0.f : fast_exp2(l2 - Mu);
+        const float4 x = s < SC ? stage[s * C4 + c] : __ldg(reinterpret_cast<const float4 *>(op + size_t(s) * D) + c);
         acc.x += w * x.x;
         acc.y += w * x.y;
         acc.z += w * x.z;
         acc.w += w * x.w;
     }
-    red[sl * C4 + c] = acc;
+    red[tid] = acc;
     __syncthreads();
-    L = bcast[1];
     if (sl != 0) return;
 #pragma unroll
     for (int k = 1; k < SL; ++k) {
