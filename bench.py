@@ -358,7 +358,9 @@ def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
                   f"(the rows of whole KV-head groups), {reps} pass(es)")
     elif isinstance(cfg, gqa_inputs.PagedKVConfig):
         cpu = {n: (t.cpu() if hasattr(t, "cpu") else t) for n, t in tensors.items()}
-        return _paged_kv_oracle_timing(orc, cfg, cpu, max_seconds, min_seconds)
+        res = _paged_kv_oracle_timing(orc, cfg, cpu, max_seconds, min_seconds)
+        return dict(res, nproc=os.cpu_count(), cpu_model=cpu_model(),
+                    single_thread=_single_thread_baseline(orc, cfg, cpu))
     else:
         cpu = {n: (t.cpu() if hasattr(t, "cpu") else t) for n, t in tensors.items()}
         nrows = cfg.B * cfg.Hq
@@ -377,10 +379,12 @@ def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
             reps += 1
         sample = f"{'all' if rows is None else len(rows)} of {nrows} (request, head) rows, {reps} pass(es)"
     per_pass = elapsed / reps
+    cpu = {"q": q, "k": k, "v": v} if isinstance(cfg, gqa_inputs.DenseConfig) else cpu
     # KV bytes in proportion to the rows covered (every row reads its group's K/V)
     return {"value": gbs(workload_kv_bytes(cfg) * frac, per_pass * 1e3), "unit": "GB/s",
             "cores": orc.num_threads(), "kind": "oracle", "sample": sample,
-            "us_per_call_equiv": per_pass / frac * 1e6}
+            "us_per_call_equiv": per_pass / frac * 1e6, "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+            "single_thread": _single_thread_baseline(orc, cfg, cpu)}
 
 
 def dense_oracle(orc, cfg, q, k, v, rows=None):
@@ -388,6 +392,64 @@ def dense_oracle(orc, cfg, q, k, v, rows=None):
     if cfg.dv == cfg.D:
         return orc.gqa_decode(q, k, v, cfg.scale, rows=rows)
     return orc.gqa_decode_dv(q, k, v, cfg.scale, rows=rows)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def _single_thread_baseline(orc, cfg, cpu, seconds=1.5) -> dict:
+    """The oracle on one host thread over the first rows of the workload,
+    repeated for about `seconds`; bytes credited as in the multi-thread leg."""
+    threads = orc.num_threads()
+    orc.set_num_threads(1)
+    try:
+        if isinstance(cfg, gqa_inputs.DenseConfig):
+            nrows = cfg.B * cfg.Hq * cfg.Sq
+            rows = list(range(min(nrows, 4)))
+            run = lambda: dense_oracle(orc, cfg, cpu["q"], cpu["k"], cpu["v"], rows=rows)  # noqa: E731
+            credit = workload_kv_bytes(cfg) * len(rows) / nrows
+        elif isinstance(cfg, gqa_inputs.PagedKVConfig):
+            lens = [int(x) for x in cpu["seq_lens"]]
+            elem = 2 if cfg.kv_dtype == "bf16" else 1
+            G = cfg.Hq // cfg.Hkv
+            rows = [0, 1]
+            run = lambda: orc.gqa_decode_paged(cpu["q"], cpu["k_pool"], cpu["v_pool"], cpu["page_table"],  # noqa: E731
+                                               cpu["seq_lens"], cfg.scale, cpu["k_scale"], cpu["v_scale"], rows=rows)
+            credit = sum(2 * lens[r // (cfg.Hq * cfg.Sq)] * cfg.D * elem / (G * cfg.Sq) for r in rows)
+        else:
+            nrows = cfg.B * cfg.Hq
+            rows = list(range(16))
+            run = lambda: orc.gqa_decode_paged_fp8(cpu["q"], cpu["gate"], cpu["k_pool"], cpu["v_pool"],  # noqa: E731
+                                                   cpu["page_table"], cpu["topk"], cpu["k_scale"], cpu["v_scale"],
+                                                   cfg.scale, rows=rows)
+            credit = workload_kv_bytes(cfg) * len(rows) / nrows
+        reps, elapsed = 0, 0.0
+        while elapsed < seconds and reps < 1000:
+            t0 = time.perf_counter()
+            run()
+            elapsed += time.perf_counter() - t0
+            reps += 1
+    finally:
+        orc.set_num_threads(threads)
+    return {"value": gbs(credit, elapsed / reps * 1e3), "unit": "GB/s", "cores": 1,
+            "sample": f"{len(rows)} query rows, {reps} pass(es)"}
 
 
 def _paged_kv_oracle_timing(orc, cfg, cpu, max_seconds, min_seconds) -> dict:
@@ -635,6 +697,7 @@ def run_reference(args) -> int:
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), CPU)",
             "config": workload_config(cfg), "impl": "reference",
             "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                             "nproc": os.cpu_count(), "cpu_model": cpu_model(),
                              "sample": probe["sample"] + " per step"},
             "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
@@ -670,6 +733,7 @@ def run_reference(args) -> int:
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), CPU)",
         "config": workload_config(cfg), "impl": "reference",
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                             "nproc": os.cpu_count(), "cpu_model": cpu_model(),
                          "sample": sample},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -120,6 +120,8 @@ class Oracle:
         lib.oracle_kv_head.restype = ctypes.c_int
         lib.oracle_kv_head.argtypes = [ctypes.c_int] * 3
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.restype = None
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
         lib.oracle_gqa_decode.restype = None
         lib.oracle_gqa_decode.argtypes = [
             _u16_p, _u16_p, _u16_p,
@@ -152,6 +154,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return self._lib.oracle_num_threads()
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads of later calls (timing only; results are identical)."""
+        self._lib.oracle_set_num_threads(int(n))
 
     # -- dense ---------------------------------------------------------
     def gqa_decode(self, q, k, v, scale: float, rows=None):

@@ -121,6 +121,18 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Sets the number of threads later calls use (timing only; results do not
+ * depend on it: rows are independent and each is computed by one thread). */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ */
 /* dense grouped-query decode attention                                 */
 /* ------------------------------------------------------------------ */

@@ -111,3 +111,16 @@ def test_reference_arm_json(capsys):
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["steps"] == 3
     assert line["metric"] == bench.METRIC
+
+
+def test_cpu_model_and_single_thread_baseline(orc):
+    """The CPU baseline names the host CPU and times the oracle on one thread
+    (restoring the thread count afterwards)."""
+    import gqa_inputs
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+    cfg = gqa_inputs.CONFIGS["dense_b1_h8x1_d64_sq1_kv1k"]
+    q, k, v = gqa_inputs.dense_config_inputs(cfg)
+    threads = orc.num_threads()
+    r = bench._single_thread_baseline(orc, cfg, {"q": q, "k": k, "v": v}, seconds=0.05)
+    assert r["cores"] == 1 and r["value"] > 0 and r["unit"] == "GB/s"
+    assert orc.num_threads() == threads
