@@ -1,6 +1,6 @@
 """fp64 CPU oracle for grouped-query decode attention -- TEST INFRASTRUCTURE.
 
-This package is the checker, not the product.  Only the test suite, the
+This package checks the product and is not part of it.  Only the test suite, the
 package's ``smoke()`` check and the benchmark's CPU-baseline leg may import
 it; the CUDA library never does, and the two share no code.  The arithmetic
 lives in ``gqa_oracle.c`` (plain C, double precision, OpenMP over rows); this
