@@ -36,7 +36,7 @@ EXPORTS = [
     "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_dv", "gqa_decode_dv_num_splits",
     "gqa_decode_dv_workspace_bytes",
     "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
-    "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged", "gqa_decode_paged_ex",
+    "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged_fp8_dev_scales", "gqa_decode_paged", "gqa_decode_paged_ex",
     "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes", "gqa_decode_paged_dev_scales",
     "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
     "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events",
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.gqa_decode_paged_fp8.restype = st
     lib.gqa_decode_paged_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f, f, vp, vp] + [i] * 8 + [f, vp]
+    lib.gqa_decode_paged_fp8_dev_scales.restype = st
+    lib.gqa_decode_paged_fp8_dev_scales.argtypes = [vp] * 8 + [i, vp, vp] + [i] * 8 + [f, vp]
     lib.gqa_decode_paged.restype = st
     lib.gqa_decode_paged.argtypes = [vp, vp, vp, i, f, f, vp, vp, vp, vp] + [i] * 8 + [f, vp]
     lib.gqa_decode_paged_ex.restype = st
@@ -258,12 +260,14 @@ def gqa_decode_host(q, k, v, out, lse=None, scale=None, stream=None):
 # ---------------------------------------------------------------------------
 # sparse paged FP8
 # ---------------------------------------------------------------------------
-def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale, v_scale, out=None,
-                         lse=None, scale=None, stream=None, with_lse=True):
+def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale=1.0, v_scale=1.0, out=None,
+                         lse=None, scale=None, stream=None, with_lse=True, k_scales=None, v_scales=None):
     """Sparse paged decode over an FP8 E4M3FN pool with a sigmoid gate.
 
     q, gate [B,Hq,D] bf16; pools uint8 [num_pages, page_size, Hkv, D];
     page_table int32 [B, pages_per_req]; topk_idx int32 [B, topk].
+    k_scales / v_scales: optional CUDA fp32 tensors of 1 or Hkv device-side
+    scales (replace k_scale / v_scale).
     Returns (out [B,Hq,D] bf16, lse [B,Hq] fp32 or None).
     """
     lib = load_library()
@@ -279,6 +283,16 @@ def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale,
         out = torch.empty_like(q)
     if lse is None and with_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if k_scales is not None or v_scales is not None:
+        _need(k_scales, "k_scales", torch.float32, "cuda")
+        _need(v_scales, "v_scales", torch.float32, "cuda")
+        st = lib.gqa_decode_paged_fp8_dev_scales(_ptr(q), _ptr(gate), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
+                                                 _ptr(topk_idx), _ptr(k_scales), _ptr(v_scales), k_scales.numel(),
+                                                 _ptr(out), _ptr(lse), B, Hq, Hkv, D, page_size,
+                                                 page_table.shape[1], num_pages, topk_idx.shape[1],
+                                                 _scale_arg(scale), _stream(stream))
+        _check(st, "gqa_decode_paged_fp8_dev_scales")
+        return out, lse
     st = lib.gqa_decode_paged_fp8(_ptr(q), _ptr(gate), _ptr(k_pool), _ptr(v_pool), _ptr(page_table),
                                   _ptr(topk_idx), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
                                   B, Hq, Hkv, D, page_size, page_table.shape[1], num_pages,

@@ -586,14 +586,27 @@ gqa_status gqa_decode_host(const void *q_host, const void *k_host, const void *v
     return result;
 }
 
-gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *k_pool, const uint8_t *v_pool,
-                                const int32_t *page_table, const int32_t *topk_idx, float k_scale, float v_scale,
-                                void *out, float *lse, int B, int Hq, int Hkv, int D, int page_size,
-                                int pages_per_req, int num_pages, int topk, float scale, gqa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The sparse top-K form: host scalars k_scale / v_scale, or (k_scales,
+// v_scales, n_scales) in device memory (n_scales 1 or Hkv), which multiply
+// the host scalars.
+gqa_status run_paged_topk(const void *q, const void *gate, const uint8_t *k_pool, const uint8_t *v_pool,
+                          const int32_t *page_table, const int32_t *topk_idx, float k_scale, float v_scale,
+                          const float *k_scales, const float *v_scales, int n_scales, void *out, float *lse, int B,
+                          int Hq, int Hkv, int D, int page_size, int pages_per_req, int num_pages, int topk,
+                          float scale, gqa_stream_t stream) {
     gqa_status st = check_paged(B, Hq, Hkv, D, page_size, pages_per_req, num_pages, topk);
     if (st != GQA_OK) return st;
     if (D == 256 || Hq / Hkv > 16) return GQA_ERR_UNSUPPORTED;
     if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return GQA_ERR_INVALID_ARG;
+    if (k_scales != nullptr || v_scales != nullptr) {
+        if (k_scales == nullptr || v_scales == nullptr || (n_scales != 1 && n_scales != Hkv))
+            return GQA_ERR_INVALID_ARG;
+        if (!aligned(k_scales, 4) || !aligned(v_scales, 4)) return GQA_ERR_ALIGNMENT;
+    }
     if (q == nullptr || gate == nullptr || k_pool == nullptr || v_pool == nullptr || out == nullptr ||
         page_table == nullptr || (topk > 0 && topk_idx == nullptr))
         return GQA_ERR_INVALID_ARG;
@@ -622,6 +635,9 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
     a.Mq = a.G;
     a.alpha = resolve_scale(scale, D) * k_scale * 1.4426950408889634f;
     a.v_scale = v_scale;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
+    a.n_scales = k_scales != nullptr ? n_scales : 0;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.fault_mode = g_fault_mode.load();
     int dev = 0;
@@ -671,6 +687,29 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *
         return GQA_ERR_CUDA;
     }
     return GQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status gqa_decode_paged_fp8(const void *q, const void *gate, const uint8_t *k_pool, const uint8_t *v_pool,
+                                const int32_t *page_table, const int32_t *topk_idx, float k_scale, float v_scale,
+                                void *out, float *lse, int B, int Hq, int Hkv, int D, int page_size,
+                                int pages_per_req, int num_pages, int topk, float scale, gqa_stream_t stream) {
+    return run_paged_topk(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale, v_scale, nullptr, nullptr, 0, out,
+                          lse, B, Hq, Hkv, D, page_size, pages_per_req, num_pages, topk, scale, stream);
+}
+
+gqa_status gqa_decode_paged_fp8_dev_scales(const void *q, const void *gate, const uint8_t *k_pool,
+                                           const uint8_t *v_pool, const int32_t *page_table,
+                                           const int32_t *topk_idx, const float *k_scales, const float *v_scales,
+                                           int n_scales, void *out, float *lse, int B, int Hq, int Hkv, int D,
+                                           int page_size, int pages_per_req, int num_pages, int topk, float scale,
+                                           gqa_stream_t stream) {
+    if (k_scales == nullptr || v_scales == nullptr) return GQA_ERR_INVALID_ARG;
+    return run_paged_topk(q, gate, k_pool, v_pool, page_table, topk_idx, 1.0f, 1.0f, k_scales, v_scales, n_scales,
+                          out, lse, B, Hq, Hkv, D, page_size, pages_per_req, num_pages, topk, scale, stream);
 }
 
 namespace {

@@ -222,6 +222,22 @@ gqa_status gqa_decode_paged_fp8(const void *q, const void *gate,
                                 int B, int Hq, int Hkv, int D, int page_size, int pages_per_req,
                                 int num_pages, int topk, float scale, gqa_stream_t stream);
 
+/* gqa_decode_paged_fp8 with the dequantisation scales in device memory:
+ * k_scales and v_scales each point to n_scales fp32 values, n_scales = 1 (per
+ * tensor) or Hkv (per KV head: KV head g uses [g]).  The kernel reads them
+ * when it starts, so earlier work in the stream may write them.
+ * GQA_ERR_INVALID_ARG for null scale pointers or another n_scales;
+ * GQA_ERR_ALIGNMENT unless 4-byte aligned.  Everything else as
+ * gqa_decode_paged_fp8. */
+gqa_status gqa_decode_paged_fp8_dev_scales(const void *q, const void *gate,
+                                           const uint8_t *k_pool, const uint8_t *v_pool,
+                                           const int32_t *page_table, const int32_t *topk_idx,
+                                           const float *k_scales, const float *v_scales, int n_scales,
+                                           void *out, float *lse,
+                                           int B, int Hq, int Hkv, int D, int page_size,
+                                           int pages_per_req, int num_pages, int topk, float scale,
+                                           gqa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Paged decode over whole requests (no top-K selection), bf16 or FP8 pools.
  *

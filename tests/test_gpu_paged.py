@@ -167,3 +167,37 @@ def test_full_workload_sampled_rows(gq, orc):
     assert_o_close(got_o, ref_o, "paged full")
     assert_lse_close(got_l, ref_l, "paged full")
     print(diagnostics(got_o, ref_o))
+
+
+def test_topk_device_scales_per_head_and_per_tensor(gq, orc):
+    """Top-K form with scales in device memory: per KV head against the oracle
+    run once per KV head with that head's scales (rows are independent), and
+    per tensor equal to the host scalars within rounding of the multiplier."""
+    B, Hq, Hkv, D = 6, 32, 8, 128
+    inp = gqa_inputs.paged_inputs(B=B, Hq=Hq, Hkv=Hkv, D=D, page_size=16, pages_per_req=8, num_pages=B * 8 + 5,
+                                  topk=100, seed=4242, pad_tail=3)
+    ks = torch.tensor([inp["k_scale"] * (0.5 + 0.125 * e) for e in range(Hkv)], dtype=torch.float32)
+    vs = torch.tensor([inp["v_scale"] * (1.5 - 0.0625 * e) for e in range(Hkv)], dtype=torch.float32)
+    d = _cuda(inp)
+    out, lse = gq.gqa_decode_paged_fp8(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["page_table"], d["topk"],
+                                       k_scales=ks.cuda(), v_scales=vs.cuda())
+    torch.cuda.synchronize()
+    assert gq.gqa_device_status() == 0
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D)
+    for g in range(Hkv):
+        rows = [b * Hq + h for b in range(B) for h in range(g * G, (g + 1) * G)]
+        ref_o, ref_l, _ = orc.gqa_decode_paged_fp8(inp["q"], inp["gate"], inp["k_pool"], inp["v_pool"],
+                                                   inp["page_table"], inp["topk"], float(ks[g]), float(vs[g]),
+                                                   scale, rows=rows)
+        got_o = out.cpu().view(B * Hq, D)[rows]
+        got_l = lse.cpu().view(B * Hq)[rows]
+        assert_o_close(got_o, ref_o, f"per-head device scales, KV head {g}")
+        assert_lse_close(got_l, ref_l, f"per-head device scales, KV head {g}")
+    o1, l1 = gq.gqa_decode_paged_fp8(d["q"], d["gate"], d["k_pool"], d["v_pool"], d["page_table"], d["topk"],
+                                     k_scales=torch.tensor([inp["k_scale"]], device="cuda"),
+                                     v_scales=torch.tensor([inp["v_scale"]], device="cuda"))
+    o2, l2 = _paged_run(gq, inp)
+    torch.cuda.synchronize()
+    assert torch.allclose(o1.cpu().float(), o2.float(), atol=1e-3, rtol=1e-2)
+    assert torch.allclose(l1.cpu(), l2, atol=1e-5, rtol=0)

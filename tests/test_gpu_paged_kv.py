@@ -238,3 +238,24 @@ def test_full_workload_sampled_rows(gq, orc, name):
     got_l = torch.stack([lg[r // nrow, (r // cfg.Sq) % cfg.Hq, r % cfg.Sq] for r in rows])
     assert_o_close(got_o, ref_o, name)
     assert_lse_close(got_l, ref_l, name)
+
+
+@pytest.mark.parametrize("kv", ["int8", "fp8", "bf16"])
+def test_contiguous_cache_as_one_page_per_request(gq, orc, kv):
+    """A contiguous (unpaged) 8-bit or bf16 cache is the paged form with one
+    page of the whole capacity per request.  Against the oracle, and bit for bit
+    equal to the same bytes addressed as pages of 16 tokens: the kernel's
+    arithmetic follows 16-token steps, never the page size."""
+    B, Sq, Hq, Hkv, D, cap = 2, 2, 64, 8, 128, 2048
+    inp = gqa_inputs.paged_kv_inputs(B, Sq, Hq, Hkv, D, cap, 1, B, seed=80, kv_dtype=kv, seq_lens=[cap, 1500])
+    out1, lse1 = _run(gq, inp, num_splits=7)
+    ref_o, ref_l = _ref(orc, inp, 1.0 / math.sqrt(D))
+    _check(out1, lse1, ref_o, ref_l, f"contiguous {kv}")
+    per = cap // 16
+    inp16 = dict(inp)
+    inp16["k_pool"] = inp["k_pool"].reshape(B * per, 16, Hkv, D).contiguous()
+    inp16["v_pool"] = inp["v_pool"].reshape(B * per, 16, Hkv, D).contiguous()
+    inp16["page_table"] = (inp["page_table"].long() * per + torch.arange(per)).to(torch.int32).contiguous()
+    out16, lse16 = _run(gq, inp16, num_splits=7)
+    assert torch.equal(out1, out16) and torch.equal(lse1, lse16)
+    assert gq.gqa_device_status() == 0
