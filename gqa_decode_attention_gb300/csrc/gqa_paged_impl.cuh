@@ -68,10 +68,10 @@ static long paged_dispatch_nt(const PagedArgs &a, cudaStream_t stream, int op) {
 // Merge of the shared requests' partials (whole-request form, several workers).
 template <int D>
 static cudaError_t launch_paged_combine(const PagedArgs &a, int hb, cudaStream_t stream) {
-    const long rows = long(a.B) * a.Hkv * a.Mq;
+    // CTA (b, y): rows 8 y .. 8 y + 7 of request b
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned((rows + 3) / 4));
-    cfg.blockDim = dim3(128);
+    cfg.gridDim = dim3(unsigned(a.B), unsigned((a.Hkv * a.Mq + kPagedMergeRows - 1) / kPagedMergeRows));
+    cfg.blockDim = dim3(32 * kPagedMergeRows);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -763,83 +763,114 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
 
 
 // Merge of the partials of requests shared by several workers of the
-// balanced whole-request form.  One warp per output row (b, h, i): the warp
-// recomputes the schedule (T, the request's first step and step count, the
-// workers w_first .. w_last holding its steps), returns when the request lies
-// within one worker (that worker wrote the final output), and otherwise
-// merges the workers' partials with weights 2^(lse_w - max) (a partial that
-// saw no visible token has lse = -inf and weight 0).
+// balanced schedule.  CTA (b, y) merges rows rr = 8 y + warp of request b
+// (rr = g * Mq + r), one warp per row.  Thread 0 works out once per CTA which
+// workers hold the request's steps (w_first .. w_last; the request's first step
+// P_b and step count come from the closed form of the top-K form or from the
+// prefix the main kernel recorded); the CTA returns when one worker holds them
+// all (that worker wrote the final output).  The threads stage the workers'
+// first steps in shared memory, and each warp loads the partials of up to 8
+// workers at a time (one round trip for all of them) before merging them in
+// worker order with weights 2^(lse_w - max) (a partial that saw no visible
+// token has lse = -inf and weight 0).
+constexpr int kPagedMergeRows = 8;       // rows (warps) per CTA
+constexpr int kPagedMergeStaged = 1024;  // worker boundaries kept in shared memory
+constexpr int kPagedMergeBatch = 8;      // workers' partials in flight per warp
+
 template <int D>
-__global__ void __launch_bounds__(128) gqa_paged_combine_kernel(const PagedArgs a, int HB) {
+__global__ void __launch_bounds__(32 * kPagedMergeRows) gqa_paged_combine_kernel(const PagedArgs a, int HB) {
+    __shared__ long wb[kPagedMergeStaged + 1];  // first global step of workers w_first + j
+    __shared__ long info[4];                     // w_first, w_last, P_b, T
     pdl_wait_primary();
+    const int b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const unsigned row = blockIdx.x * 4u + unsigned(warp);  // (b * Hkv + g) * Mq + r  (< 2^31)
-    if (row >= unsigned(a.B) * unsigned(a.Hkv) * unsigned(a.Mq)) return;
-    const unsigned unit = row / unsigned(a.Mq);
-    const int r = int(row - unit * unsigned(a.Mq));
-    const int b = int(unit / unsigned(a.Hkv));
-    const int g = int(unit - unsigned(b) * unsigned(a.Hkv));
-    long T, Pb, steps_b;
-    if (a.seq_lens == nullptr) {  // top-K form: every list has topk_n entries
-        const long steps = (a.topk_n + kPagedStageTokens - 1) / kPagedStageTokens;
-        T = steps * a.B;
-        Pb = steps * b;
-        steps_b = steps;
-    } else {  // whole-request form: the main kernel recorded every request's first step
-        Pb = a.step_prefix[b];
-        steps_b = a.step_prefix[b + 1] - Pb;
-        T = a.step_prefix[a.B];
-    }
-    if (steps_b == 0) return;  // written by the worker that walked it
     const long W = a.num_splits;
-    // floor(x / y) for the schedule's products; 32-bit when they fit (the
-    // common case: 64-bit division is a long instruction sequence)
+    if (threadIdx.x == 0) {
+        long T, Pb, steps_b;
+        if (a.seq_lens == nullptr) {  // top-K form: every list has topk_n entries
+            const long steps = (a.topk_n + kPagedStageTokens - 1) / kPagedStageTokens;
+            T = steps * a.B;
+            Pb = steps * b;
+            steps_b = steps;
+        } else {  // whole-request form: the main kernel recorded every request's first step
+            Pb = a.step_prefix[b];
+            steps_b = a.step_prefix[b + 1] - Pb;
+            T = a.step_prefix[a.B];
+        }
+        // worker holding global step s: the largest w with floor(w T / W) <= s
+        info[0] = steps_b > 0 ? ((Pb + 1) * W - 1) / T : -1;
+        info[1] = steps_b > 0 ? ((Pb + steps_b) * W - 1) / T : -1;
+        info[2] = Pb;
+        info[3] = T;
+    }
+    __syncthreads();
+    const long w_first = info[0], w_last = info[1], Pb = info[2], T = info[3];
+    if (w_first == w_last) return;  // one worker (or an empty request): written by the main kernel
+    // floor(x / y) for the schedule's products; 32-bit when they fit
     const bool narrow = (unsigned long long)(T + 1) * (unsigned long long)(W + 1) < (1ull << 32);
     auto qdiv = [narrow](long x, long y) -> long {
         return narrow ? long(unsigned(x) / unsigned(y)) : x / y;
     };
-    // worker holding global step s: the largest w with floor(w T / W) <= s
-    const long w_first = qdiv((Pb + 1) * W - 1, T);
-    const long w_last = qdiv((Pb + steps_b) * W - 1, T);
-    if (w_first == w_last) return;
-    const int hb = g / HB, lh = g % HB;
+    const long nw = w_last - w_first + 1;
+    for (long j = threadIdx.x; j <= nw && j <= kPagedMergeStaged; j += 32 * kPagedMergeRows)
+        wb[j] = qdiv((w_first + j) * T, W);
+    __syncthreads();
+    auto wstart = [&](long w) -> long {
+        const long j = w - w_first;
+        return j <= kPagedMergeStaged ? wb[j] : qdiv(w * T, W);
+    };
+
+    const int rr = blockIdx.y * kPagedMergeRows + warp;
+    if (rr >= a.Hkv * a.Mq) return;
+    const int g = rr / a.Mq, r = rr - g * a.Mq;
+    const int hb = g / HB, lh = g - hb * HB;
     constexpr int V = D / 32;  // values per lane
     float m = -INFINITY, L = 0.f;
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    long w_start = qdiv(w_first * T, W);
-    for (long w = w_first; w <= w_last; ++w) {
-        const long w_next = qdiv((w + 1) * T, W);
-        const bool empty_range = w_start == w_next;  // a worker with no steps holds nothing
-        const int slot = (w == w_first && w_start < Pb) ? 1 : 0;
-        w_start = w_next;
-        if (empty_range) continue;
-        const size_t prow = ((((size_t(hb) * W + w) * 2 + slot) * HB + lh) * a.Mq) + r;
-        const float l2 = __ldg(a.lse_part + prow);
-        float x[V];
-        if constexpr (V == 4) {
-            const float4 x4 = __ldg(reinterpret_cast<const float4 *>(a.o_part + prow * D) + lane);
-            x[0] = x4.x;
-            x[1] = x4.y;
-            x[2] = x4.z;
-            x[3] = x4.w;
-        } else {
-            const float2 x2 = __ldg(reinterpret_cast<const float2 *>(a.o_part + prow * D) + lane);
-            x[0] = x2.x;
-            x[1] = x2.y;
-        }
-        if (l2 == -INFINITY) continue;
-        const float mn = fmaxf(m, l2);
-        const float sc = fast_exp2(m - mn), wgt = fast_exp2(l2 - mn);
+    for (long w0 = w_first; w0 <= w_last; w0 += kPagedMergeBatch) {
+        float l2[kPagedMergeBatch];
+        float x[kPagedMergeBatch][V];
+        bool ok[kPagedMergeBatch];
 #pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = acc[v] * sc + wgt * x[v];
-        L = L * sc + wgt;
-        m = mn;
+        for (int k = 0; k < kPagedMergeBatch; ++k) {
+            const long w = w0 + k;
+            ok[k] = false;
+            l2[k] = -INFINITY;
+            if (w > w_last) continue;
+            const long ws = wstart(w);
+            if (ws == wstart(w + 1)) continue;  // a worker with no steps holds nothing
+            ok[k] = true;
+            const int slot = (w == w_first && ws < Pb) ? 1 : 0;
+            const size_t prow = ((((size_t(hb) * W + w) * 2 + slot) * HB + lh) * a.Mq) + r;
+            l2[k] = __ldg(a.lse_part + prow);
+            if constexpr (V == 4) {
+                const float4 x4 = __ldg(reinterpret_cast<const float4 *>(a.o_part + prow * D) + lane);
+                x[k][0] = x4.x;
+                x[k][1] = x4.y;
+                x[k][2] = x4.z;
+                x[k][3] = x4.w;
+            } else {
+                const float2 x2 = __ldg(reinterpret_cast<const float2 *>(a.o_part + prow * D) + lane);
+                x[k][0] = x2.x;
+                x[k][1] = x2.y;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kPagedMergeBatch; ++k) {
+            if (!ok[k] || l2[k] == -INFINITY) continue;
+            const float mn = fmaxf(m, l2[k]);
+            const float sc = fast_exp2(m - mn), wgt = fast_exp2(l2[k] - mn);
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = acc[v] * sc + wgt * x[k][v];
+            L = L * sc + wgt;
+            m = mn;
+        }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int i = r / a.G;
-    const int h = g * a.G + r % a.G;
+    const int h = g * a.G + (r - i * a.G);
     const size_t off = ((size_t(b) * a.Sq + i) * a.Hq + h) * D + lane * V;
 #pragma unroll
     for (int v = 0; v < V; v += 2) {
