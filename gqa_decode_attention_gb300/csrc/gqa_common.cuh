@@ -117,6 +117,11 @@ __device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void *src, ui
                  : "memory");
 }
 
+// Brings the 128-byte line holding `p` (global memory) into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }

@@ -329,6 +329,24 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
     const bool complete = seg_t == seg_p && seg_next == seg_p + steps_b;
     const int slot = seg_t == w_begin ? 0 : 1;
 
+    // The producer is idle while the consumers load Q: it warms L2 with the
+    // index tables the segment's first index-map pass reads (the top-K list
+    // and the request's page-table row, or the page-table entries of the
+    // pass's tokens), so that pass costs L2 rather than DRAM latencies.
+    if (producer) {
+        const int cn0 = min(kPagedChunk, n_tok);
+        const int32_t *pt_row = a.page_table + size_t(b) * a.pages_per_req;
+        if constexpr (RANGE) {
+            const int p0 = t_begin / a.page_size;
+            const int p1 = cn0 > 0 ? (t_begin + cn0 - 1) / a.page_size : p0 - 1;
+            for (int p = p0 + 32 * lane; p <= p1; p += 32 * 32) prefetch_l2(pt_row + p);
+        } else {
+            const int32_t *tk_row = a.topk + size_t(b) * a.topk_n + t_begin;
+            for (int k = 32 * lane; k < cn0; k += 32 * 32) prefetch_l2(tk_row + k);
+            for (int p = 32 * lane; p < a.pages_per_req && p < 32 * 32 * 8; p += 32 * 32) prefetch_l2(pt_row + p);
+        }
+    }
+
     // ---- Q^T fragments.  Lane gi holds query row gi (+8 per n-tile) at the
     // elements k_dbase(kk, c) .. +3.  FP8 pools: f16 with a per-row
     // power-of-two scale; bf16 pools: the bf16 values as they are.
@@ -494,6 +512,16 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 const uint8_t *kst = psmem + st * C::STAGE_BYTES;
                 const uint8_t *vst = kst + C::T * C::KRS;
                 const uint32_t mask = vmask[st];
+                if constexpr (!RANGE) {  // top-K form: the gate rows are read by the epilogue
+                    if (a.gate != nullptr && complete && base_k + (s + 1) * C::T >= n_tok && lane < 2 * NT * 8) {
+                        // last step of the request: bring this warp's gate rows into L2 for the epilogue
+                        const int r = lane >> 1;
+                        if (r < a.Mq) {
+                            const int hr = g * a.G + r % a.G;
+                            prefetch_l2(a.gate + ((size_t(b) * a.Sq + r / a.G) * a.Hq + hr) * D + (lane & 1) * (D / 2));
+                        }
+                    }
+                }
 
                 // token validity of the two tokens this lane holds in S^T (gi, gi + 8)
                 const bool tv0 = (mask >> gi) & 1u, tv1 = (mask >> (gi + 8)) & 1u;
