@@ -329,23 +329,31 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
     const bool complete = seg_t == seg_p && seg_next == seg_p + steps_b;
     const int slot = seg_t == w_begin ? 0 : 1;
 
-    // The producer is idle while the consumers load Q: it warms L2 with the
-    // index tables the segment's first index-map pass reads (the top-K list
-    // and the request's page-table row, or the page-table entries of the
-    // pass's tokens), so that pass costs L2 rather than DRAM latencies.
-    if (producer) {
-        const int cn0 = min(kPagedChunk, n_tok);
-        const int32_t *pt_row = a.page_table + size_t(b) * a.pages_per_req;
-        if constexpr (RANGE) {
-            const int p0 = t_begin / a.page_size;
-            const int p1 = cn0 > 0 ? (t_begin + cn0 - 1) / a.page_size : p0 - 1;
-            for (int p = p0 + 32 * lane; p <= p1; p += 32 * 32) prefetch_l2(pt_row + p);
-        } else {
-            const int32_t *tk_row = a.topk + size_t(b) * a.topk_n + t_begin;
-            for (int k = 32 * lane; k < cn0; k += 32 * 32) prefetch_l2(tk_row + k);
-            for (int p = 32 * lane; p < a.pages_per_req && p < 32 * 32 * 8; p += 32 * 32) prefetch_l2(pt_row + p);
+    // Index map of tokens [base_k, base_k + cn) of the segment into rows_s,
+    // batched so each thread has all its top-K loads and then all its
+    // page-table loads in flight together.
+    auto index_pass = [&](int base_k, int cn) {
+        int tk[C::IPT];
+#pragma unroll
+        for (int u = 0; u < C::IPT; ++u) {
+            const int k = threadIdx.x + u * C::THREADS;
+            if constexpr (RANGE)
+                tk[u] = k < cn ? t_begin + base_k + k : -1;
+            else
+                tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + t_begin + base_k + k) : -1;
         }
-    }
+#pragma unroll
+        for (int u = 0; u < C::IPT; ++u) {
+            const int k = threadIdx.x + u * C::THREADS;
+            const int row = paged_token_row(a.page_table, b, a.pages_per_req, a.page_size, a.num_pages, tk[u], &bad);
+            if (k < cn) rows_s[k] = row;
+        }
+    };
+    // The segment's first pass runs before the consumers load Q (the previous
+    // segment's closing barrier left rows_s free), so the producer starts its
+    // copies while Q is still in flight.
+    if (n_tok > 0) index_pass(0, min(kPagedChunk, n_tok));
+    __syncthreads();
 
     // ---- Q^T fragments.  Lane gi holds query row gi (+8 per n-tile) at the
     // elements k_dbase(kk, c) .. +3.  FP8 pools: f16 with a per-row
@@ -446,26 +454,12 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
 
     for (int base_k = 0; base_k < n_tok; base_k += kPagedChunk) {
         const int cn = min(kPagedChunk, n_tok - base_k);
-        __syncthreads();  // previous pass fully consumed
-        if (*abort_flag) break;
-        // Index map, batched so each thread has all its top-K loads and then
-        // all its page-table loads in flight together.
-        int tk[C::IPT];
-#pragma unroll
-        for (int u = 0; u < C::IPT; ++u) {
-            const int k = threadIdx.x + u * C::THREADS;
-            if constexpr (RANGE)
-                tk[u] = k < cn ? t_begin + base_k + k : -1;
-            else
-                tk[u] = k < cn ? __ldg(a.topk + size_t(b) * a.topk_n + t_begin + base_k + k) : -1;
+        if (base_k > 0) {  // the first pass was mapped before Q was loaded
+            __syncthreads();  // previous pass fully consumed
+            if (*abort_flag) break;
+            index_pass(base_k, cn);
+            __syncthreads();
         }
-#pragma unroll
-        for (int u = 0; u < C::IPT; ++u) {
-            const int k = threadIdx.x + u * C::THREADS;
-            const int row = paged_token_row(a.page_table, b, a.pages_per_req, a.page_size, a.num_pages, tk[u], &bad);
-            if (k < cn) rows_s[k] = row;
-        }
-        __syncthreads();
         const int steps = (cn + C::T - 1) / C::T;
 
         if (producer) {
