@@ -226,7 +226,16 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv", "-lms", "200"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            # The sampler's start-up (its first query of the device) disturbs a
+            # step that overlaps it: let it write its first sample before the
+            # timed region begins.
+            deadline = time.monotonic() + 5.0
+            while time.monotonic() < deadline and self.proc.poll() is None:
+                with open(self.path) as f:
+                    if len(f.read().splitlines()) >= 2:
+                        break
+                time.sleep(0.05)
+            time.sleep(0.1)
         except OSError:
             self.proc = None
         return self
@@ -544,13 +553,18 @@ def run_gqa(args) -> int:
     if gq.gqa_device_status() != 0:
         raise RuntimeError("device error during warm-up")
 
-    # ---- timed region: exactly K steps
-    _barrier()
-    torch.cuda.synchronize()
+    # ---- timed region: exactly K steps.  The clock sampler starts first (the
+    # GPU idles while it comes up), then two more untimed steps bring the
+    # clocks back before the barrier + synchronize that open the region.
     with ClockSampler(local) as clk:
+        for _ in range(2):
+            flush_l2()
+            call()
+        _barrier()
+        torch.cuda.synchronize()
         step_ms, _ = step_events(args.steps)
-    torch.cuda.synchronize()
-    _barrier()
+        torch.cuda.synchronize()
+        _barrier()
     clocks = clk.summary()
     total_ms = sum(step_ms)
     (max_total_ms,) = reduce_over_ranks([total_ms], "max")
