@@ -2,7 +2,8 @@
 //
 // Thin inline-PTX wrappers for the pieces the kernels are built from:
 // mbarrier pipelines with bounded waits, TMA tile loads
-// (cp.async.bulk.tensor), ldmatrix, bf16 tensor-core MMA, base-2
+// (cp.async.bulk.tensor) and bulk copies (cp.async.bulk), 16-byte cp.async
+// copies, L2 prefetches, ldmatrix, tensor-core MMA (bf16 and f16), base-2
 // exponentials, and the packed FP8 E4M3 -> f16x2 conversion.
 #pragma once
 

@@ -1,5 +1,5 @@
-// gqa_dense_impl.cuh -- launch code of the dense split and combine kernels for
-// one head dimension; included once per head dimension (GQA_HEAD_DIM).
+// gqa_dense_impl.cuh -- launch templates of the dense split and combine kernels,
+// instantiated by one translation unit per head size (d64, d128, d256, d192x128).
 #pragma once
 
 #include "gqa_dense_kernel.cuh"

@@ -18,7 +18,8 @@
 // rows share the CTA, which makes native GQA bit-identical to the same kernel
 // run on K/V expanded to every query head.  With one split the CTA writes
 // bf16 O and fp32 LSE; otherwise fp32 partials (O / l and log2-domain LSE) for
-// the combine kernel.
+// the combine kernel.  D is the score head size (q, K) and DV the value head
+// size (V, O, partials); they differ only in the d192x128 instance.
 //
 // Every mbarrier wait is bounded in wall time; on expiry the CTA flags the
 // device error word, waits (bounded) for its own loads still in flight, and

@@ -1,6 +1,6 @@
-// gqa_paged_impl.cuh -- launch templates of the paged kernel, shared by the
-// translation units that instantiate its forms (top-K FP8; whole-request FP8;
-// whole-request bf16).
+// gqa_paged_impl.cuh -- launch templates of the paged kernel and its merge
+// pass, shared by the translation units that instantiate its forms (top-K
+// FP8; whole-request bf16, FP8 and int8).
 #pragma once
 
 #include "gqa_launch.h"

@@ -1,7 +1,7 @@
 // gqa_paged_kernel.cuh -- paged GQA decode over a shared K/V pool (sm_103a):
 // the sparse top-K form with an FP8 E4M3FN pool and a sigmoid output gate,
 // and the whole-request form (every token of each request up to its own
-// length) over a bf16 or FP8 pool.
+// length) over a bf16, FP8 or int8 pool.
 //
 // The sparse operation is the one of "Sparse paged GQA decode attention with
 // FP8 KV cache on SM89", sections "Workload" and "Implementations": per
@@ -12,13 +12,19 @@
 // and log2(e) (base-2 exponentials), v_scale applied once to the output, then
 // out = sigmoid(gate) * attn.  The whole-request form walks tokens
 // 0 .. seq_len-1 of each request through the same page table (the serving
-// layout the pages leave open), masks query row i of S_q to tokens
-// t <= seq_len - S_q + i, and may split a request's tokens over several CTAs
-// whose fp32 partials (O / l, log2-domain LSE) the dense path's combine
-// kernel merges.
+// layout the pages leave open) and masks query row i of S_q to tokens
+// t <= seq_len - S_q + i.  int8 pools hold symmetric codes (value = code *
+// scale), the int8 KV cache that "Profiling down to the register, then an
+// extension that broke my assumptions twice" leaves open.
 //
-// Mapping: a CTA serves one request (and one token split) and a block of HB
-// KV heads, one consumer warp per head; each consumer owns its head's whole
+// Schedule: a CTA serves a block of HB KV heads and one worker's share of the
+// 16-token steps of all requests, taken in request order (the balanced
+// schedule: every worker gets the same number of steps whatever the length
+// mix).  A request that lies inside one worker is written whole; one shared
+// by several workers leaves fp32 partials (O / l, log2-domain LSE) that
+// gqa_paged_combine_kernel merges.
+//
+// Mapping: one consumer warp per KV head; each consumer owns its head's whole
 // group of G * S_q query rows (at most 16), so every K/V row is fetched from
 // HBM once for the group (the page's "Open problem": its grouped kernels
 // requested every row once per query head).  A producer warp gathers the
@@ -29,7 +35,7 @@
 // read below is free of bank conflicts.
 //
 // Per 16 tokens a consumer computes, on the tensor cores with fp32
-// accumulation (f16 inputs for FP8 pools, bf16 for bf16 pools),
+// accumulation (f16 inputs for 8-bit pools, bf16 for bf16 pools),
 //   S^T[16 tokens x 8 rows] = K[16 x D] . Q^T[D x 8]     (D/16 MMAs)
 //   O^T[D x 8 rows]        += V^T[D x 16] . P^T[16 x 8]  (D/16 MMAs)
 // with the query rows in the MMA's N dimension (8 rows per n-tile), so no
@@ -38,8 +44,11 @@
 // the output dimension is mapped back in the epilogue, which lets every lane
 // read whole 16-byte pieces of its K / V rows.  FP8 codes are widened to f16
 // with the packed cvt instruction -- exact, since every E4M3FN value is an
-// f16 value -- and q is converted to f16 per row with a power-of-two row
-// scale folded back into the score multiplier, so no q value overflows.
+// f16 value; an int8 code c becomes the f16 value c + 1152 by a byte permute
+// and one logic op (exact), the 1152 subtracted exactly from V in f16 and
+// folded into the scores for K.  q is converted to f16 per row with a
+// power-of-two row scale folded back into the score multiplier, so no q
+// value overflows.
 #pragma once
 
 #include "gqa_common.cuh"

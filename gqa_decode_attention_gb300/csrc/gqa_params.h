@@ -20,7 +20,8 @@ constexpr int kSplitKeys = 64;
 constexpr int kPagedMaxHeadsPerCta = 8;
 // Selected tokens per stage of the paged kernel's copy pipeline (one MMA tile).
 constexpr int kPagedStageTokens = 16;
-// Top-K entries whose rows are resolved per pass of the paged kernel.
+// Tokens (top-K entries or request tokens) whose pool rows one index-map pass
+// of the paged kernel resolves.
 constexpr int kPagedChunk = 2048;
 
 struct DenseArgs {
