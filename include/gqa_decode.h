@@ -17,6 +17,13 @@
  *    selected token indices per request, a page table, page size 16, an FP8
  *    E4M3FN K/V pool with per-tensor k_scale / v_scale (k_scale folded into the
  *    score scale, v_scale applied once on the output), then a sigmoid gate.
+ *  - The same page-table addressing over every token of each request up to
+ *    its own length (the serving layout), over bf16, FP8 or int8 pools; int8
+ *    is the in-kernel dequantised cache that "Profiling down to the register,
+ *    then an extension that broke my assumptions twice" leaves open.
+ *  - A score head size different from the value head size (the d192x128
+ *    flavour of "When the K/V copy costs more than the attention", section
+ *    "Limits, and what I'd do next").
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - S_q > 1 uses a bottom-right aligned causal mask: query row i of S_q sees
