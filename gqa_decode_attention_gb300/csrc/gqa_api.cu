@@ -428,15 +428,6 @@ void paged_bind_workspace(const PagedShape &s, int workers, void *ws, PagedArgs 
 
 }  // namespace
 
-cudaError_t launch_combine_partials(int D, const float *o_part, const float *lse_part, __nv_bfloat16 *out,
-                                    float *lse, int B, int Sq, int Hq, int Hkv, int G, int Mq, int S,
-                                    cudaStream_t stream) {
-    if (D == 64) return launch_combine_d64(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
-    if (D == 128) return launch_combine_d128(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
-    if (D == 256) return launch_combine_d256(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
-    return cudaErrorInvalidValue;
-}
-
 // K or V as a 4-D tensor (d, kv head, key, batch) with a box of 64 head-dim
 // elements (128 bytes, one swizzle atom) x 1 head x box_keys keys x 1 batch.
 // Keys past Skv read as zeros.

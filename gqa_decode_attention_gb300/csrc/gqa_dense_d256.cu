@@ -1,4 +1,4 @@
-// gqa_dense_d256.cu -- dense split-KV decode and combine kernels, head dim 256.
+// gqa_dense_d256.cu -- dense split-KV decode (and its combine), head dim 256.
 #include "gqa_dense_impl.cuh"
 
 namespace gqa {
@@ -6,8 +6,4 @@ namespace gqa {
 // head dim keeps a row's arithmetic independent of the group size).
 cudaError_t launch_dense_d256(const DenseLaunch &L) { return launch_umma<256>(L); }
 int dense_ctas_per_sm_d256(int) { return umma_occupancy<256>(); }
-cudaError_t launch_combine_d256(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
-                              int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream) {
-    return launch_combine_rows<256>(o_part, lse_part, out, lse, B, Sq, Hq, Hkv, G, Mq, S, stream);
-}
 }  // namespace gqa

@@ -54,23 +54,6 @@ static int occupancy_cfg() {
 }
 
 template <int D>
-static cudaError_t launch_combine_rows(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse,
-                                       int B, int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream) {
-    const long rows = long(B) * Hkv * Mq;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(rows));
-    cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = (size_t(combine_staged_splits<D>(S)) * (D / 4) + kCombineThreads) * sizeof(float4);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gqa_combine_kernel<D>, o_part, lse_part, out, lse, Sq, Hq, Hkv, G, Mq, S);
-}
-
-template <int D>
 static cudaError_t launch_combine(const DenseLaunch &L) {
     const DenseArgs &a = L.args;
     const long rows = long(a.B) * a.Hkv * a.Mq;

@@ -91,18 +91,6 @@ cudaError_t launch_paged_range_int8(const PagedArgs &a, int D, cudaStream_t stre
 int paged_range_ctas_per_sm_int8(const PagedArgs &a, int D);
 cudaError_t launch_paged_range_combine_int8(const PagedArgs &a, int D, cudaStream_t stream);
 cudaError_t launch_paged_range_combine_bf16(const PagedArgs &a, int D, cudaStream_t stream);
-cudaError_t launch_combine_d64(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
-                               int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
-cudaError_t launch_combine_d128(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
-                                int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
-cudaError_t launch_combine_d256(const float *o_part, const float *lse_part, __nv_bfloat16 *out, float *lse, int B,
-                                int Sq, int Hq, int Hkv, int G, int Mq, int S, cudaStream_t stream);
-// LSE-weighted combine of fp32 split partials laid out [B*Hkv, Mq, S, D]
-// (and [B*Hkv, Mq, S] log2-domain LSE) into out [B, Sq, Hq, D] bf16 and
-// lse [B, Hq, Sq] (nullable), launched as a programmatic dependent.
-cudaError_t launch_combine_partials(int D, const float *o_part, const float *lse_part, __nv_bfloat16 *out,
-                                    float *lse, int B, int Sq, int Hq, int Hkv, int G, int Mq, int S,
-                                    cudaStream_t stream);
 cudaError_t launch_paged_gather(const uint8_t *pool, const int32_t *page_table, const int32_t *topk, uint8_t *out,
                                 int B, int Hkv, int D, int page_size, int pages_per_req, int num_pages, int topk_n,
                                 unsigned *err, cudaStream_t stream);

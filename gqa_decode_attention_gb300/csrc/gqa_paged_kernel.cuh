@@ -79,16 +79,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// Two int8 codes (low byte first) as f16x2, exactly: a code x biased to
-// x + 128 in [0, 255] becomes the mantissa of the f16 1024 + (x + 128)
-// (exponent 2^10, where f16 counts in units of one), and 1152 is subtracted.
-__device__ __forceinline__ uint32_t s8x2_to_f16x2(uint16_t two) {
-    const uint32_t h = prmt(uint32_t(two) ^ 0x8080u, 0x6464u, 0x5140u);
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
-    return r;
-}
-
 // Biased f16x2 of two int8 codes picked from the bytes of (a, b) by the
 // permute selector `sel` (result bytes 0 and 2; bytes 1 and 3 are
 // overwritten): one lop3 flips each code's sign bit (code + 128 in
@@ -109,10 +99,11 @@ __device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t h) {
 // K/V element types of the paged kernel.
 enum : int { kKvBf16 = 0, kKvFp8 = 1, kKvInt8 = 2 };
 
-// Two 8-bit codes (FP8 E4M3FN or int8) widened to f16x2, exactly.
+// Two FP8 E4M3FN codes widened to f16x2, exactly (int8 codes take the biased
+// path of s8pair_biased instead).
 template <int KVT>
 __device__ __forceinline__ uint32_t widen8(uint16_t two) {
-    if constexpr (KVT == kKvInt8) return s8x2_to_f16x2(two);
+    static_assert(KVT == kKvFp8, "widen8 serves FP8 pools");
     return e4m3x2_to_f16x2(two);
 }
 
