@@ -50,8 +50,10 @@ def kv_bytes(B: int, Hkv: int, N: int, D: int, bytes_per_elem: int) -> int:
     return 2 * B * Hkv * N * D * bytes_per_elem
 
 
-def dense_flops(B, Hq, Sq, Skv, D) -> int:
-    return 4 * B * Hq * Sq * Skv * D
+def dense_flops(B, Hq, Sq, Skv, D, Dv=None) -> int:
+    """Score and P.V products: 2 flops per multiply-add, D (score) + Dv
+    (value) dims per key, every key counted for every query row."""
+    return 2 * B * Hq * Sq * Skv * (D + (D if Dv is None else Dv))
 
 
 def paged_flops(B, Hq, topk, D) -> int:
@@ -70,6 +72,14 @@ def workload_kv_bytes(cfg) -> int:
         elem = 2 if cfg.kv_dtype == "bf16" else 1
         return sum(kv_bytes(1, cfg.Hkv, n, cfg.D, elem) for n in paged_kv_lens(cfg))
     return kv_bytes(cfg.B, cfg.Hkv, cfg.topk, cfg.D, 1)
+
+
+def workload_flops(cfg) -> int:
+    if isinstance(cfg, gqa_inputs.DenseConfig):
+        return dense_flops(cfg.B, cfg.Hq, cfg.Sq, cfg.Skv, cfg.D, cfg.dv)
+    if isinstance(cfg, gqa_inputs.PagedKVConfig):
+        return sum(dense_flops(1, cfg.Hq, cfg.Sq, n, cfg.D) for n in paged_kv_lens(cfg))
+    return paged_flops(cfg.B, cfg.Hq, cfg.topk, cfg.D)
 
 
 def workload_config(cfg) -> dict:
@@ -653,6 +663,8 @@ def run_gqa(args) -> int:
             "us_per_call": {"median": round(statistics.median(us), 2), "p10": round(percentile(us, 10), 2),
                             "p90": round(percentile(us, 90), 2)},
             "kv_bytes_per_call": nbytes,
+            "flops_per_call": workload_flops(cfg),
+            "tflops": round(world * workload_flops(cfg) / (max_total_ms / args.steps * 1e-3) / 1e12, 2),
             "frac_of_peak": round(value / world / peak, 4),
             "peak_gbs": peak, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback",

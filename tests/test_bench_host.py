@@ -50,6 +50,10 @@ def test_workload_bytes():
     assert bench.workload_kv_bytes(c["dense_b1_h8x1_d64_sq1_kv1k"]) == 256 << 10
     # 131072 keys x 8 KV heads x (192 K dims + 128 V dims) x 2 bytes
     assert bench.workload_kv_bytes(c["dense_b1_h64x8_d192x128_sq2_kv128k"]) == 640 << 20
+    # flops: 4 B Hq Sq Skv D for equal head sizes (8.59 G for the 128K headline)
+    assert bench.workload_flops(c["dense_b1_h64x8_d128_sq2_kv128k"]) == 4 * 64 * 2 * 131072 * 128
+    assert bench.workload_flops(c["dense_b1_h64x8_d192x128_sq2_kv128k"]) == 2 * 64 * 2 * 131072 * (192 + 128)
+    assert bench.workload_flops(c["paged_fp8_b256_h32x8_d128_top512_ps16"]) == 4 * 256 * 512 * 32 * 128
 
 
 CLOCKS = """index, clocks.current.sm [MHz], clocks.max.sm [MHz], power.draw [W], clocks_event_reasons.active, clocks_event_reasons.hw_slowdown, clocks_event_reasons.hw_thermal_slowdown, clocks_event_reasons.sw_thermal_slowdown, clocks_event_reasons.sw_power_cap
