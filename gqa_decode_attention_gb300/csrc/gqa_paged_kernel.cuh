@@ -44,9 +44,9 @@
 // the output dimension is mapped back in the epilogue, which lets every lane
 // read whole 16-byte pieces of its K / V rows.  FP8 codes are widened to f16
 // with the packed cvt instruction -- exact, since every E4M3FN value is an
-// f16 value; an int8 code c becomes the f16 value c + 1152 by a byte permute
-// and one logic op (exact), the 1152 subtracted exactly from V in f16 and
-// folded into the scores for K.  q is converted to f16 per row with a
+// f16 value; an int8 code c becomes the f16 value c + 1152 by one logic op
+// (after a byte permute where needed), exactly; the 1152 is folded into the
+// scores for K and taken off O once per row for V.  q is converted to f16 per row with a
 // power-of-two row scale folded back into the score multiplier, so no q
 // value overflows.
 #pragma once
@@ -90,9 +90,10 @@ __device__ __forceinline__ uint32_t s8pair_biased(uint32_t a, uint32_t b, uint32
     asm("lop3.b32 %0, %1, %2, %3, 0x9C;" : "=r"(r) : "r"(x), "r"(0x64806480u), "r"(0xFF00FF00u));
     return r;
 }
-__device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t h) {
+// Biased f16x2 (code + 1152) of bytes 0 and 2 of x, in place: one lop3.
+__device__ __forceinline__ uint32_t s8even_biased(uint32_t x) {
     uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x9C;" : "=r"(r) : "r"(x), "r"(0x64806480u), "r"(0xFF00FF00u));
     return r;
 }
 
@@ -361,6 +362,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
     uint32_t qf[NT][C::KSTEPS][2];
     float alpha_s[NT][2];
     float m_run[NT][2], l_run[NT][2];
+    float lq[NT][2];  // int8: sum of the f16-rounded weights the P.V product used (its V bias is 1152 x this)
     float o[NT][C::DB][4];
     int kmax[NT][2];  // last visible token of the rows this lane holds in S^T (S_q > 1)
     float kbias[NT][2];  // int8: score offset of the biased K (1152 * sum of the row's q)
@@ -398,8 +400,14 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 row_alpha[nt] = alpha_w * ldexpf(1.f, ex);
 #pragma unroll
                 for (int kk = 0; kk < C::KSTEPS; ++kk) {
-                    qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
-                    qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+                    if constexpr (KVT == kKvInt8) {
+                        // int8 K pairs dims (0, 2) and (1, 3) of each 4-byte word (no byte permute)
+                        qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][2] * down);  // k = 2c, 2c+1
+                        qf[nt][kk][1] = pack_f16x2(qv[kk][1] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+                    } else {
+                        qf[nt][kk][0] = pack_f16x2(qv[kk][0] * down, qv[kk][1] * down);  // k = 2c, 2c+1
+                        qf[nt][kk][1] = pack_f16x2(qv[kk][2] * down, qv[kk][3] * down);  // k = 2c+8, 2c+9
+                    }
                 }
             } else {
 #pragma unroll
@@ -446,6 +454,7 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
         for (int nt = 0; nt < NT; ++nt) {
             m_run[nt][0] = m_run[nt][1] = -INFINITY;
             l_run[nt][0] = l_run[nt][1] = 0.f;
+            lq[nt][0] = lq[nt][1] = 0.f;
 #pragma unroll
             for (int t = 0; t < C::DB; ++t) o[nt][t][0] = o[nt][t][1] = o[nt][t][2] = o[nt][t][3] = 0.f;
         }
@@ -571,10 +580,11 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                         const uint32_t w0 = w == 0 ? kr[0][u].x : w == 1 ? kr[0][u].y : w == 2 ? kr[0][u].z : kr[0][u].w;
                         const uint32_t w1 = w == 0 ? kr[1][u].x : w == 1 ? kr[1][u].y : w == 2 ? kr[1][u].z : kr[1][u].w;
                         if constexpr (KVT == kKvInt8) {  // biased by +1152, corrected in the scores
-                            af[0] = s8pair_biased(w0, w0, 0x1100u);
-                            af[1] = s8pair_biased(w1, w1, 0x1100u);
-                            af[2] = s8pair_biased(w0, w0, 0x3322u);
-                            af[3] = s8pair_biased(w1, w1, 0x3322u);
+                            // pairs (byte 0, byte 2) and (byte 1, byte 3): Q is packed to match
+                            af[0] = s8even_biased(w0);
+                            af[1] = s8even_biased(w1);
+                            af[2] = s8even_biased(w0 >> 8);
+                            af[3] = s8even_biased(w1 >> 8);
                         } else {
                             af[0] = widen8<KVT>(uint16_t(w0 & 0xffffu));
                             af[1] = widen8<KVT>(uint16_t(w1 & 0xffffu));
@@ -626,6 +636,12 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                     // P^T B fragments: b0 = rows gi at tokens 2c, 2c+1; b1 = tokens 2c+8, 2c+9.
                     const uint32_t pk_lo = KV8 ? pack_f16x2(pv[0], pv[1]) : pack_bf16x2(pv[0], pv[1]);  // token gi
                     const uint32_t pk_hi = KV8 ? pack_f16x2(pv[2], pv[3]) : pack_bf16x2(pv[2], pv[3]);  // token gi + 8
+                    if constexpr (KVT == kKvInt8) {  // the rounded weights, rows 2c, 2c+1 (rescaled like l_run)
+                        const float2 rlo = __half22float2(*reinterpret_cast<const __half2 *>(&pk_lo));
+                        const float2 rhi = __half22float2(*reinterpret_cast<const __half2 *>(&pk_hi));
+                        lq[nt][0] = lq[nt][0] * corr[nt][0] + rlo.x + rhi.x;
+                        lq[nt][1] = lq[nt][1] * corr[nt][1] + rlo.y + rhi.y;
+                    }
                     const int src0 = 4 * (2 * c) + (gi >> 1), src1 = 4 * (2 * c + 1) + (gi >> 1);
                     const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;
                     pb[nt][0] = prmt(__shfl_sync(0xffffffffu, pk_lo, src0), __shfl_sync(0xffffffffu, pk_lo, src1), sel);
@@ -654,15 +670,16 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                     for (int w = 0; w < C::VW; ++w) {
                         uint32_t a_t0[4], a_t1[4];
                         if constexpr (KVT == kKvInt8) {
-                            // pair (token 2c, 2c+1) of byte k of word w: permute, lop3, exact -1152
-                            a_t0[0] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x4400u));
-                            a_t0[1] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x5511u));
-                            a_t0[2] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x4400u));
-                            a_t0[3] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x5511u));
-                            a_t1[0] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x6622u));
-                            a_t1[1] = f16x2_minus_1152(s8pair_biased(vw[0][w], vw[1][w], 0x7733u));
-                            a_t1[2] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x6622u));
-                            a_t1[3] = f16x2_minus_1152(s8pair_biased(vw[2][w], vw[3][w], 0x7733u));
+                            // pair (token 2c, 2c+1) of byte k of word w: permute, lop3; the
+                            // +1152 bias stays in and is removed per row in the epilogue
+                            a_t0[0] = s8pair_biased(vw[0][w], vw[1][w], 0x4400u);
+                            a_t0[1] = s8pair_biased(vw[0][w], vw[1][w], 0x5511u);
+                            a_t0[2] = s8pair_biased(vw[2][w], vw[3][w], 0x4400u);
+                            a_t0[3] = s8pair_biased(vw[2][w], vw[3][w], 0x5511u);
+                            a_t1[0] = s8pair_biased(vw[0][w], vw[1][w], 0x6622u);
+                            a_t1[1] = s8pair_biased(vw[0][w], vw[1][w], 0x7733u);
+                            a_t1[2] = s8pair_biased(vw[2][w], vw[3][w], 0x6622u);
+                            a_t1[3] = s8pair_biased(vw[2][w], vw[3][w], 0x7733u);
                         } else {
                             const uint32_t ab01 = prmt(vw[0][w], vw[1][w], 0x5140u);  // bytes 4w, 4w+1 of tokens 2c / 2c+1
                             const uint32_t ab23 = prmt(vw[0][w], vw[1][w], 0x7362u);  // bytes 4w+2, 4w+3
@@ -715,6 +732,17 @@ __global__ void __launch_bounds__(PagedCfg<D, NT, HB, KVT != kKvBf16>::THREADS,
                 L += __shfl_xor_sync(0xffffffffu, L, 4);
                 L += __shfl_xor_sync(0xffffffffu, L, 8);
                 L += __shfl_xor_sync(0xffffffffu, L, 16);
+                if constexpr (KVT == kKvInt8) {  // O^T accumulated (v + 1152) p~: take 1152 sum(p~) off
+                    float Lq = lq[nt][e];
+                    Lq += __shfl_xor_sync(0xffffffffu, Lq, 4);
+                    Lq += __shfl_xor_sync(0xffffffffu, Lq, 8);
+                    Lq += __shfl_xor_sync(0xffffffffu, Lq, 16);
+#pragma unroll
+                    for (int t = 0; t < C::DB; ++t) {
+                        o[nt][t][e] -= 1152.f * Lq;
+                        o[nt][t][2 + e] -= 1152.f * Lq;
+                    }
+                }
                 const int r = 8 * nt + 2 * c + e;
                 if (r >= a.Mq) continue;
                 const int i = r / a.G;
