@@ -866,7 +866,12 @@ def main(argv=None) -> int:
         return run_reference(args)
     if args.latency_grid:
         return run_latency_grid(args)
-    return run_gqa(args)
+    try:
+        return run_gqa(args)
+    finally:
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
 
 
 if __name__ == "__main__":
