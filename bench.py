@@ -111,7 +111,9 @@ def workload_dtype(cfg) -> str:
 
 def workload_kernel(cfg) -> str:
     if isinstance(cfg, gqa_inputs.DenseConfig):
-        return "gqa_dense_umma_kernel" if cfg.D == 256 else "gqa_dense_split_kernel"
+        import gqa_decode_attention_gb300 as gq
+        eng = gq.gqa_decode_dense_engine(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D, cfg.dv)
+        return "gqa_dense_umma_kernel" if eng == "tcgen05" else "gqa_dense_split_kernel"
     return "gqa_paged_kernel"
 
 

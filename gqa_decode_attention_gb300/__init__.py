@@ -34,7 +34,7 @@ GQA_OK = 0
 EXPORTS = [
     "gqa_status_string", "gqa_version", "gqa_decode", "gqa_decode_num_splits",
     "gqa_decode_workspace_bytes", "gqa_decode_ex", "gqa_decode_dv", "gqa_decode_dv_num_splits",
-    "gqa_decode_dv_workspace_bytes",
+    "gqa_decode_dv_workspace_bytes", "gqa_decode_dense_engine",
     "gqa_decode_noalloc", "gqa_decode_noalloc_scratch_bytes",
     "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged_fp8_dev_scales", "gqa_decode_paged", "gqa_decode_paged_ex",
     "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes", "gqa_decode_paged_dev_scales",
@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_decode_dv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, sz, vp]
     lib.gqa_decode_dv_num_splits.restype = i
     lib.gqa_decode_dv_num_splits.argtypes = [i] * 7
+    lib.gqa_decode_dense_engine.restype = i
+    lib.gqa_decode_dense_engine.argtypes = [i] * 7
     lib.gqa_decode_dv_workspace_bytes.restype = sz
     lib.gqa_decode_dv_workspace_bytes.argtypes = [i] * 8
     lib.gqa_decode_noalloc.restype = st
@@ -209,6 +211,17 @@ def gqa_decode_dv_num_splits(B, Sq, Skv, Hq, Hkv, Dqk, Dv) -> int:
     if n < 0:
         raise GQAError(-n, "gqa_decode_dv_num_splits")
     return n
+
+
+ENGINES = {0: "mma.sync", 1: "tcgen05"}
+
+
+def gqa_decode_dense_engine(B, Sq, Skv, Hq, Hkv, Dqk, Dv=None) -> str:
+    """Kernel engine a dense call of this shape runs: "mma.sync" or "tcgen05"."""
+    n = load_library().gqa_decode_dense_engine(B, Sq, Skv, Hq, Hkv, Dqk, Dqk if Dv is None else Dv)
+    if n < 0:
+        raise GQAError(-n, "gqa_decode_dense_engine")
+    return ENGINES[n]
 
 
 def gqa_decode_dv_workspace_bytes(B, Sq, Skv, Hq, Hkv, Dqk, Dv, num_splits=0) -> int:

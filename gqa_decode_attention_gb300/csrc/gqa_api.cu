@@ -36,7 +36,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------ device facts
 std::mutex g_mu;
 int g_sm_count[kMaxDevices];
-int g_occ[kMaxDevices][4][kDenseCfgs];
+int g_occ[kMaxDevices][4][kDenseCfgs + 1];  // + the tcgen05 engine
 
 bool current_device(int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return false;
@@ -154,8 +154,8 @@ gqa_status check_dense_dv(int B, int Sq, int Skv, int Hq, int Hkv, int D, int Dv
     s->D = D;
     s->G = int(G);
     s->Mq = int(Mq);
-    s->cfg = D == 256 ? 0 : dense_cfg_for_rows(int(Mq < 128 ? Mq : 128));
-    s->qrows = dense_rows_per_cta(D, s->cfg);
+    s->cfg = dense_uses_umma(D, Dv, Sq) ? kUmmaCfg : dense_cfg_for_rows(int(Mq < 128 ? Mq : 128));
+    s->qrows = dense_rows_per_cta(s->cfg);
     s->row_groups = int((Mq + s->qrows - 1) / s->qrows);
     if (long(Hkv) * s->row_groups > 65535) return GQA_ERR_UNSUPPORTED;
     s->n_blocks = (Skv + kSplitKeys - 1) / kSplitKeys;
@@ -520,6 +520,13 @@ int gqa_decode_dv_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, i
     const int splits = choose_splits(s, 0, dev);
     const int tps = blocks_per_split(s, splits);
     return (s.n_blocks + tps - 1) / tps;
+}
+
+int gqa_decode_dense_engine(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv) {
+    DenseShape s;
+    gqa_status st = check_dense_dv(B, Sq, Skv, Hq, Hkv, Dqk, Dv, &s);
+    if (st != GQA_OK) return -int(st);
+    return s.cfg == kUmmaCfg ? GQA_ENGINE_TCGEN05 : GQA_ENGINE_MMA_SYNC;
 }
 
 size_t gqa_decode_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int D, int num_splits) {

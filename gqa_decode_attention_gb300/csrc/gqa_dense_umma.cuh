@@ -1,5 +1,7 @@
 // gqa_dense_umma.cuh -- split-KV grouped-query decode on the fifth-generation
-// tensor cores (tcgen05 + TMEM), for the wide head dimension (D = 256).
+// tensor cores (tcgen05 + TMEM): head dim 256 at every size, and head dim 128
+// when a call has many decode rows per head (the contractions then no longer
+// fit the legacy tensor pipe's latency budget).
 //
 // Same unit of work as the mma.sync kernel: one CTA owns (batch row b, KV
 // head g, KV split s) and up to 128 query rows of that head's group (rows
@@ -8,17 +10,19 @@
 // attention", section "What I was looking at") and each K/V byte of the split
 // is read from HBM once for the whole group.
 //
-// Roles (6 warps):
+// Roles (8 warps):
 //   warp 0      TMA producer: K and V tiles of 64 keys x D into a ring of
 //               shared-memory stages (128-byte swizzle), full / empty mbarriers.
-//   warp 1      allocates TMEM; lane 0 issues every MMA:
+//   warps 1, 2  leave at once (they keep the issuer off sub-partition 1).
+//   warp 3      allocates TMEM; lane 0 issues every MMA:
 //                 S(j) = Q K(j)^T   M=128 rows, N=64 keys, K=D  -> TMEM S[j%2]
 //                 O   += P(j) V(j)  M=128 rows, N=D,  K=64 keys -> TMEM O
 //               in the order QK(0), QK(1), PV(0), QK(2), PV(1), ... so the
 //               tensor core computes the next scores while the softmax runs.
-//   warps 2..5  one thread per query row (TMEM lane): load the S row, scale
-//               into the log2 domain, causal mask, online softmax, write P as
-//               bf16 to shared memory (the A operand of PV), and the epilogue.
+//   warps 4..7  one thread per query row (TMEM lane): load the S row, take
+//               the maximum, causal mask, online softmax in the log2 domain,
+//               write P as bf16 to shared memory (the A operand of PV), and
+//               the epilogue.
 // The online softmax keeps a per-row reference maximum and rescales O (in
 // TMEM) only when a row's maximum grows by more than 2^8; in between, the
 // weights are exp2(s - reference) <= 2^8, which changes rounding only.  Every
@@ -34,6 +38,13 @@
 #include "gqa_umma.cuh"
 
 namespace gqa {
+
+// Longest suspension of the MMA issuer in one wait on P while the next tile's
+// scores are still to be issued (nanoseconds).
+#ifndef GQA_UMMA_ISSUER_POLL_NS
+#define GQA_UMMA_ISSUER_POLL_NS 200
+#endif
+constexpr uint32_t kIssuerPollNs = GQA_UMMA_ISSUER_POLL_NS;
 
 // Keys per tile of the tcgen05 engine; a compile-time knob for tuning builds.
 #ifndef GQA_UMMA_TILE_KEYS
@@ -58,7 +69,17 @@ struct UmmaCfg {
     static constexpr int P_OFF = RING_OFF + STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
-    static constexpr int THREADS = 192;
+    // Warp roles: 0 TMA producer, 1 and 2 leave at once, 3 allocates TMEM and
+    // issues the MMAs, 4..7 softmax (warp w reads TMEM lane quarter w % 4).
+    // The issuer shares SM sub-partition 3 with the softmax warp of lanes
+    // 96..127, which hold query rows only when a CTA has more than 96 of
+    // them: with the issuer beside a busy softmax warp, every MMA issue waits
+    // for issue slots and the score / output chain stretches (measured: 64
+    // rows per CTA at d128 ran at 67% of the HBM copy rate with the issuer in
+    // sub-partition 1, next to the rows 32..63, and at 80% in sub-partition 3).
+    static constexpr int ISSUER = 3;
+    static constexpr int SW0 = ISSUER + 1;  // first softmax warp
+    static constexpr int THREADS = 32 * SW0 + 128;
     static constexpr uint32_t S_COL = 0;            // two BN-column score buffers
     static constexpr uint32_t O_COL = 2 * BN;       // D columns of fp32 output
     static constexpr uint32_t Q_COL = O_COL + D;    // the CTA's queries, D/2 columns (A operand of QK)
@@ -74,7 +95,7 @@ struct UmmaCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
     gqa_dense_umma_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const DenseArgs a) {
     using C = UmmaCfg<D>;
@@ -117,7 +138,7 @@ __global__ void __launch_bounds__(192, 1)
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == 1) tmem_alloc(tmem_base_s, C::TMEM_COLS);
+    if (warp == C::ISSUER) tmem_alloc(tmem_base_s, C::TMEM_COLS);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -166,8 +187,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         return;  // the producer never touches TMEM
     }
+    if (warp < C::ISSUER) return;  // spare warps
 
-    if (warp == 1) {
+    if (warp == C::ISSUER) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_bf16_f32(C::BM, C::BN, false, false);
@@ -200,7 +222,11 @@ __global__ void __launch_bounds__(192, 1)
             }
             for (int j = 0; ok && j < n_it; ++j) {
                 // Wait for P(j) while issuing QK(j+1) the moment its tile lands,
-                // so PV(j) never waits on the next tile's copy.
+                // so PV(j) never waits on the next tile's copy.  The wait on P(j)
+                // suspends the thread in the barrier instruction instead of
+                // polling: this warp shares an SM sub-partition with softmax warps
+                // and must not take their issue slots.  While QK(j+1) is still
+                // pending the suspension is capped so the tile is seen soon.
                 const uint64_t t0 = globaltimer_ns();
                 for (uint32_t spin = 1;; ++spin) {
                     if (qk_issued == j + 1 && j + 1 < n_it &&
@@ -208,7 +234,10 @@ __global__ void __launch_bounds__(192, 1)
                         issue_qk(j + 1);
                         qk_issued = j + 2;
                     }
-                    if (mbar_test_wait(&p_ready[j & 1], (j >> 1) & 1)) break;
+                    const bool pending = qk_issued == j + 1 && j + 1 < n_it;
+                    if (pending ? mbar_try_wait_for(&p_ready[j & 1], (j >> 1) & 1, kIssuerPollNs)
+                                : mbar_try_wait(&p_ready[j & 1], (j >> 1) & 1))
+                        break;
                     if ((spin & 63u) == 0u && (*abort_flag || globaltimer_ns() - t0 > a.wait_limit_ns)) {
                         ok = false;
                         break;
@@ -256,6 +285,9 @@ __global__ void __launch_bounds__(192, 1)
         const int kmax = a.Skv - a.Sq + i_row;  // last visible key (bottom-right causal)
         const int mask_from = a.Skv - a.Sq;
         const uint32_t lane_base = tbase + (uint32_t(quarter * 32) << 16);
+        // A warp whose 32 rows all lie past the group's rows only keeps the
+        // barrier protocol (its lanes' P rows and O rows are never read out).
+        const bool idle = rg * C::BM + quarter * 32 >= a.Mq;
         // This thread's query row -> its TMEM lane, columns Q_COL.. (zeros past Mq).
         {
             const __nv_bfloat16 *qrow =
@@ -293,72 +325,78 @@ __global__ void __launch_bounds__(192, 1)
                 failed = true;
                 break;
             }
-            tc_fence_after_sync();
-            uint32_t sr[C::BN / 32][32];
-#pragma unroll
-            for (int h = 0; h < C::BN / 32; ++h) tmem_ld32(lane_base + C::S_COL + sb * C::BN + h * 32, sr[h]);
-            tmem_wait_ld();
-
-            const int key0 = key_begin + j * C::BN;
-            const bool need_mask = key0 + C::BN - 1 > mask_from;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int h = 0; h < C::BN / 32; ++h)
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float t = __uint_as_float(sr[h][c]) * a.alpha;
-                    if (need_mask && key0 + h * 32 + c > kmax) t = -INFINITY;
-                    sr[h][c] = __float_as_uint(t);
-                    mx = fmaxf(mx, t);
-                }
-            // A row whose maximum grew by more than 2^8 takes it as the new
-            // reference; if it had accumulated anything, its O row is rescaled.
-            const bool renew = mx > m_ref + C::kRescaleLog2;
-            const bool rescale = renew && l > 0.f;
-            if (__any_sync(0xffffffffu, rescale)) {
-                // PV(j-1) must have finished writing O.  Unambiguous: S(j) was
-                // committed after QK(j), which was issued after PV(j-2), so at
-                // least j-1 PV phases are complete when this thread gets here.
-                const bool od = mbar_wait_bounded(o_done, (j - 1) & 1, a.wait_limit_ns, abort_flag);
-                if (!__all_sync(0xffffffffu, od)) {
-                    failed = true;
-                    break;
-                }
+            if (!idle) {
                 tc_fence_after_sync();
-                const float corr = rescale ? fast_exp2(m_ref - mx) : 1.f;
+                uint32_t sr[C::BN / 32][32];
+#pragma unroll
+                for (int h = 0; h < C::BN / 32; ++h) tmem_ld32(lane_base + C::S_COL + sb * C::BN + h * 32, sr[h]);
+                tmem_wait_ld();
+
+                // Scores stay raw; the scale (log2 domain) enters through the
+                // maximum (exact: the scale is positive) and one fma per weight.
+                const int key0 = key_begin + j * C::BN;
+                const bool need_mask = key0 + C::BN - 1 > mask_from;
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int h = 0; h < C::BN / 32; ++h)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        float t = __uint_as_float(sr[h][c]);
+                        if (need_mask && key0 + h * 32 + c > kmax) t = -INFINITY;
+                        sr[h][c] = __float_as_uint(t);
+                        m4[c & 3] = fmaxf(m4[c & 3], t);
+                    }
+                const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.alpha;
+                // A row whose maximum grew by more than 2^8 takes it as the new
+                // reference; if it had accumulated anything, its O row is rescaled.
+                const bool renew = mx > m_ref + C::kRescaleLog2;
+                const bool rescale = renew && l > 0.f;
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // PV(j-1) must have finished writing O.  Unambiguous: S(j) was
+                    // committed after QK(j), which was issued after PV(j-2), so at
+                    // least j-1 PV phases are complete when this thread gets here.
+                    const bool od = mbar_wait_bounded(o_done, (j - 1) & 1, a.wait_limit_ns, abort_flag);
+                    if (!__all_sync(0xffffffffu, od)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const float corr = rescale ? fast_exp2(m_ref - mx) : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(lane_base + C::O_COL + c * 32, ov);
-                    tmem_wait_ld();
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_base + C::O_COL + c * 32, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
-                    tmem_st32(lane_base + C::O_COL + c * 32, ov);
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+                        tmem_st32(lane_base + C::O_COL + c * 32, ov);
+                    }
+                    tmem_wait_st();
+                    l *= corr;
                 }
-                tmem_wait_st();
-                l *= corr;
-            }
-            if (renew) m_ref = mx;
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            // P = exp2(t - reference) as bf16, straight into the swizzled P tile
-            uint8_t *prow = prow_base + sb * C::P_BYTES;
-            float psum = 0.f;
+                if (renew) m_ref = mx;
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                // P = exp2(scale * s - reference) as bf16, straight into the swizzled P tile
+                uint8_t *prow = prow_base + sb * C::P_BYTES;
+                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int u = 0; u < C::BN / 8; ++u) {
-                uint32_t w[4];
+                for (int u = 0; u < C::BN / 8; ++u) {
+                    uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = u * 8 + e * 2;
-                    const float p0 = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_use);
-                    const float p1 = fast_exp2(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]) - m_use);
-                    psum += p0 + p1;
-                    w[e] = pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = u * 8 + e * 2;
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.alpha, -m_use));
+                        const float p1 =
+                            fast_exp2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), a.alpha, -m_use));
+                        ps4[e] += p0 + p1;
+                        w[e] = pack_bf16x2(p0, p1);
+                    }
+                    *reinterpret_cast<uint4 *>(prow + ((u ^ (lr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                *reinterpret_cast<uint4 *>(prow + ((u ^ (lr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                fence_proxy_async_shared();
+                tc_fence_before_sync();
             }
-            l += psum;
-            fence_proxy_async_shared();
-            tc_fence_before_sync();
             mbar_arrive(&p_ready[sb]);
         }
 
@@ -380,7 +418,7 @@ __global__ void __launch_bounds__(192, 1)
                 *abort_flag = 1;
             }
         }
-        if (have_o) {
+        if (have_o && !idle) {
             tc_fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse2 = l > 0.f ? m_ref + log2f(l) : -INFINITY;
@@ -423,10 +461,10 @@ __global__ void __launch_bounds__(192, 1)
         }
     }
 
-    // ---- teardown (warps 1..5): every TMEM access and MMA is done; free TMEM
+    // ---- teardown (issuer and softmax warps): every TMEM access and MMA is done; free TMEM
     tc_fence_before_sync();
     asm volatile("bar.sync 2, 160;" ::: "memory");
-    if (warp == 1) {
+    if (warp == C::ISSUER) {
         tc_fence_after_sync();
         tmem_dealloc(tbase, C::TMEM_COLS);
     }

@@ -16,10 +16,24 @@ namespace gqa {
 constexpr int kDenseCfgs = 4;
 inline int dense_cfg_for_rows(int rows) { return rows <= 16 ? 0 : rows <= 32 ? 1 : rows <= 64 ? 2 : 3; }
 inline int dense_cfg_rows(int cfg) { return 16 << cfg; }
-// Query rows per CTA of the engine serving head dim D: the tcgen05 engine
-// (D = 256) always holds 128 rows (its TMEM lanes); the mma.sync engine holds
-// the group's rows rounded up to 16, at most 128.
-inline int dense_rows_per_cta(int D, int cfg) { return D == 256 ? 128 : dense_cfg_rows(cfg); }
+// The tcgen05 engine takes the slot after the mma.sync configurations.  It
+// serves head dim 256 at every size, and head dim 128 once a call has at least
+// GQA_D128_UMMA_MIN_SQ decode rows per head: from there a CTA holds 64 or more
+// query rows, the score and output contractions stop fitting the legacy
+// tensor pipe's latency budget, and the 128-lane TMEM tile pays.  The choice
+// depends on Sq and the head dims only, never on the group size, so a query
+// row gets the same arithmetic with native GQA as with K/V expanded per head.
+constexpr int kUmmaCfg = kDenseCfgs;
+#ifndef GQA_D128_UMMA_MIN_SQ
+#define GQA_D128_UMMA_MIN_SQ 8
+#endif
+inline bool dense_uses_umma(int D, int Dv, int Sq) {
+    return D == 256 || (D == 128 && Dv == 128 && Sq >= GQA_D128_UMMA_MIN_SQ);
+}
+// Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM
+// lanes); the mma.sync engine holds the group's rows rounded up to 16, at
+// most 128.
+inline int dense_rows_per_cta(int cfg) { return cfg == kUmmaCfg ? 128 : dense_cfg_rows(cfg); }
 // Tile keys and ring depth of the 16-row instance at D = 128 (the decode
 // shape with the most traffic); compile-time knobs for tuning builds.
 #ifndef GQA_D128_R16_TILE
@@ -45,7 +59,7 @@ struct DenseLaunch {
     const void *k;
     const void *v;
     int D;
-    int cfg;
+    int cfg;  // mma.sync configuration 0..kDenseCfgs-1, or kUmmaCfg
     cudaStream_t stream;
     cudaEvent_t ev_before;  // measurement hook: recorded around the split kernel when both are set
     cudaEvent_t ev_after;
@@ -63,6 +77,7 @@ cudaError_t launch_dense_d256(const DenseLaunch &L);
 cudaError_t launch_dense_d192x128(const DenseLaunch &L);
 int dense_ctas_per_sm_d192x128(int cfg);
 // Resident CTAs per SM of the dense split kernel for (D, cfg); 0 on error.
+// cfg = kUmmaCfg gives the tcgen05 engine's figure (D = 128 and 256).
 int dense_ctas_per_sm_d64(int cfg);
 int dense_ctas_per_sm_d128(int cfg);
 int dense_ctas_per_sm_d256(int cfg);

@@ -102,6 +102,10 @@ CONFIGS = {
         "dense_b32_h64x8_d128_sq1_kv32k", B=32, Sq=1, Skv=32768, Hq=64, Hkv=8, D=128, seed=1003),
     "dense_b8_h32x2_d256_sq8_kv128k": DenseConfig(
         "dense_b8_h32x2_d256_sq8_kv128k", B=8, Sq=8, Skv=131072, Hq=32, Hkv=2, D=256, seed=1004),
+    # eight decode rows per head (draft tokens verified in one call) on the
+    # headline's long-cache shape: 64 query rows per KV head
+    "dense_b1_h64x8_d128_sq8_kv128k": DenseConfig(
+        "dense_b1_h64x8_d128_sq8_kv128k", B=1, Sq=8, Skv=131072, Hq=64, Hkv=8, D=128, seed=1010),
     # the d192x128 head flavour (scores over 192 dims, values of 128) on the
     # headline's long-cache shape
     "dense_b1_h64x8_d192x128_sq2_kv128k": DenseConfig(

@@ -151,6 +151,20 @@ gqa_status gqa_decode_dv(const void *q, const void *k, const void *v, void *out,
 /* Split count gqa_decode_dv would use (>= 1), or a negative gqa_status. */
 int gqa_decode_dv_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv);
 
+/* Which kernel engine a dense call of this shape runs (gqa_decode,
+ * gqa_decode_ex, gqa_decode_noalloc, gqa_decode_host with Dqk == Dv, and
+ * gqa_decode_dv): GQA_ENGINE_MMA_SYNC (TMA ring + mma.sync, query rows of the
+ * group rounded up to 16 per CTA) or GQA_ENGINE_TCGEN05 (TMA ring + tcgen05
+ * with the scores and output in tensor memory, 128 query rows per CTA).  Head
+ * dim 256 always runs on tcgen05, head dim 128 on tcgen05 from 8 decode rows
+ * per head (Sq >= 8), everything else on mma.sync.  The choice depends on
+ * (Sq, Dqk, Dv) only, never on the group size, so native GQA and the same
+ * call on K/V expanded per query head share a row's arithmetic.  Host-only:
+ * touches no device.  Returns a negative gqa_status on invalid arguments. */
+#define GQA_ENGINE_MMA_SYNC 0
+#define GQA_ENGINE_TCGEN05 1
+int gqa_decode_dense_engine(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv);
+
 /* Bytes of workspace gqa_decode_dv needs for `num_splits` (0 = automatic);
  * 0 when a single split is used or on invalid arguments. */
 size_t gqa_decode_dv_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv,

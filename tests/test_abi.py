@@ -95,6 +95,22 @@ def test_dense_ex_rejects(lib):
     assert lib.gqa_decode_num_splits(1, 1, 64, 8, 2, 96) == -2
 
 
+def test_dense_engine_choice(lib):
+    """Host-only: d256 always on tcgen05, d128 on tcgen05 from 8 decode rows
+    per head, the rest on mma.sync; the group size never changes the engine."""
+    eng = lib.gqa_decode_dense_engine
+    for Hq, Hkv in [(8, 8), (64, 8), (64, 1)]:
+        assert eng(1, 1, 100, Hq, Hkv, 256, 256) == 1
+        assert eng(1, 7, 100, Hq, Hkv, 128, 128) == 0
+        assert eng(1, 8, 100, Hq, Hkv, 128, 128) == 1
+        assert eng(1, 64, 100, Hq, 1, 128, 128) == 1
+        assert eng(1, 8, 100, Hq, Hkv, 64, 64) == 0
+        assert eng(1, 8, 100, Hq, Hkv, 192, 128) == 0
+    assert eng(1, 2, 1, 8, 2, 128, 128) == -1     # Sq > Skv
+    assert eng(1, 8, 100, 8, 2, 96, 96) == -2     # unsupported head size
+    assert eng(1, 8, 100, 8, 2, 128, 192) == -2
+
+
 def test_dense_dv_rejects(lib):
     def dv(Dqk=192, Dv=128, splits=0, B=1, Sq=1, Skv=64, Hq=8, Hkv=2, q=A, v=A, ws_bytes=0):
         return lib.gqa_decode_dv(q, A, v, A, A, B, Sq, Skv, Hq, Hkv, Dqk, Dv, 0.0, splits, None, ws_bytes, None)

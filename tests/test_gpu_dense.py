@@ -53,6 +53,45 @@ def test_dense_small_vs_oracle(gq, orc, shape):
     assert_lse_close(lse, ref_l, f"LSE {shape}")
 
 
+# Head dim 128 with 8 or more decode rows per head runs on the tcgen05 engine:
+# partial tiles (32, 36, 64 rows), one full 128-row tile, two and three row
+# groups, ragged key tails, a cache shorter than one 64-key tile.
+UMMA128 = [
+    (1, 8, 8, 8, 1, 128), (2, 8, 65, 8, 2, 128), (1, 8, 1000, 64, 8, 128), (1, 9, 777, 16, 4, 128),
+    (1, 16, 4097, 64, 8, 128), (2, 12, 3000, 32, 2, 128), (1, 33, 500, 8, 1, 128), (1, 64, 200, 4, 1, 128),
+]
+
+
+@pytest.mark.parametrize("shape", UMMA128, ids=lambda s: "b{}_sq{}_kv{}_h{}x{}_d{}".format(*s))
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_d128_tcgen05_vs_oracle(gq, orc, shape, splits):
+    B, Sq, Skv, Hq, Hkv, D = shape
+    assert gq.gqa_decode_dense_engine(B, Sq, Skv, Hq, Hkv, D) == "tcgen05"
+    q, k, v = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=hash(shape) % 100000 + splits)
+    out, lse = _run(gq, q, k, v, num_splits=splits)
+    ref_o, ref_l = orc.gqa_decode(q, k, v, 1.0 / math.sqrt(D))
+    assert_o_close(out, ref_o, f"O {shape} splits {splits}")
+    assert_lse_close(lse, ref_l, f"LSE {shape} splits {splits}")
+
+
+def test_d128_engine_boundary(gq, orc):
+    """Sq = 7 (mma.sync) and Sq = 8 (tcgen05) on the same cache agree with the
+    oracle and with each other on the rows they share (the last 7 rows of the
+    Sq = 8 call see the same keys as the Sq = 7 call)."""
+    B, Skv, Hq, Hkv, D = 1, 2000, 16, 2, 128
+    q8, k, v = gqa_inputs.dense_inputs(B, 8, Skv, Hq, Hkv, D, seed=77)
+    q7 = q8[:, 1:].contiguous()
+    assert gq.gqa_decode_dense_engine(B, 7, Skv, Hq, Hkv, D) == "mma.sync"
+    o7, l7 = _run(gq, q7, k, v)
+    o8, l8 = _run(gq, q8, k, v)
+    for o, l, q in ((o7, l7, q7), (o8, l8, q8)):
+        ref_o, ref_l = orc.gqa_decode(q, k, v, 1.0 / math.sqrt(D))
+        assert_o_close(o, ref_o, f"Sq {q.shape[1]}")
+        assert_lse_close(l, ref_l)
+    assert_o_close(o8[:, 1:], o7.double(), "Sq 8 rows 1.. vs Sq 7")
+    assert torch.allclose(l8[:, :, 1:], l7, atol=1e-4, rtol=0)
+
+
 @pytest.mark.parametrize("splits", [1, 2, 7, 10**6])
 def test_split_counts_agree(gq, orc, splits):
     B, Sq, Skv, Hq, Hkv, D = 1, 2, 1000, 16, 2, 128
@@ -81,7 +120,7 @@ def test_same_splits_bitwise_repeatable(gq):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 4), (8, 2), (4, 2), (16, 4), (8, 1), (64, 8), (32, 2)])
-@pytest.mark.parametrize("Sq", [1, 2])
+@pytest.mark.parametrize("Sq", [1, 2, 8])
 @pytest.mark.parametrize("D", [128, 256])
 def test_gqa_bitwise_equals_expanded_mha(gq, Hq, Hkv, Sq, D):
     """Native GQA == the same kernel on K/V pre-expanded to Hq heads, bit for bit
@@ -197,11 +236,12 @@ def test_invalid_args_launch_nothing(gq):
     assert gq.gqa_device_status() == 0
 
 
-@pytest.mark.parametrize("D", [128, 256])
-def test_wait_timeout_is_reported_not_hung(gq, D):
+@pytest.mark.parametrize("D,Sq", [(128, 1), (128, 8), (256, 1)])
+def test_wait_timeout_is_reported_not_hung(gq, D, Sq):
     """A load that never arrives makes the bounded pipeline wait run out: the
-    kernel flags GQA_ERR_DEVICE_TIMEOUT and returns; the context stays usable."""
-    q, k, v = (t.cuda() for t in gqa_inputs.dense_inputs(1, 1, 1000, 8, 2, D, seed=17))
+    kernel flags GQA_ERR_DEVICE_TIMEOUT and returns; the context stays usable.
+    (d128 with Sq 1: mma.sync engine; d128 with Sq 8 and d256: tcgen05.)"""
+    q, k, v = (t.cuda() for t in gqa_inputs.dense_inputs(1, Sq, 1000, 8, 2, D, seed=17))
     gq.gqa_set_wait_limit_ns(50_000_000)
     gq.gqa_debug_set_fault_mode(1)
     try:
