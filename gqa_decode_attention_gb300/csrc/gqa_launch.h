@@ -18,11 +18,13 @@ inline int dense_cfg_for_rows(int rows) { return rows <= 16 ? 0 : rows <= 32 ? 1
 inline int dense_cfg_rows(int cfg) { return 16 << cfg; }
 // The tcgen05 engine takes the slot after the mma.sync configurations.  It
 // serves head dim 256 at every size, and head dim 128 once a call has at least
-// GQA_D128_UMMA_MIN_SQ decode rows per head: from there a CTA holds 64 or more
-// query rows, the score and output contractions stop fitting the legacy
-// tensor pipe's latency budget, and the 128-lane TMEM tile pays.  The choice
-// depends on Sq and the head dims only, never on the group size, so a query
-// row gets the same arithmetic with native GQA as with K/V expanded per head.
+// GQA_D128_UMMA_MIN_SQ decode rows per head: with the usual groups of 8 or more
+// query heads a CTA then holds 64 or more rows, the score and output
+// contractions stop fitting the legacy tensor pipe's latency budget, and the
+// 128-lane TMEM tile pays (with small groups the tcgen05 kernel runs a few
+// points below the mma.sync one).  The choice depends on Sq and the head dims
+// only, never on the group size, so a query row gets the same arithmetic with
+// native GQA as with K/V expanded per head.
 constexpr int kUmmaCfg = kDenseCfgs;
 #ifndef GQA_D128_UMMA_MIN_SQ
 #define GQA_D128_UMMA_MIN_SQ 8
