@@ -64,6 +64,20 @@ CLOCKS = """index, clocks.current.sm [MHz], clocks.max.sm [MHz], power.draw [W],
 """
 
 
+def test_workload_kernel_names_the_engine():
+    """The roofline's kernel is the engine the library picks (host-only query)."""
+    import gqa_inputs
+    from gqa_decode_attention_gb300 import build as gbuild
+    gbuild.build()
+    c = gqa_inputs.CONFIGS
+    assert bench.workload_kernel(c["dense_b1_h64x8_d128_sq2_kv128k"]) == "gqa_dense_split_kernel"
+    assert bench.workload_kernel(c["dense_b1_h64x8_d128_sq8_kv128k"]) == "gqa_dense_umma_kernel"
+    assert bench.workload_kernel(c["dense_b8_h32x2_d256_sq8_kv128k"]) == "gqa_dense_umma_kernel"
+    assert bench.workload_kernel(c["dense_b1_h64x8_d192x128_sq2_kv128k"]) == "gqa_dense_split_kernel"
+    assert bench.workload_kernel(c["paged_fp8_b256_h32x8_d128_top512_ps16"]) == "gqa_paged_kernel"
+    assert bench.workload_kv_bytes(c["dense_b1_h64x8_d128_sq8_kv128k"]) == 512 << 20
+
+
 def test_parse_clocks():
     c = bench.parse_clocks(CLOCKS)
     assert c["sm_mhz"] == 1965 and c["sm_max_mhz"] == 2070
