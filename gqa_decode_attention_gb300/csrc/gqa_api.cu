@@ -231,6 +231,10 @@ gqa_status run_dense(const void *q, const void *k, const void *v, void *out, flo
     int dev = 0;
     if (!current_device(&dev)) return GQA_ERR_CUDA;
     if (encode_fn() == nullptr) return GQA_ERR_CUDA;
+    // The first occupancy query on a device also raises the kernel's dynamic
+    // shared-memory limit there (a per-device attribute); made here so that a
+    // call with an explicit split count on a second device is covered too.
+    dense_occupancy(dev, s.D, s.cfg);
     int splits = choose_splits(s, requested_splits, dev);
     // Equalise: the split count actually realised by blocks_per_split.
     const int tps = blocks_per_split(s, splits);
@@ -734,6 +738,7 @@ gqa_status run_paged_kv(const void *q, const void *k_pool, const void *v_pool, i
         return GQA_ERR_ALIGNMENT;
     int dev = 0;
     if (!current_device(&dev)) return GQA_ERR_CUDA;
+    paged_occupancy(dev, s);  // sets the kernel's shared-memory limit on this device (see run_dense)
     const int splits = choose_paged_workers(s, num_splits, dev);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const size_t need = paged_workspace_bytes(s, splits);
