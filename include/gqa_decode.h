@@ -91,9 +91,13 @@ const char *gqa_version(void);
  * row i < Sq:  s_j = scale * q[b,i,h,:] . k[b,j,g,:]  for visible j,
  *   lse[b,h,i] = ln sum_j exp(s_j),  out[b,i,h,:] = sum_j exp(s_j - lse) v[b,j,g,:].
  * The KV walk is split across CTAs (split count chosen from Skv, B*Hkv and
- * the SM count); each CTA owns one (b, g, split) and the whole group of
- * (Hq/Hkv)*Sq query rows, so each K/V byte is read from HBM once.  When more
- * than one split is used, an LSE-weighted combine kernel produces out / lse.
+ * the SM count); each CTA owns one (b, g, split) and the group's
+ * (Hq/Hkv)*Sq query rows, up to 128 of them, so each K/V byte is read from
+ * HBM once per 128 query rows of a group (once for groups of up to 128
+ * rows).  When more than one split is used, an LSE-weighted combine kernel
+ * produces out / lse.  Two kernel engines serve the dense calls (see
+ * gqa_decode_dense_engine): mma.sync, and tcgen05 for head dim 256 and for
+ * head dim 128 from Sq >= 8.
  *
  * q, k, v, out : device, bf16, layouts above.   lse : device fp32 or NULL.
  * Limits: 1 <= Sq <= Skv, B >= 1, Hkv >= 1, Hq % Hkv == 0,
