@@ -32,11 +32,12 @@ def _dense(gq, q, k, v, num_splits=0):
     return out.cpu(), lse.cpu()
 
 
-@pytest.mark.parametrize("D", [64, 256])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_largest_query_group(gq, orc, D):
-    """d 64: 4096 query rows per KV head (512 heads over 1, 8 decode rows), 32
-    row groups of 128; d 256 (tcgen05 engine): 512 rows, 4 row groups."""
-    Hq = 512 if D == 64 else 64
+    """d 64 (mma.sync engine) and d 128 (tcgen05 engine, Sq 8): 4096 query rows
+    per KV head (512 heads over 1, 8 decode rows), 32 row groups of 128; d 256
+    (tcgen05 engine): 512 rows, 4 row groups."""
+    Hq = 64 if D == 256 else 512
     Sq = 8
     q, k, v = gqa_inputs.dense_inputs(1, Sq, 300, Hq, 1, D, seed=500 + D, device="cuda")
     out, lse = _dense(gq, q, k, v)
