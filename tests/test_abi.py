@@ -111,6 +111,14 @@ def test_dense_engine_choice(lib):
     assert eng(1, 8, 100, 8, 2, 128, 192) == -2
 
 
+def test_engine_names_match_header():
+    """The binding's engine names follow the header's GQA_ENGINE_* values."""
+    text = open(os.path.join(ROOT, "include", "gqa_decode.h")).read()
+    vals = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define GQA_ENGINE_(\w+) (\d+)", text)}
+    assert vals == {"MMA_SYNC": 0, "TCGEN05": 1}
+    assert gq.ENGINES == {vals["MMA_SYNC"]: "mma.sync", vals["TCGEN05"]: "tcgen05"}
+
+
 def test_dense_dv_rejects(lib):
     def dv(Dqk=192, Dv=128, splits=0, B=1, Sq=1, Skv=64, Hq=8, Hkv=2, q=A, v=A, ws_bytes=0):
         return lib.gqa_decode_dv(q, A, v, A, A, B, Sq, Skv, Hq, Hkv, Dqk, Dv, 0.0, splits, None, ws_bytes, None)
