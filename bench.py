@@ -355,6 +355,29 @@ def _copy_peak_gbs(dev) -> float:
     return best
 
 
+def _read_peak_gbs(dev) -> float:
+    """Read-only stream bandwidth of this run: a sum over 4 GiB of fp32
+    (bytes read / time, the result is 4 bytes), best of 5.  A decode kernel
+    only reads its K/V, so it is the denominator that matches its traffic;
+    the copy peak (read + write) is the one the benchmark configuration
+    quotes, and a read-only stream can exceed it."""
+    import torch
+    n = 1 << 30
+    a = torch.ones(n, dtype=torch.float32, device=dev)
+    r = torch.empty((), dtype=torch.float32, device=dev)
+    best = 0.0
+    for _ in range(6):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch.sum(a, dtype=torch.float32, out=r)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, gbs(a.numel() * a.element_size(), e0.elapsed_time(e1)))
+    del a, r
+    torch.cuda.empty_cache()
+    return best
+
+
 def _cpu_baseline(cfg, tensors, max_seconds=30.0, min_seconds=10.0) -> dict:
     """The fp64 oracle, as it stands, on this host's cores: the full workload
     repeated until min_seconds (or a row subset when one pass would exceed
@@ -523,6 +546,7 @@ def run_gqa(args) -> int:
     peak, peak_kind = measured_hbm_peak()
 
     copy_peak = _copy_peak_gbs(dev)
+    read_peak = _read_peak_gbs(dev)
     call, tensors, launches_per_call, splits = _make_call(gq, cfg, dev, seed_offset=rank)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_bytes = max(512 << 20, 4 * l2)
@@ -672,11 +696,15 @@ def run_gqa(args) -> int:
             else "fallback",
             "copy_peak_gbs_this_run": round(copy_peak, 1),
             "frac_of_copy_peak_this_run": round(value / world / copy_peak, 4),
+            "read_peak_gbs_this_run": round(read_peak, 1),
+            "frac_of_read_peak_this_run": round(value / world / read_peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(cfg.name),
                          "kernel": workload_kernel(cfg),
                          "kernel_us": round(kern_avg * 1e3, 2),
-                         "algorithmic_bytes_per_launch": nbytes},
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "read_peak_this_run": round(read_peak, 1),
+                         "frac_of_read_peak_this_run": round(achieved / read_peak, 4)},
             "cpu_baseline": cpu_base,
             "e2e": e2e,
             "gpu_launches": args.steps * launches_per_call,

@@ -15,8 +15,7 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-# GQA_DECODE_LIB selects another build of the library (for example a tuning build).
-LIB_PATH = os.environ.get("GQA_DECODE_LIB") or os.path.join(_HERE, "libgqa_decode.so")
+LIB_PATH = os.path.join(_HERE, "libgqa_decode.so")
 
 STATUS = {
     0: "GQA_OK",
@@ -141,6 +140,37 @@ def _need(t: torch.Tensor, name: str, dtype, device_type: str):
         raise ValueError(f"{name}: must be contiguous")
 
 
+def _need_shape(t, name: str, shape, dtype, like: torch.Tensor):
+    """A caller-supplied tensor the library reads or writes through a raw
+    pointer: it must have exactly the shape the call implies (a smaller one
+    would be read or written out of bounds), the dtype, and lie contiguous on
+    the device of `like`."""
+    if t is None:
+        return
+    _need(t, name, dtype, like.device.type)
+    if t.device != like.device:
+        raise ValueError(f"{name}: expected a tensor on {like.device}, got {t.device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _dense_shapes(fn: str, q, k, v, out, lse, Dv=None):
+    """Shape checks shared by the dense entry points: q [B,Sq,Hq,D],
+    k [B,Skv,Hkv,D], v [B,Skv,Hkv,Dv], out [B,Sq,Hq,Dv], lse [B,Hq,Sq]."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError(f"{fn}: q, k and v must be 4-D")
+    B, Sq, Hq, D = q.shape
+    _, Skv, Hkv, _ = k.shape
+    Dv = D if Dv is None else Dv
+    if tuple(k.shape) != (B, Skv, Hkv, D) or tuple(v.shape) != (B, Skv, Hkv, Dv):
+        raise ValueError(f"{fn}: k must be [B,Skv,Hkv,{D}] and v [B,Skv,Hkv,{Dv}] with q's batch")
+    for t, n in ((k, "k"), (v, "v")):
+        if t.device != q.device:
+            raise ValueError(f"{fn}: {n} is on {t.device}, q on {q.device}")
+    _need_shape(out, "out", (B, Sq, Hq, Dv), torch.bfloat16, q)
+    _need_shape(lse, "lse", (B, Hq, Sq), torch.float32, q)
+
+
 def _scale_arg(scale):
     return 0.0 if scale is None else float(scale)
 
@@ -164,6 +194,7 @@ def gqa_decode_ex(q, k, v, out=None, lse=None, scale=None, num_splits=0, workspa
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16, "cuda")
+    _dense_shapes("gqa_decode_ex", q, k, v, out, lse)
     B, Sq, Hq, D = q.shape
     _, Skv, Hkv, _ = k.shape
     if out is None:
@@ -191,8 +222,7 @@ def gqa_decode_dv(q, k, v, out=None, lse=None, scale=None, num_splits=0, workspa
     B, Sq, Hq, Dqk = q.shape
     _, Skv, Hkv, _ = k.shape
     Dv = v.shape[-1]
-    if tuple(v.shape[:3]) != (B, Skv, Hkv) or tuple(k.shape) != (B, Skv, Hkv, Dqk):
-        raise ValueError("gqa_decode_dv: k must be [B,Skv,Hkv,Dqk] and v [B,Skv,Hkv,Dv]")
+    _dense_shapes("gqa_decode_dv", q, k, v, out, lse, Dv=Dv)
     if out is None:
         out = torch.empty((B, Sq, Hq, Dv), dtype=torch.bfloat16, device=q.device)
     if lse is None and with_lse:
@@ -234,6 +264,7 @@ def gqa_decode_noalloc(q, k, v, out, lse=None, scale=None, num_splits=0, stream=
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _need(t, n, torch.bfloat16, "cuda")
+    _dense_shapes("gqa_decode_noalloc", q, k, v, out, lse)
     B, Sq, Hq, D = q.shape
     _, Skv, Hkv, _ = k.shape
     st = lib.gqa_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Skv, Hq, Hkv, D,
@@ -262,6 +293,7 @@ def gqa_decode_host(q, k, v, out, lse=None, scale=None, stream=None):
     lib = load_library()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _need(t, n, torch.bfloat16, "cpu")
+    _dense_shapes("gqa_decode_host", q, k, v, out, lse)
     B, Sq, Hq, D = q.shape
     _, Skv, Hkv, _ = k.shape
     st = lib.gqa_decode_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Sq, Skv, Hq, Hkv, D,
@@ -290,8 +322,21 @@ def gqa_decode_paged_fp8(q, gate, k_pool, v_pool, page_table, topk_idx, k_scale=
         _need(t, n, torch.uint8, "cuda")
     _need(page_table, "page_table", torch.int32, "cuda")
     _need(topk_idx, "topk_idx", torch.int32, "cuda")
+    if q.dim() != 3 or k_pool.dim() != 4 or page_table.dim() != 2 or topk_idx.dim() != 2:
+        raise ValueError("gqa_decode_paged_fp8: q [B,Hq,D], pools [pages,page_size,Hkv,D], page_table and "
+                         "topk_idx 2-D")
     B, Hq, D = q.shape
     num_pages, page_size, Hkv, _ = k_pool.shape
+    if tuple(v_pool.shape) != tuple(k_pool.shape) or k_pool.shape[3] != D:
+        raise ValueError("gqa_decode_paged_fp8: v_pool must have k_pool's shape, with q's head size")
+    if page_table.shape[0] != B or topk_idx.shape[0] != B:
+        raise ValueError("gqa_decode_paged_fp8: page_table and topk_idx need one row per request")
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool"), (page_table, "page_table"), (topk_idx, "topk_idx")):
+        if t.device != q.device:
+            raise ValueError(f"gqa_decode_paged_fp8: {n} is on {t.device}, q on {q.device}")
+    _need_shape(gate, "gate", (B, Hq, D), torch.bfloat16, q)
+    _need_shape(out, "out", (B, Hq, D), torch.bfloat16, q)
+    _need_shape(lse, "lse", (B, Hq), torch.float32, q)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and with_lse:
@@ -350,8 +395,19 @@ def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_sca
         _need(t, n, k_pool.dtype, "cuda")
     _need(page_table, "page_table", torch.int32, "cuda")
     _need(seq_lens, "seq_lens", torch.int32, "cuda")
+    if q.dim() != 4 or k_pool.dim() != 4 or page_table.dim() != 2:
+        raise ValueError("gqa_decode_paged: q [B,Sq,Hq,D], pools [pages,page_size,Hkv,D], page_table 2-D")
     B, Sq, Hq, D = q.shape
     num_pages, page_size, Hkv, _ = k_pool.shape
+    if tuple(v_pool.shape) != tuple(k_pool.shape) or k_pool.shape[3] != D:
+        raise ValueError("gqa_decode_paged: v_pool must have k_pool's shape, with q's head size")
+    if page_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("gqa_decode_paged: page_table needs one row and seq_lens one entry per request")
+    for t, n in ((k_pool, "k_pool"), (v_pool, "v_pool"), (page_table, "page_table"), (seq_lens, "seq_lens")):
+        if t.device != q.device:
+            raise ValueError(f"gqa_decode_paged: {n} is on {t.device}, q on {q.device}")
+    _need_shape(out, "out", (B, Sq, Hq, D), torch.bfloat16, q)
+    _need_shape(lse, "lse", (B, Hq, Sq), torch.float32, q)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and with_lse:

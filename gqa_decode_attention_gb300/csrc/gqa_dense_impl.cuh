@@ -18,17 +18,14 @@ struct DenseInst {
     static constexpr auto kernel() { return gqa_dense_split_kernel<D, DV, RB, T, S>; }
 };
 
+// The launches below rely on the kernel's dynamic shared-memory limit having
+// been raised on the current device: the front end's occupancy query (once
+// per device and kernel, under its lock) does that before any call launches.
 template <int D, int DV, int CFG>
 static cudaError_t launch_split_cfg(const DenseLaunch &L) {
     using I = DenseInst<D, DV, CFG>;
     using C = typename I::C;
     auto kern = I::kernel();
-    static bool attr_set = false;  // per process; the attribute is per function
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     CUtensorMap tk, tv;
     if (!make_kv_tensor_map(&tk, L.k, L.args.B, L.args.Skv, L.args.Hkv, D, I::T) ||
         !make_kv_tensor_map(&tv, L.v, L.args.B, L.args.Skv, L.args.Hkv, DV, I::T))
@@ -76,12 +73,6 @@ template <int D>
 static cudaError_t launch_umma(const DenseLaunch &L) {
     using C = UmmaCfg<D>;
     auto kern = gqa_dense_umma_kernel<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     CUtensorMap tk, tv;
     if (!make_kv_tensor_map(&tk, L.k, L.args.B, L.args.Skv, L.args.Hkv, D, C::BN) ||
         !make_kv_tensor_map(&tv, L.v, L.args.B, L.args.Skv, L.args.Hkv, D, C::BN))

@@ -8,16 +8,13 @@
 
 namespace gqa {
 
+// The kernel's dynamic shared-memory limit is raised on each device by the
+// front end's occupancy query (once per device and instance, under its lock),
+// which every call makes before it launches.
 template <int D, int NT, int HB, int KVT, bool RANGE>
 static cudaError_t launch_paged_inst(const PagedArgs &a, cudaStream_t stream) {
     using C = PagedCfg<D, NT, HB, KVT != kKvBf16>;
     auto kern = gqa_paged_kernel<D, NT, HB, KVT, RANGE>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     // Programmatic dependent launch: the CTAs may be scheduled while the
     // previous kernel in the stream drains; they wait for it before reading.
     cudaLaunchConfig_t cfg = {};

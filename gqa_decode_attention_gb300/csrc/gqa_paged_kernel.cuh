@@ -83,6 +83,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // permute selector `sel` (result bytes 0 and 2; bytes 1 and 3 are
 // overwritten): one lop3 flips each code's sign bit (code + 128 in
 // [0, 255]) and sets the f16 exponent of 1024, giving code + 1152 exactly.
+// This is the "magic number" integer-to-floating-point conversion (an
+// integer written into the low mantissa bits of a float whose exponent makes
+// one mantissa unit worth 1, so the float equals a constant plus the integer;
+// H. S. Warren, "Hacker's Delight", chapter "Floating-Point"), here with the
+// constant 1024 + 128 left in and taken off later by sums, not per element.
 __device__ __forceinline__ uint32_t s8pair_biased(uint32_t a, uint32_t b, uint32_t sel) {
     const uint32_t x = prmt(a, b, sel);
     uint32_t r;

@@ -49,7 +49,15 @@
  *    other than GQA_ERR_CUDA nothing has been launched.
  *  - Device-detected problems (an index out of range in the paged path, a
  *    pipeline wait that exceeded its time limit) set a sticky device error
- *    word that gqa_device_status reads and clears.
+ *    word that gqa_device_status reads and clears.  After a wait that ran
+ *    out, the out and lse of that call are undefined (its kernels stop early
+ *    and what they leave unwritten may hold earlier contents).
+ *  - The library keeps, per device and for the life of the process, the
+ *    device addresses of its own device variables (the error word, the
+ *    allocation-free scratch), its memory pool and the kernels' raised
+ *    shared-memory limits.  Resetting a device's primary context
+ *    (cudaDeviceReset) invalidates them: do not call the library on that
+ *    device again in the same process.
  *  - scale <= 0 or NaN selects the default 1 / sqrt(D).
  *  - Hq must be a multiple of Hkv.
  */
@@ -192,8 +200,10 @@ size_t gqa_decode_dv_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, in
  *    with that device current; make that first call before any stream
  *    capture.
  *  - Every call on a device shares the one scratch array and it keeps the
- *    last call's contents.  Nothing in it needs to start at zero: every
- *    partial a call reads was written earlier in the same call.  Calls that
+ *    last call's contents.  Nothing in it needs to start at zero: in a call
+ *    that completes without a device error, every partial it reads was
+ *    written earlier in the same call (after a wait that ran out, out and lse
+ *    are undefined, as for every entry point).  Calls that
  *    may overlap on the GPU (different streams, or devices' work not ordered
  *    by the caller) race on the scratch: serialise them. */
 #define GQA_NOALLOC_SCRATCH_BYTES (32u << 20)
