@@ -106,6 +106,8 @@ def workload_dtype(cfg) -> str:
         return "bf16"
     if isinstance(cfg, gqa_inputs.PagedKVConfig) and cfg.kv_dtype == "int8":
         return "int8 kv, bf16 q/out, f16 mma"
+    if workload_kernel(cfg) == "gqa_paged_umma_kernel":
+        return "fp8_e4m3fn kv, bf16 q/out, e4m3 mma (q and p as two e4m3 terms)"
     return "fp8_e4m3fn kv, bf16 q/out, f16 mma"
 
 
@@ -114,7 +116,13 @@ def workload_kernel(cfg) -> str:
         import gqa_decode_attention_gb300 as gq
         eng = gq.gqa_decode_dense_engine(cfg.B, cfg.Sq, cfg.Skv, cfg.Hq, cfg.Hkv, cfg.D, cfg.dv)
         return "gqa_dense_umma_kernel" if eng == "tcgen05" else "gqa_dense_split_kernel"
-    return "gqa_paged_kernel"
+    import gqa_decode_attention_gb300 as gq
+    if isinstance(cfg, gqa_inputs.PagedKVConfig):
+        kvd = {"bf16": 0, "fp8": 1, "int8": 2}[cfg.kv_dtype]
+        eng = gq.gqa_decode_paged_engine(cfg.B, cfg.Sq, cfg.Hq, cfg.Hkv, cfg.D, kvd)
+    else:
+        eng = gq.gqa_decode_paged_engine(cfg.B, 1, cfg.Hq, cfg.Hkv, cfg.D, 1, topk_form=True)
+    return "gqa_paged_umma_kernel" if eng == "tcgen05" else "gqa_paged_kernel"
 
 
 def gbs(nbytes: float, ms: float) -> float:
@@ -236,7 +244,7 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv", "-lms", "200"],
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
             # The sampler's start-up (its first query of the device) disturbs a
             # step that overlaps it: let it write its first sample before the
@@ -355,25 +363,24 @@ def _copy_peak_gbs(dev) -> float:
     return best
 
 
-def _read_peak_gbs(dev) -> float:
-    """Read-only stream bandwidth of this run: a sum over 4 GiB of fp32
-    (bytes read / time, the result is 4 bytes), best of 5.  A decode kernel
-    only reads its K/V, so it is the denominator that matches its traffic;
-    the copy peak (read + write) is the one the benchmark configuration
-    quotes, and a read-only stream can exceed it."""
+def _read_peak_gbs(gq, dev) -> float:
+    """Read-only stream bandwidth of this run: the library's read-stream hook
+    over 4 GiB (bytes read / time), best of 5.  A decode kernel only reads its
+    K/V, so this is the denominator that matches its traffic; the copy peak
+    (read + write) is the one the benchmark configuration quotes, and a
+    read-only stream can exceed it."""
     import torch
-    n = 1 << 30
-    a = torch.ones(n, dtype=torch.float32, device=dev)
-    r = torch.empty((), dtype=torch.float32, device=dev)
+    a = torch.ones(1 << 30, dtype=torch.float32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
     best = 0.0
     for _ in range(6):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        torch.sum(a, dtype=torch.float32, out=r)
+        gq.gqa_debug_read_stream(a, sink)
         e1.record()
         torch.cuda.synchronize()
         best = max(best, gbs(a.numel() * a.element_size(), e0.elapsed_time(e1)))
-    del a, r
+    del a, sink
     torch.cuda.empty_cache()
     return best
 
@@ -546,7 +553,7 @@ def run_gqa(args) -> int:
     peak, peak_kind = measured_hbm_peak()
 
     copy_peak = _copy_peak_gbs(dev)
-    read_peak = _read_peak_gbs(dev)
+    read_peak = _read_peak_gbs(gq, dev)
     call, tensors, launches_per_call, splits = _make_call(gq, cfg, dev, seed_offset=rank)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_bytes = max(512 << 20, 4 * l2)

@@ -38,7 +38,8 @@ EXPORTS = [
     "gqa_decode_host", "gqa_decode_paged_fp8", "gqa_decode_paged_fp8_dev_scales", "gqa_decode_paged", "gqa_decode_paged_ex",
     "gqa_decode_paged_num_splits", "gqa_decode_paged_workspace_bytes", "gqa_decode_paged_dev_scales",
     "gqa_paged_gather_fp8", "gqa_fp8_e4m3fn_to_f32", "gqa_device_status", "gqa_set_wait_limit_ns",
-    "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events",
+    "gqa_debug_set_fault_mode", "gqa_debug_set_kernel_events", "gqa_debug_read_stream",
+    "gqa_decode_paged_engine", "gqa_debug_set_paged_engine",
 ]
 
 
@@ -112,6 +113,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_debug_set_fault_mode.argtypes = [i]
     lib.gqa_debug_set_kernel_events.restype = None
     lib.gqa_debug_set_kernel_events.argtypes = [vp, vp]
+    lib.gqa_decode_paged_engine.restype = i
+    lib.gqa_decode_paged_engine.argtypes = [i] * 7
+    lib.gqa_debug_set_paged_engine.restype = None
+    lib.gqa_debug_set_paged_engine.argtypes = [i]
+    lib.gqa_debug_read_stream.restype = st
+    lib.gqa_debug_read_stream.argtypes = [vp, sz, vp, vp]
     _lib_handle = lib
     return lib
 
@@ -433,6 +440,21 @@ def gqa_decode_paged(q, k_pool, v_pool, page_table, seq_lens, k_scale=1.0, v_sca
     return out, lse
 
 
+def gqa_decode_paged_engine(B, Sq, Hq, Hkv, D, kv_dtype=1, topk_form=False) -> str:
+    """Kernel engine a paged call of this shape runs: "mma.sync" or "tcgen05"
+    (topk_form: the sparse top-K form; else whole requests with kv_dtype 0
+    bf16, 1 FP8, 2 int8)."""
+    n = load_library().gqa_decode_paged_engine(B, Sq, Hq, Hkv, D, int(kv_dtype), 1 if topk_form else 0)
+    if n < 0:
+        raise GQAError(-n, "gqa_decode_paged_engine")
+    return ENGINES[n]
+
+
+def gqa_debug_set_paged_engine(mode: int):
+    """mode 1: every later paged call runs on the mma.sync engine; 0: by shape."""
+    load_library().gqa_debug_set_paged_engine(int(mode))
+
+
 def gqa_decode_paged_num_splits(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req) -> int:
     return load_library().gqa_decode_paged_num_splits(B, Sq, Hq, Hkv, D, kv_dtype, page_size, pages_per_req)
 
@@ -493,6 +515,17 @@ def gqa_debug_set_kernel_events(before=None, after=None):
         lib.gqa_debug_set_kernel_events(None, None)
     else:
         lib.gqa_debug_set_kernel_events(ctypes.c_void_p(before.cuda_event), ctypes.c_void_p(after.cuda_event))
+
+
+def gqa_debug_read_stream(buf, sink, stream=None):
+    """Measurement hook: reads every byte of the CUDA tensor `buf` once and
+    XORs its words into `sink` (a CUDA int32 tensor of one element)."""
+    lib = load_library()
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf: expected a contiguous CUDA tensor")
+    _need(sink, "sink", torch.int32, "cuda")
+    st = lib.gqa_debug_read_stream(_ptr(buf), buf.numel() * buf.element_size(), _ptr(sink), _stream(stream))
+    _check(st, "gqa_debug_read_stream")
 
 
 def gqa_status_string(status: int) -> str:

@@ -19,7 +19,8 @@ LIB = os.path.join(HERE, "libgqa_decode.so")
 
 SOURCES = ["gqa_api.cu", "gqa_dense_d64.cu", "gqa_dense_d128.cu", "gqa_dense_d256.cu", "gqa_dense_d192x128.cu",
            "gqa_paged.cu",
-           "gqa_paged_kv_fp8.cu", "gqa_paged_kv_bf16.cu", "gqa_paged_kv_int8.cu", "gqa_noalloc.cu"]
+           "gqa_paged_kv_fp8.cu", "gqa_paged_kv_bf16.cu", "gqa_paged_kv_int8.cu", "gqa_noalloc.cu",
+           "gqa_read_stream.cu", "gqa_paged_umma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

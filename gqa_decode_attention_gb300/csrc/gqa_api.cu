@@ -22,6 +22,7 @@ namespace {
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int> g_fault_mode{0};
+std::atomic<int> g_paged_engine{0};  // 0: by shape; 1: the mma.sync engine for every paged call
 std::atomic<cudaEvent_t> g_ev_before{nullptr};
 std::atomic<cudaEvent_t> g_ev_after{nullptr};
 
@@ -333,6 +334,12 @@ struct PagedShape {
     bool topk_form;  // the sparse top-K form (FP8, gated) rather than whole requests
 };
 
+// The paged engine a shape runs on: tcgen05 where the shape fits it (unless
+// the measurement hook asks for the mma.sync engine everywhere).
+bool paged_umma(const PagedShape &s) {
+    return g_paged_engine.load() == 0 && paged_shape_fits_umma(s.kvt == GQA_KV_FP8_E4M3FN, s.D, s.Hkv, s.Mq);
+}
+
 gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int page_size, int pages_per_req,
                           int num_pages, PagedShape *s) {
     if (B < 1 || Sq < 1 || Hq < 1 || Hkv < 1 || page_size < 1 || pages_per_req < 1 || num_pages < 1)
@@ -366,10 +373,17 @@ gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, i
 // Resident CTAs per SM of the paged instance serving shape s (cached).
 int paged_occupancy(int dev, const PagedShape &s) {
     static int cache[kMaxDevices][4][2][2][4];  // [dev][form][D][two n-tiles][log2 heads per CTA]
+    static int cache_umma[kMaxDevices][2][3];   // tcgen05 engine: [dev][whole-request form][rows 2 / 4 / 8]
     const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
     const int lh = hb == 1 ? 0 : hb == 2 ? 1 : hb == 4 ? 2 : 3;
     const int form = s.topk_form ? 3 : s.kvt;
     std::lock_guard<std::mutex> lk(g_mu);
+    if (paged_umma(s)) {
+        const int R = paged_umma_rows(s.Mq);
+        int &u = cache_umma[dev][s.topk_form ? 0 : 1][R == 2 ? 0 : R == 4 ? 1 : 2];
+        if (u == 0) u = paged_umma_ctas_per_sm(s.Mq, !s.topk_form);
+        return u;
+    }
     int &slot = cache[dev][form][s.D == 128][s.Mq > 8][lh];
     if (slot == 0) {
         PagedArgs a;
@@ -680,7 +694,7 @@ gqa_status run_paged_topk(const void *q, const void *gate, const uint8_t *k_pool
     }
     cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
     if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
-    cudaError_t pe = launch_paged_topk_fp8(a, D, cs);
+    cudaError_t pe = paged_umma(ps_) ? launch_paged_umma(a, false, cs) : launch_paged_topk_fp8(a, D, cs);
     if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
     if (pe == cudaSuccess && shared) pe = launch_paged_topk_combine_fp8(a, D, cs);
     if (ws != nullptr) cudaFreeAsync(ws, cs);
@@ -786,7 +800,8 @@ gqa_status run_paged_kv(const void *q, const void *k_pool, const void *v_pool, i
     a.err = error_word(dev);
     cudaEvent_t eb = g_ev_before.load(), ea = g_ev_after.load();
     if (eb != nullptr && ea != nullptr) cudaEventRecord(eb, cs);
-    cudaError_t e = s.kvt == GQA_KV_INT8        ? launch_paged_range_int8(a, D, cs)
+    cudaError_t e = paged_umma(s)                ? launch_paged_umma(a, true, cs)
+                    : s.kvt == GQA_KV_INT8        ? launch_paged_range_int8(a, D, cs)
                     : s.kvt == GQA_KV_FP8_E4M3FN ? launch_paged_range_fp8(a, D, cs)
                                                  : launch_paged_range_bf16(a, D, cs);
     if (eb != nullptr && ea != nullptr) cudaEventRecord(ea, cs);
@@ -904,6 +919,32 @@ gqa_status gqa_device_status(gqa_stream_t stream) {
 void gqa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns); }
 
 void gqa_debug_set_fault_mode(int mode) { g_fault_mode.store(mode); }
+
+int gqa_decode_paged_engine(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int topk_form) {
+    PagedShape s;
+    std::memset(&s, 0, sizeof(s));
+    if (topk_form) {
+        gqa_status st = check_paged(B, Hq, Hkv, D, 1, 1, 1, 0);
+        if (st != GQA_OK) return -int(st);
+        if (D == 256 || Hq / Hkv > 16) return -int(GQA_ERR_UNSUPPORTED);
+        s.B = B;
+        s.Sq = 1;
+        s.Hq = Hq;
+        s.Hkv = Hkv;
+        s.D = D;
+        s.G = Hq / Hkv;
+        s.Mq = s.G;
+        s.kvt = GQA_KV_FP8_E4M3FN;
+        s.kv8 = true;
+        s.topk_form = true;
+    } else {
+        gqa_status st = check_paged_kv(B, Sq, Hq, Hkv, D, kv_dtype, 1, 1, 1, &s);
+        if (st != GQA_OK) return -int(st);
+    }
+    return paged_umma(s) ? GQA_ENGINE_TCGEN05 : GQA_ENGINE_MMA_SYNC;
+}
+
+void gqa_debug_set_paged_engine(int mode) { g_paged_engine.store(mode == 1 ? 1 : 0); }
 
 void gqa_debug_set_kernel_events(void *before, void *after) {
     g_ev_before.store(static_cast<cudaEvent_t>(before));

@@ -177,6 +177,21 @@ int gqa_decode_dv_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, i
 #define GQA_ENGINE_TCGEN05 1
 int gqa_decode_dense_engine(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv);
 
+/* Which kernel engine a paged call of this shape runs: the sparse top-K form
+ * (gqa_decode_paged_fp8[_dev_scales]; topk_form != 0, kv_dtype and Sq
+ * ignored, Sq = 1) or the whole-request form (gqa_decode_paged[_ex,
+ * _dev_scales]; topk_form == 0).  GQA_ENGINE_TCGEN05 (bulk copies of whole
+ * token rows, E4M3 products on tcgen05 with scores and output in tensor
+ * memory) serves FP8 E4M3FN pools of head dim 128 with Hkv a multiple of 8
+ * and at most 8 query rows per KV head (Hq/Hkv * Sq <= 8);
+ * GQA_ENGINE_MMA_SYNC (bulk copies + mma.sync) serves every other shape.
+ * Both give the same results within the stated tolerances; the tcgen05
+ * engine represents the query rows and the softmax weights as sums of two
+ * E4M3 values (relative error near 2^-8 per weight; weights below about 2^-20
+ * of their row's running maximum are dropped).  Host-only: touches no device.
+ * Returns a negative gqa_status on invalid arguments. */
+int gqa_decode_paged_engine(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, int topk_form);
+
 /* Bytes of workspace gqa_decode_dv needs for `num_splits` (0 = automatic);
  * 0 when a single split is used or on invalid arguments. */
 size_t gqa_decode_dv_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv,

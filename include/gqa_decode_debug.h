@@ -8,6 +8,10 @@
 #ifndef GQA_DECODE_DEBUG_H
 #define GQA_DECODE_DEBUG_H
 
+#include <stddef.h>
+
+#include "gqa_decode.h"
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -33,6 +37,22 @@ void gqa_debug_set_fault_mode(int mode);
  * pass NULL, NULL to stop.  Recording between the split and the combine
  * kernel serialises the combine's early launch, so use it only to measure. */
 void gqa_debug_set_kernel_events(void *before, void *after);
+
+/* Measurement and test hook: mode 1 runs every later paged call on the
+ * mma.sync engine, even where gqa_decode_paged_engine reports tcgen05, so
+ * the two engines can be compared on the same shapes; mode 0 (default)
+ * chooses by shape.  Affects workspace sizes and worker counts computed
+ * afterwards as well; set it only between calls. */
+void gqa_debug_set_paged_engine(int mode);
+
+/* Measurement hook: reads `bytes` (a multiple of 16) of device memory at
+ * `buf` (16-byte aligned) once with 16-byte loads and XORs every 32-bit word
+ * into *sink (device memory, 4-byte aligned; the caller owns both).  The
+ * benchmark times it to report a read-only HBM rate beside the copy peak: a
+ * decode kernel only reads its K/V, so its traffic matches this stream, not a
+ * copy's read + write.  Asynchronous on `stream`; GQA_ERR_INVALID_ARG or
+ * GQA_ERR_ALIGNMENT before launching for bad arguments. */
+gqa_status gqa_debug_read_stream(const void *buf, size_t bytes, unsigned *sink, gqa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -111,6 +111,37 @@ def test_dense_engine_choice(lib):
     assert eng(1, 8, 100, 8, 2, 128, 192) == -2
 
 
+def test_paged_engine_choice(lib):
+    """Host-only: FP8 pools of head dim 128 with KV heads in blocks of 8 and at
+    most 8 query rows per KV head run on tcgen05 (both forms); every other
+    paged shape on mma.sync; the measurement hook forces mma.sync."""
+    eng = lib.gqa_decode_paged_engine
+    # whole requests: (B, Sq, Hq, Hkv, D, kv_dtype, topk_form)
+    assert eng(4, 1, 64, 8, 128, 1, 0) == 1         # FP8, 8 rows per KV head
+    assert eng(4, 2, 32, 8, 128, 1, 0) == 1         # 4 x 2 rows
+    assert eng(4, 1, 128, 16, 128, 1, 0) == 1       # two blocks of 8 KV heads
+    assert eng(4, 1, 8, 8, 128, 1, 0) == 1          # one row per KV head
+    assert eng(4, 2, 64, 8, 128, 1, 0) == 0         # 16 rows per KV head
+    assert eng(4, 1, 32, 4, 128, 1, 0) == 0         # 4 KV heads
+    assert eng(4, 1, 96, 12, 128, 1, 0) == 0        # 12 KV heads
+    assert eng(4, 1, 64, 8, 64, 1, 0) == 0          # head dim 64
+    assert eng(4, 1, 64, 8, 128, 0, 0) == 0         # bf16 pool
+    assert eng(4, 1, 64, 8, 128, 2, 0) == 0         # int8 pool
+    # top-K form (FP8, Sq = 1; kv_dtype ignored)
+    assert eng(256, 1, 32, 8, 128, 0, 1) == 1
+    assert eng(256, 1, 32, 4, 128, 0, 1) == 0
+    assert eng(256, 1, 128, 8, 128, 0, 1) == 0      # 16 rows per KV head
+    assert eng(4, 1, 6, 4, 128, 1, 0) == -1         # Hq % Hkv != 0
+    assert eng(4, 1, 64, 8, 96, 1, 0) == -2         # unsupported head size
+    lib.gqa_debug_set_paged_engine(1)
+    try:
+        assert eng(4, 1, 64, 8, 128, 1, 0) == 0
+        assert eng(256, 1, 32, 8, 128, 0, 1) == 0
+    finally:
+        lib.gqa_debug_set_paged_engine(0)
+    assert eng(4, 1, 64, 8, 128, 1, 0) == 1
+
+
 def test_engine_names_match_header():
     """The binding's engine names follow the header's GQA_ENGINE_* values."""
     text = open(os.path.join(ROOT, "include", "gqa_decode.h")).read()
