@@ -135,15 +135,29 @@ struct PagedUmmaCfg {
     // Separate K and V rings: a K stage is free once its scores are computed,
     // a V stage only after the block's softmax and output product, so the K
     // ring runs further ahead.  Depths fill two CTAs' shared memory per SM.
-    static constexpr int KST = R == 2 ? 4 : R == 4 ? 3 : 2;
-    static constexpr int VST = 2;
+#ifndef GQA_PAGED_UMMA_KST4
+#define GQA_PAGED_UMMA_KST4 2
+#endif
+#ifndef GQA_PAGED_UMMA_VST4
+#define GQA_PAGED_UMMA_VST4 3
+#endif
+    static constexpr int KST = R == 2 ? 3 : R == 4 ? GQA_PAGED_UMMA_KST4 : 2;
+    static constexpr int VST = R == 2 ? 3 : R == 4 ? GQA_PAGED_UMMA_VST4 : 2;
     static constexpr int Q_BYTES = N * 128;       // one E4M3 piece of Q' (N rows of 128 codes)
     static constexpr int P_BYTES = 128 * N;       // one E4M3 piece of P'^T (128 rows x N bytes)
     static constexpr int P_BUFS = R <= 4 ? 2 : 1;
     static constexpr int P_NBLK = 2048;           // P'^T: byte distance between 16-column blocks
     static constexpr float kPExp = 6.f;           // p = 2^kPExp exp2(x - m)
     static constexpr float kLazy = 2.75f;         // rescale once x exceeds m by more than this
-    static constexpr int NP = 2;                  // producer warps: K, then V
+    static constexpr int NP = 3;                  // producer warps: K, V, index map
+    static constexpr int IDX_SLOTS = 8;           // blocks of pool rows the index warp resolves ahead
+    // Token masks of the blocks, written by the index warp, read by the softmax.
+    // The index warp writes block j only after both copy warps read block
+    // j - IDX_SLOTS, and the V warp gets there only after the output product
+    // of block j - IDX_SLOTS - 1 - VST, i.e. after the softmax finished it: the
+    // index warp runs at most IDX_SLOTS + VST + 1 blocks ahead of the softmax,
+    // fewer than VM_SLOTS.
+    static constexpr int VM_SLOTS = 16;
     static constexpr int SW = 0;                  // first softmax warp (lane quarter = warp)
     static constexpr int ISSUER = 4;
     static constexpr int PW0 = 5;                 // first producer warp
@@ -155,17 +169,21 @@ struct PagedUmmaCfg {
     static constexpr int P_OFF = Q_OFF + 2 * Q_BYTES;
     static constexpr int BAR_OFF = P_OFF + P_BUFS * 2 * P_BYTES;
     // barriers: kfull[KST], kempty[KST], vfull[VST], vempty[VST], s_full[2], s_free[2],
-    // p_full[PB], pv_done[PB], q_full, o_free, fin
-    static constexpr int NBARS = 2 * KST + 2 * VST + 4 + 2 * P_BUFS + 3;
-    static constexpr int VMASK_OFF = BAR_OFF + NBARS * 8;           // u32 per K stage (valid tokens)
-    static constexpr int ALPHA_OFF = VMASK_OFF + KST * 4;           // float [N]
+    // p_full[PB], pv_done[PB], q_full, o_free, fin, idx_full[IDX_SLOTS], idx_empty[IDX_SLOTS],
+    // vm_full[VM_SLOTS]
+    static constexpr int NBARS = 2 * KST + 2 * VST + 4 + 2 * P_BUFS + 3 + 2 * IDX_SLOTS + VM_SLOTS;
+    static constexpr int VMASK_OFF = BAR_OFF + NBARS * 8;           // u32 per block slot (valid tokens)
+    static constexpr int ALPHA_OFF = VMASK_OFF + VM_SLOTS * 4;      // float [N]
     static constexpr int MREF_OFF = ALPHA_OFF + N * 4;              // float [N] reference maxima
     static constexpr int CORR_OFF = MREF_OFF + N * 4;               // float [N]
     static constexpr int XCH_OFF = CORR_OFF + N * 4;                // float [2][4][N] block maxima
     static constexpr int LSUM_OFF = XCH_OFF + 2 * 4 * N * 4;        // float [4][N]
     static constexpr int SCHED_OFF = (LSUM_OFF + 4 * N * 4 + 7) / 8 * 8;  // long [4]
     static constexpr int MISC_OFF = SCHED_OFF + 32;                 // tmem base, abort flag
-    static constexpr int SMEM_USED = MISC_OFF + 16;
+    static constexpr int IDX_OFF = MISC_OFF + 16;                   // int [IDX_SLOTS][BT] pool rows
+    static constexpr int COLB_OFF = (IDX_OFF + IDX_SLOTS * BT * 4 + 7) / 8 * 8;  // long long [N] output row offsets
+    static constexpr int COLF_OFF = COLB_OFF + N * 8;               // float [N] output factors
+    static constexpr int SMEM_USED = COLF_OFF + N * 4;
     static constexpr int SMEM_BYTES = SMEM_USED + 1024;             // + alignment slack
     // TMEM columns: two score buffers, then O_hi and O_lo
     static constexpr uint32_t S_COL = 0;
@@ -318,6 +336,40 @@ struct PagedSegWalk {
     }
 };
 
+// Block-by-block walk of the same sequence: the non-empty segments' 16-token
+// blocks in order; `blk` is the block within its segment and `ns` the index
+// of its segment among the non-empty ones.
+struct PagedBlockWalk {
+    PagedSegWalk w;
+    int blk, ns;
+    bool in_seg;
+    __device__ __forceinline__ void init(long wb, long we, int sb, long sp, bool last) {
+        w.init(wb, we, sb, sp, last);
+        in_seg = false;
+        blk = 0;
+        ns = -1;
+    }
+    template <bool RANGE>
+    __device__ __forceinline__ bool next(const PagedArgs &a) {
+        if (in_seg && blk + 1 < w.nblk) {
+            ++blk;
+            return true;
+        }
+        if (in_seg) w.advance();
+        while (w.next<RANGE>(a)) {
+            if (w.nblk > 0) {
+                in_seg = true;
+                blk = 0;
+                ++ns;
+                return true;
+            }
+            w.advance();
+        }
+        in_seg = false;
+        return false;
+    }
+};
+
 template <int R, bool RANGE>
 __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN_BLOCKS)
     gqa_paged_umma_kernel(const PagedArgs a) {
@@ -335,6 +387,12 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
     uint64_t *q_full = pv_done + C::P_BUFS;
     uint64_t *o_free = q_full + 1;
     uint64_t *fin = o_free + 1;
+    uint64_t *idx_full = fin + 1;              // [IDX_SLOTS]
+    uint64_t *idx_empty = idx_full + C::IDX_SLOTS;
+    uint64_t *vm_full = idx_empty + C::IDX_SLOTS;  // [VM_SLOTS]
+    int *idx_rows = reinterpret_cast<int *>(smem + C::IDX_OFF);
+    long long *col_base = reinterpret_cast<long long *>(smem + C::COLB_OFF);
+    float *col_f = reinterpret_cast<float *>(smem + C::COLF_OFF);
     uint32_t *vmask = reinterpret_cast<uint32_t *>(smem + C::VMASK_OFF);
     float *alpha_s = reinterpret_cast<float *>(smem + C::ALPHA_OFF);
     float *mref_s = reinterpret_cast<float *>(smem + C::MREF_OFF);
@@ -353,9 +411,7 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::KST; ++s) {
             mbar_init(&kfull[s], 1);
-            // released by the scores' commit and by every softmax thread once it has
-            // read the stage's token mask (which the next fill overwrites)
-            mbar_init(&kempty[s], 1 + 128);
+            mbar_init(&kempty[s], 1);  // the scores' commit
         }
         for (int s = 0; s < C::VST; ++s) {
             mbar_init(&vfull[s], 1);
@@ -363,15 +419,20 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
-            mbar_init(&s_free[s], 128);
+            mbar_init(&s_free[s], 4);  // one arrival per softmax warp
         }
         for (int s = 0; s < C::P_BUFS; ++s) {
-            mbar_init(&p_full[s], 128);
+            mbar_init(&p_full[s], 4);
             mbar_init(&pv_done[s], 1);
         }
         mbar_init(q_full, 1);
-        mbar_init(o_free, 128);
+        mbar_init(o_free, 4);
         mbar_init(fin, 1);
+        for (int s = 0; s < C::IDX_SLOTS; ++s) {
+            mbar_init(&idx_full[s], 1);
+            mbar_init(&idx_empty[s], 2);  // the K and the V producer
+        }
+        for (int s = 0; s < C::VM_SLOTS; ++s) mbar_init(&vm_full[s], 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -393,8 +454,81 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
     const bool last_worker = int(blockIdx.y) == a.num_splits - 1;
     const size_t row_bytes = size_t(a.Hkv) * C::D;
 
+    if (warp == C::PW0 + 2) {
+        // ============================================================ index map
+        // Pool rows of the coming blocks into a ring of IDX_SLOTS blocks, four
+        // blocks per round: every lane loads its two tokens' list entries (top-K
+        // form) and page-table entries together, so a round costs two memory
+        // latencies whatever its size, and the copy warps never wait on them.
+        PagedSegWalk w;
+        w.init(w_begin, w_end, seg_b, seg_p, last_worker);
+        bool failed = false;
+        int j = 0;
+        while (!failed && w.next<RANGE>(a)) {
+            for (int b0 = 0; b0 < w.nblk && !failed; b0 += 4) {
+                const int nb = min(4, w.nblk - b0);
+                int tk[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = b0 * C::BT + lane + 32 * e;  // token of the segment
+                    const bool in = k < (b0 + nb) * C::BT && k < w.n_tok;
+                    if constexpr (RANGE)
+                        tk[e] = in ? w.t_begin + k : -1;
+                    else
+                        tk[e] = in ? __ldg(a.topk + size_t(w.b) * a.topk_n + w.t_begin + k) : -1;
+                }
+                int rw[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    bool bad = false;
+                    rw[e] = paged_token_row(a.page_table, w.b, a.pages_per_req, a.page_size, a.num_pages, tk[e], &bad);
+                    if (bad) w.bad = true;
+                }
+                for (int q = 0; q < nb; ++q) {
+                    const int jj = j + q;
+                    if (jj < C::IDX_SLOTS) continue;
+                    bool ok = true;
+                    if (lane == 0)
+                        ok = mbar_wait_bounded(&idx_empty[jj % C::IDX_SLOTS], ((jj / C::IDX_SLOTS) - 1) & 1,
+                                               a.wait_limit_ns, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        failed = true;
+                        break;
+                    }
+                }
+                if (failed) break;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int q = (lane >> 4) + 2 * e;  // block of the round holding this token
+                    if (q < nb) idx_rows[((j + q) % C::IDX_SLOTS) * C::BT + (lane & 15)] = rw[e];
+                }
+                // token masks: bit i of block q = token i has a row
+                const unsigned b0m = __ballot_sync(0xffffffffu, rw[0] >= 0);  // blocks 0, 1 of the round
+                const unsigned b1m = __ballot_sync(0xffffffffu, rw[1] >= 0);  // blocks 2, 3
+                if (lane < nb) {
+                    const unsigned wm = lane < 2 ? b0m : b1m;
+                    vmask[(j + lane) % C::VM_SLOTS] = (lane & 1) ? (wm >> 16) : (wm & 0xffffu);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    for (int q = 0; q < nb; ++q) {
+                        mbar_arrive(&idx_full[(j + q) % C::IDX_SLOTS]);
+                        mbar_arrive(&vm_full[(j + q) % C::VM_SLOTS]);
+                    }
+                j += nb;
+            }
+            w.advance();
+        }
+        if (failed) {
+            if (lane == 0) flag_error(a.err, kErrTimeout);
+            *abort_flag = 1;
+        }
+        if (w.bad && lane == 0) flag_error(a.err, kErrIndex);
+        return;
+    }
+
     if (warp >= C::PW0) {
-        // ============================================================ producers
+        // ============================================================ copy warps
         // Warp PW0 copies K, warp PW0 + 1 copies V, each into its own ring:
         // lane i < 16 one copy of token i's row piece, or lane 0 one copy of
         // the whole block when its 16 rows are consecutive pool rows of full
@@ -413,26 +547,21 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
         bool failed = false;
         int jb = 0;      // global block index of this CTA
         int issued = 0;  // blocks issued so far
-        // the pool row of this lane's token in block `blk` of segment sg (-1: none)
-        auto resolve = [&](const PagedSegWalk &sg, int blk) -> int {
-            const int k = blk * C::BT + lane;
-            if (!copier || k >= sg.n_tok) return -1;
-            int t;
-            if constexpr (RANGE)
-                t = sg.t_begin + k;
-            else
-                t = __ldg(a.topk + size_t(sg.b) * a.topk_n + sg.t_begin + k);
-            bool bad = false;
-            const int row = paged_token_row(a.page_table, sg.b, a.pages_per_req, a.page_size, a.num_pages, t, &bad);
-            if (bad) w.bad = true;
-            return row;
-        };
         while (!failed && w.next<RANGE>(a)) {
-            int row = w.nblk > 0 ? resolve(w, 0) : -1;
             for (int blk = 0; blk < w.nblk; ++blk, ++jb) {
+                // this block's rows from the index warp
+                const int slot = jb % C::IDX_SLOTS;
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(&idx_full[slot], (jb / C::IDX_SLOTS) & 1, a.wait_limit_ns, abort_flag);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    failed = true;
+                    break;
+                }
+                const int row = copier ? idx_rows[slot * C::BT + lane] : -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&idx_empty[slot]);
                 const int st = jb % nst;
                 if (jb >= nst) {
-                    bool ok = true;
                     if (lane == 0) ok = mbar_wait_bounded(&emptyb[st], ((jb / nst) - 1) & 1, a.wait_limit_ns, abort_flag);
                     if (!__shfl_sync(0xffffffffu, ok, 0)) {
                         failed = true;
@@ -445,24 +574,18 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                     whole_rows && __ballot_sync(0xffffffffu, copier && row >= 0 && row == r0 + lane) == 0xffffu;
                 issued = jb + 1;
                 const uint32_t dst = base + uint32_t(st * C::KV_BYTES);
-                if (lane == 0) {
-                    if (!is_v) vmask[st] = valid;
-                    mbar_arrive_expect_tx(&fullb[st], uint32_t(__popc(valid)) * C::PIECE);
-                }
+                if (lane == 0) mbar_arrive_expect_tx(&fullb[st], uint32_t(__popc(valid)) * C::PIECE);
                 __syncwarp();
                 // Test hook: the first stage's bytes are expected but never copied, so
                 // the stage never completes (the barrier phases stay exact).
                 if (!(a.fault_mode == 1 && jb == 0 && valid != 0u)) {
                     if (contig) {
-                        if (lane == 0)
-                            bulk_load(dst, pool + size_t(r0) * row_bytes, C::KV_BYTES, &fullb[st]);
+                        if (lane == 0) bulk_load(dst, pool + size_t(r0) * row_bytes, C::KV_BYTES, &fullb[st]);
                     } else if (row >= 0) {
                         bulk_load(dst + uint32_t(lane * C::PIECE), pool + size_t(row) * row_bytes, C::PIECE,
                                   &fullb[st]);
                     }
                 }
-                // the next block's rows, while this stage is in flight
-                row = blk + 1 < w.nblk ? resolve(w, blk + 1) : -1;
             }
             w.advance();
         }
@@ -470,7 +593,6 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
             if (lane == 0) flag_error(a.err, kErrTimeout);
             *abort_flag = 1;
         }
-        if (w.bad && !is_v) flag_error(a.err, kErrIndex);
         // Every copy this warp issued lands before the CTA's shared memory is
         // released.  (Each issued block arrived once on its stage, so the last
         // nst blocks are exactly the fills that can still be in flight.)
@@ -493,47 +615,26 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
             const uint32_t vring = smem_u32(smem + C::V_OFF);
             const uint32_t qaddr = smem_u32(smem + C::Q_OFF);
             const uint32_t paddr = smem_u32(smem + C::P_OFF);
-            PagedSegWalk w;
-            w.init(w_begin, w_end, seg_b, seg_p, last_worker);
+            // Two walks over the same blocks: the next score product QK(qj) and the
+            // next output product PV(pj < qj).  Whichever is ready is issued, so an
+            // output product never waits on a later block's copies and a score
+            // product never waits on an earlier block's softmax.
+            PagedBlockWalk qw, pw;
+            qw.init(w_begin, w_end, seg_b, seg_p, last_worker);
+            pw.init(w_begin, w_end, seg_b, seg_p, last_worker);
+            bool q_has = qw.next<RANGE>(a);
+            if (q_has) pw.next<RANGE>(a);
+            int qj = 0, pj = 0;
             bool ok = true;
-            int jb = 0;
-            int ns = 0;  // non-empty segments begun
-            // the block whose PV is still to be issued
-            int pv_jb = -1, pv_ns = 0;
-            bool pv_first = false;
-            auto issue_pv = [&]() -> bool {
-                const int pb = pv_jb % C::P_BUFS;
-                if (!mbar_wait_bounded(&p_full[pb], (pv_jb / C::P_BUFS) & 1, a.wait_limit_ns, abort_flag)) return false;
-                // a segment's first PV overwrites O: the previous segment's epilogue has read it
-                if (pv_first && pv_ns > 0 &&
-                    !mbar_wait_bounded(o_free, (pv_ns - 1) & 1, a.wait_limit_ns, abort_flag))
-                    return false;
-                const int vs = pv_jb % C::VST;
-                if (!mbar_wait_bounded(&vfull[vs], (pv_jb / C::VST) & 1, a.wait_limit_ns, abort_flag)) return false;
-                tc_fence_after_sync();
-                const uint32_t vaddr = vring + vs * C::KV_BYTES;
-                const uint32_t pbase = paddr + pb * 2 * C::P_BYTES;
-#pragma unroll
-                for (int piece = 0; piece < 2; ++piece)
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {  // 32 (token, head) rows per step
-                        const uint64_t ad = smem_desc_sw128(vaddr + kk * 4096, 1024, 1024);
-                        const uint64_t bd = smem_desc_plain(pbase + piece * C::P_BYTES + kk * 512, 128, C::P_NBLK);
-                        umma_e4m3(tbase + (piece ? C::OL_COL : C::OH_COL), ad, bd, idesc_pv,
-                                  (pv_first && kk == 0) ? 0u : 1u);
-                    }
-                umma_commit(&pv_done[pb]);
-                umma_commit(&vempty[vs]);
-                return true;
-            };
-            while (ok && w.next<RANGE>(a)) {
-                if (w.nblk > 0) {
-                    ok = mbar_wait_bounded(q_full, ns & 1, a.wait_limit_ns, abort_flag);  // Q' of this segment
-                    for (int blk = 0; ok && blk < w.nblk; ++blk, ++jb) {
-                        const int ks = jb % C::KST;
-                        ok = mbar_wait_bounded(&kfull[ks], (jb / C::KST) & 1, a.wait_limit_ns, abort_flag);
-                        if (ok && jb >= 2) ok = mbar_wait_bounded(&s_free[jb & 1], ((jb - 2) >> 1) & 1, a.wait_limit_ns, abort_flag);
-                        if (!ok) break;
+            uint64_t t_last = globaltimer_ns();
+            uint32_t idle = 0;
+            while (ok && (q_has || pj < qj)) {
+                bool prog = false;
+                if (q_has) {
+                    const int ks = qj % C::KST;
+                    if ((qw.blk != 0 || mbar_test_wait(q_full, qw.ns & 1)) &&
+                        mbar_test_wait(&kfull[ks], (qj / C::KST) & 1) &&
+                        (qj < 2 || mbar_test_wait(&s_free[qj & 1], ((qj - 2) >> 1) & 1))) {
                         tc_fence_after_sync();
                         const uint32_t kaddr = kring + ks * C::KV_BYTES;
 #pragma unroll
@@ -542,24 +643,58 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                             for (int kk = 0; kk < 4; ++kk) {  // 32 codes per step
                                 const uint64_t ad = smem_desc_sw128(kaddr + kk * 32, 16, 1024);
                                 const uint64_t bd = smem_desc_sw128(qaddr + piece * C::Q_BYTES + kk * 32, 16, 1024);
-                                umma_e4m3(tbase + C::S_COL + (jb & 1) * C::N, ad, bd, idesc_qk,
+                                umma_e4m3(tbase + C::S_COL + (qj & 1) * C::N, ad, bd, idesc_qk,
                                           (piece | kk) ? 1u : 0u);
                             }
-                        umma_commit(&s_full[jb & 1]);
+                        umma_commit(&s_full[qj & 1]);
                         umma_commit(&kempty[ks]);
-                        if (pv_jb >= 0 && !issue_pv()) {
-                            ok = false;
-                            break;
-                        }
-                        pv_jb = jb;
-                        pv_first = blk == 0;
-                        pv_ns = ns;
+                        ++qj;
+                        q_has = qw.next<RANGE>(a);
+                        prog = true;
                     }
-                    ++ns;
                 }
-                w.advance();
+                if (pj < qj) {
+                    const int pb = pj % C::P_BUFS, vs = pj % C::VST;
+                    const bool first = pw.blk == 0;
+                    // a segment's first PV overwrites O: the previous segment's epilogue has read it
+                    if (mbar_test_wait(&p_full[pb], (pj / C::P_BUFS) & 1) &&
+                        mbar_test_wait(&vfull[vs], (pj / C::VST) & 1) &&
+                        (!first || pw.ns == 0 || mbar_test_wait(o_free, (pw.ns - 1) & 1))) {
+                        tc_fence_after_sync();
+                        const uint32_t vaddr = vring + vs * C::KV_BYTES;
+                        const uint32_t pbase = paddr + pb * 2 * C::P_BYTES;
+#pragma unroll
+                        for (int piece = 0; piece < 2; ++piece)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {  // 32 (token, head) rows per step
+                                const uint64_t ad = smem_desc_sw128(vaddr + kk * 4096, 1024, 1024);
+                                const uint64_t bd =
+                                    smem_desc_plain(pbase + piece * C::P_BYTES + kk * 512, 128, C::P_NBLK);
+                                umma_e4m3(tbase + (piece ? C::OL_COL : C::OH_COL), ad, bd, idesc_pv,
+                                          (first && kk == 0) ? 0u : 1u);
+                            }
+                        umma_commit(&pv_done[pb]);
+                        umma_commit(&vempty[vs]);
+                        ++pj;
+                        if (pj < qj || q_has) pw.next<RANGE>(a);
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    t_last = globaltimer_ns();
+                    idle = 0;
+                } else {
+                    // nothing ready: sleep in the barrier instruction (a bounded
+                    // suspension) instead of polling, to leave issue slots to the
+                    // softmax warp that shares this sub-partition
+                    if (pj < qj)
+                        mbar_try_wait_for(&p_full[pj % C::P_BUFS], (pj / C::P_BUFS) & 1, 100);
+                    else if (q_has)
+                        mbar_try_wait_for(&kfull[qj % C::KST], (qj / C::KST) & 1, 100);
+                    if ((++idle & 15u) == 0u && (*abort_flag || globaltimer_ns() - t_last > a.wait_limit_ns))
+                        ok = false;
+                }
             }
-            if (ok && pv_jb >= 0) ok = issue_pv();
             if (!ok) {
                 flag_error(a.err, kErrTimeout);
                 *abort_flag = 1;
@@ -680,13 +815,23 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                 l[r] = 0.f;
                 kmax[r] = r < a.Mq ? w.seq_len - a.Sq + r / a.G : -1;
             }
-            if (m < C::N) mref_s[m] = -INFINITY;
+            if (m < C::N) {
+                mref_s[m] = -INFINITY;
+                // where column (g', r) goes: its output row, or its partial row; -1 for padding rows
+                const int gq = m / R, r = m % R;
+                long long base = -1;
+                if (r < a.Mq) {
+                    const int i = r / a.G;
+                    const int h = (hb0 + gq) * a.G + r % a.G;
+                    base = w.complete ? ((long long)(w.b) * a.Sq + i) * a.Hq + h
+                                      : (((long long)(hb) * a.num_splits + blockIdx.y) * 2 + w.slot) * C::HB * a.Mq +
+                                            gq * a.Mq + r;
+                }
+                col_base[m] = base;
+            }
             for (int blk = 0; blk < w.nblk; ++blk, ++jb) {
-                const int ks = jb % C::KST;
-                // the scores first: their K stage has landed, and it cannot be refilled
-                // before this thread releases it below (so the parity wait is exact)
                 wait(&s_full[jb & 1], (jb >> 1) & 1);
-                wait(&kfull[ks], (jb / C::KST) & 1);
+                wait(&vm_full[jb % C::VM_SLOTS], (jb / C::VM_SLOTS) & 1);  // the block's token mask
                 // this lane's scores: columns g R .. g R + R - 1 of the N
                 float s[R];
 #pragma unroll
@@ -734,13 +879,20 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                     }
                 }
                 tc_fence_before_sync();
+                __syncwarp();
                 // a warp that gave up stops arriving anywhere: spurious phases would
                 // let the other roles reuse buffers that are still in flight
-                if (!failed) mbar_arrive(&s_free[jb & 1]);
+                if (!failed && lane == 0) mbar_arrive(&s_free[jb & 1]);
 
-                const uint32_t vm = failed ? 0u : vmask[ks];
+                if (blk == 0 && RANGE == false && a.gate != nullptr && w.complete && m < C::HB * R * 2) {
+                    // the segment's gate rows (read by its epilogue), into L2: 2 lines per row
+                    const int n = m >> 1, gq = n / R, r = n % R;
+                    if (r < a.Mq)
+                        prefetch_l2(a.gate + (((size_t)w.b * a.Sq + r / a.G) * a.Hq + (hb0 + gq) * a.G + r % a.G) * C::D +
+                                    (m & 1) * 64);
+                }
+                const uint32_t vm = failed ? 0u : vmask[jb % C::VM_SLOTS];
                 const bool tvalid = (vm >> t) & 1u;
-                if (!failed) mbar_arrive(&kempty[ks]);
                 const int tokn = w.t_begin + blk * C::BT + t;  // token (list entry) of the request
                 float x[R];
                 bool need = false;
@@ -861,7 +1013,8 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                 }
                 fence_proxy_async_shared();
                 tc_fence_before_sync();
-                if (!failed) mbar_arrive(&p_full[pb]);
+                __syncwarp();
+                if (!failed && lane == 0) mbar_arrive(&p_full[pb]);
 
                 // last block: Q' of the next non-empty segment (this segment's scores
                 // are all computed), so its first QK overlaps this epilogue
@@ -875,6 +1028,24 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                 if (!failed) tc_fence_after_sync();
             }
             const bool dead = softmax_bar_any(failed);  // no output from a CTA that gave up
+            // The gate values of this lane's outputs first (top-K form): their
+            // latency then overlaps the reductions below.
+            // (Only the top-K form has a gate; two bf16 values per register.)
+            const __nv_bfloat16 *__restrict__ gatep = a.gate;
+            uint32_t graw[RANGE ? 1 : C::N / 2];
+            const bool gated = !RANGE && gatep != nullptr && w.complete && !dead;
+            if constexpr (!RANGE) {
+                if (gated) {
+#pragma unroll
+                    for (int n = 0; n < C::N; n += 2) {
+                        const long long r0 = col_base[n], r1 = col_base[n + 1];
+                        const int d = 16 * ((m >> 4) ^ (n / R)) + (m & 15);  // columns n, n + 1: same head
+                        const uint32_t g0 = r0 >= 0 ? __bfloat16_as_ushort(gatep[r0 * C::D + d]) : 0u;
+                        const uint32_t g1 = r1 >= 0 ? __bfloat16_as_ushort(gatep[r1 * C::D + d]) : 0u;
+                        graw[n / 2] = g0 | (g1 << 16);
+                    }
+                }
+            }
             // row sums of the 16 lanes of each head
             float *ls = lsum + warp * C::N;
 #pragma unroll
@@ -885,8 +1056,33 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                 if (lane < 8) ls[g * R + r] = v;
             }
             softmax_bar();
+            // per column (g', r) once: the normaliser and the LSE
+            if (m < C::N && !dead) {
+                const int gq = m / R;
+                const long long base = col_base[m];
+                float f = 0.f;
+                if (base >= 0) {
+                    const float L = lsum[m] + lsum[C::N + m] + lsum[2 * C::N + m] + lsum[3 * C::N + m];
+                    float vs = a.v_scale;
+                    if (a.v_scales != nullptr) vs *= __ldg(a.v_scales + (a.n_scales > 1 ? hb0 + gq : 0));
+                    f = L > 0.f ? vs / L : 0.f;
+                    const float lse2 = L > 0.f ? mref_s[m] - C::kPExp + log2f(L) : -INFINITY;
+                    if (w.complete) {
+                        if (a.lse != nullptr) {
+                            const int r = m % R, i = r / a.G, h = (hb0 + gq) * a.G + r % a.G;
+                            a.lse[((size_t)w.b * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
+                        }
+                    } else {
+                        a.lse_part[base] = lse2;
+                    }
+                }
+                col_f[m] = f;
+            }
+            softmax_bar();
             // lane m holds output dimension d = 16 ((m / 16) ^ g') + m % 16 of head g'
             // in every column (g', r) of O^T
+            __nv_bfloat16 *__restrict__ outp = a.out;
+            float *__restrict__ opart = a.o_part;
 #pragma unroll
             for (int c0 = 0; c0 < C::N; c0 += 16) {
                 uint32_t oh[16], ol[16];
@@ -897,41 +1093,33 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                     tmem_ld16(lane_base + C::OL_COL + c0, ol);
                     tmem_wait_ld();
                 }
+                if (dead) continue;
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int n = c0 + e;
-                    const int gq = n / R, r = n % R;
-                    if (dead || r >= a.Mq) continue;
-                    const float L = lsum[n] + lsum[C::N + n] + lsum[2 * C::N + n] + lsum[3 * C::N + n];
-                    const float o = __uint_as_float(oh[e]) + 0.0625f * __uint_as_float(ol[e]);
-                    const int d = 16 * ((m >> 4) ^ gq) + (m & 15);
-                    const int i = r / a.G;
-                    const int h = (hb0 + gq) * a.G + r % a.G;
-                    float vs = a.v_scale;
-                    if (a.v_scales != nullptr) vs *= __ldg(a.v_scales + (a.n_scales > 1 ? hb0 + gq : 0));
-                    const float f = L > 0.f ? vs / L : 0.f;
-                    const float lse2 = L > 0.f ? mref_s[n] - C::kPExp + log2f(L) : -INFINITY;
-                    if (!w.complete) {
-                        const size_t prow =
-                            ((((size_t(hb) * a.num_splits + blockIdx.y) * 2 + w.slot) * C::HB + gq) * a.Mq) + r;
-                        a.o_part[prow * C::D + d] = o * f;
-                        if (d == 0) a.lse_part[prow] = lse2;
-                        continue;
+                    const long long rb = col_base[n];
+                    if (rb < 0) continue;
+                    const int d = 16 * ((m >> 4) ^ (n / R)) + (m & 15);
+                    const float o = (__uint_as_float(oh[e]) + 0.0625f * __uint_as_float(ol[e])) * col_f[n];
+                    if (w.complete) {
+                        float gsig = 1.f;
+                        if constexpr (!RANGE) {
+                            if (gated) {
+                                const uint32_t gw = graw[n / 2];
+                                const float gv = __uint_as_float((n & 1) ? (gw & 0xffff0000u) : (gw << 16));
+                                gsig = __fdividef(1.f, 1.f + __expf(-gv));
+                            }
+                        }
+                        outp[rb * C::D + d] = __float2bfloat16_rn(o * gsig);
+                    } else {
+                        opart[rb * C::D + d] = o;
                     }
-                    const size_t off = ((size_t(w.b) * a.Sq + i) * a.Hq + h) * C::D + d;
-                    float val = o * f;
-                    if (a.gate != nullptr) {
-                        const float gv = __bfloat162float(a.gate[off]);
-                        val *= __fdividef(1.f, 1.f + __expf(-gv));
-                    }
-                    a.out[off] = __float2bfloat16_rn(val);
-                    if (a.lse != nullptr && d == 0)
-                        a.lse[(size_t(w.b) * a.Hq + h) * a.Sq + i] = lse2 * 0.69314718055994530942f;
                 }
             }
             if (nonempty && !failed) {
                 tc_fence_before_sync();
-                mbar_arrive(o_free);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
             }
             softmax_bar();  // lsum and mref_s are reused by the next segment
             w.advance();
