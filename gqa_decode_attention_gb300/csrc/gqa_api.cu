@@ -373,14 +373,14 @@ gqa_status check_paged_kv(int B, int Sq, int Hq, int Hkv, int D, int kv_dtype, i
 // Resident CTAs per SM of the paged instance serving shape s (cached).
 int paged_occupancy(int dev, const PagedShape &s) {
     static int cache[kMaxDevices][4][2][2][4];  // [dev][form][D][two n-tiles][log2 heads per CTA]
-    static int cache_umma[kMaxDevices][2][3];   // tcgen05 engine: [dev][whole-request form][rows 2 / 4 / 8]
+    static int cache_umma[kMaxDevices][2][2];   // tcgen05 engine: [dev][whole-request form][rows 2 / 4]
     const int hb = paged_heads_per_cta(s.D, s.kv8, s.Mq, s.Hkv);
     const int lh = hb == 1 ? 0 : hb == 2 ? 1 : hb == 4 ? 2 : 3;
     const int form = s.topk_form ? 3 : s.kvt;
     std::lock_guard<std::mutex> lk(g_mu);
     if (paged_umma(s)) {
         const int R = paged_umma_rows(s.Mq);
-        int &u = cache_umma[dev][s.topk_form ? 0 : 1][R == 2 ? 0 : R == 4 ? 1 : 2];
+        int &u = cache_umma[dev][s.topk_form ? 0 : 1][R == 2 ? 0 : 1];
         if (u == 0) u = paged_umma_ctas_per_sm(s.Mq, !s.topk_form);
         return u;
     }
@@ -403,7 +403,7 @@ int paged_occupancy(int dev, const PagedShape &s) {
 // at least one.  The top-K form (equal lists) uses one worker per request as
 // soon as the requests fill half the slots: a request then never straddles
 // two workers and no merge pass is needed, which costs less than the idle
-// slots it leaves.
+// slots it leaves (measured on both engines).
 int choose_paged_workers(const PagedShape &s, int requested, int dev) {
     long W;
     if (requested > 0) {
@@ -916,7 +916,10 @@ gqa_status gqa_device_status(gqa_stream_t stream) {
     return GQA_OK;
 }
 
-void gqa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns); }
+void gqa_set_wait_limit_ns(uint64_t ns) {
+    constexpr uint64_t kMinWaitLimitNs = 1000000ull;
+    g_wait_limit_ns.store(ns == 0 ? kDefaultWaitLimitNs : ns < kMinWaitLimitNs ? kMinWaitLimitNs : ns);
+}
 
 void gqa_debug_set_fault_mode(int mode) { g_fault_mode.store(mode); }
 

@@ -98,15 +98,18 @@ inline int paged_heads_per_cta(int D, bool kv8, int Mq, int Hkv) {
 }
 // The paged kernels' tcgen05 engine (gqa_paged_umma.cuh) serves FP8 pools of
 // head dim 128 whose KV heads come in blocks of 8 (one 1 KiB row piece per
-// token) with at most 8 query rows per KV head, in both the top-K and the
-// whole-request form; other shapes run on the mma.sync engine.  Both engines
-// use 8 heads per CTA for these shapes, so the schedule, the partials and the
-// merge pass are the same.
+// token) with at most 4 query rows per KV head, in both the top-K and the
+// whole-request form; other shapes run on the mma.sync engine.  (Measured on
+// GB300: with 1-4 rows per KV head the tcgen05 engine is 3-16 % faster; with
+// 8 rows, where two CTAs per SM leave room for only a single P buffer and
+// two-stage rings, it was 4-60 % slower, so that shape stays on mma.sync.)
+// Both engines use 8 heads per CTA for these shapes, so the schedule, the
+// partials and the merge pass are the same.
 inline bool paged_shape_fits_umma(bool fp8, int D, int Hkv, int Mq) {
-    return fp8 && D == 128 && Hkv % 8 == 0 && Mq <= 8;
+    return fp8 && D == 128 && Hkv % 8 == 0 && Mq <= 4;
 }
-// Query rows per KV head of the instance: Mq rounded up to 2, 4 or 8.
-inline int paged_umma_rows(int Mq) { return Mq <= 2 ? 2 : Mq <= 4 ? 4 : 8; }
+// Query rows per KV head of the instance: Mq rounded up to 2 or 4.
+inline int paged_umma_rows(int Mq) { return Mq <= 2 ? 2 : 4; }
 cudaError_t launch_paged_umma(const PagedArgs &a, bool range, cudaStream_t stream);
 // Resident CTAs per SM (also raises the dynamic shared-memory limit on the
 // current device); 0 on error.

@@ -1,5 +1,5 @@
 // gqa_paged_umma.cu -- launchers of the paged decode on tcgen05 (FP8 pools,
-// head dim 128, multiples of 8 KV heads, up to 8 query rows per KV head), for
+// head dim 128, multiples of 8 KV heads, up to 4 query rows per KV head), for
 // the sparse top-K form and the whole-request form.
 #include "gqa_launch.h"
 #include "gqa_paged_umma.cuh"
@@ -63,16 +63,14 @@ int occupancy_inst() {
 
 cudaError_t launch_paged_umma(const PagedArgs &a, bool range, cudaStream_t stream) {
     const int R = paged_umma_rows(a.Mq);
-    if (range) return R == 2 ? launch_inst<2, true>(a, stream) : R == 4 ? launch_inst<4, true>(a, stream)
-                                                                        : launch_inst<8, true>(a, stream);
-    return R == 2 ? launch_inst<2, false>(a, stream) : R == 4 ? launch_inst<4, false>(a, stream)
-                                                              : launch_inst<8, false>(a, stream);
+    if (range) return R == 2 ? launch_inst<2, true>(a, stream) : launch_inst<4, true>(a, stream);
+    return R == 2 ? launch_inst<2, false>(a, stream) : launch_inst<4, false>(a, stream);
 }
 
 int paged_umma_ctas_per_sm(int Mq, bool range) {
     const int R = paged_umma_rows(Mq);
-    if (range) return R == 2 ? occupancy_inst<2, true>() : R == 4 ? occupancy_inst<4, true>() : occupancy_inst<8, true>();
-    return R == 2 ? occupancy_inst<2, false>() : R == 4 ? occupancy_inst<4, false>() : occupancy_inst<8, false>();
+    if (range) return R == 2 ? occupancy_inst<2, true>() : occupancy_inst<4, true>();
+    return R == 2 ? occupancy_inst<2, false>() : occupancy_inst<4, false>();
 }
 
 }  // namespace gqa

@@ -183,7 +183,7 @@ int gqa_decode_dense_engine(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, in
  * _dev_scales]; topk_form == 0).  GQA_ENGINE_TCGEN05 (bulk copies of whole
  * token rows, E4M3 products on tcgen05 with scores and output in tensor
  * memory) serves FP8 E4M3FN pools of head dim 128 with Hkv a multiple of 8
- * and at most 8 query rows per KV head (Hq/Hkv * Sq <= 8);
+ * and at most 4 query rows per KV head (Hq/Hkv * Sq <= 4);
  * GQA_ENGINE_MMA_SYNC (bulk copies + mma.sync) serves every other shape.
  * Both give the same results within the stated tolerances; the tcgen05
  * engine represents the query rows and the softmax weights as sums of two
@@ -396,8 +396,10 @@ gqa_status gqa_device_status(gqa_stream_t stream);
 
 /* Sets the time limit, in nanoseconds, of every pipeline wait in the dense
  * and the paged kernels (default 2e9).  Exceeding it aborts the CTA and flags
- * GQA_ERR_DEVICE_TIMEOUT.  0 restores the default.  Affects later launches
- * on all streams. */
+ * GQA_ERR_DEVICE_TIMEOUT.  0 restores the default; values below 1e6 (1 ms)
+ * are raised to 1e6, so that an aborting CTA's bounded drain outlasts every
+ * copy still in flight into its shared memory.  Affects later launches on all
+ * streams. */
 void gqa_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus

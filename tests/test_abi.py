@@ -113,14 +113,15 @@ def test_dense_engine_choice(lib):
 
 def test_paged_engine_choice(lib):
     """Host-only: FP8 pools of head dim 128 with KV heads in blocks of 8 and at
-    most 8 query rows per KV head run on tcgen05 (both forms); every other
+    most 4 query rows per KV head run on tcgen05 (both forms); every other
     paged shape on mma.sync; the measurement hook forces mma.sync."""
     eng = lib.gqa_decode_paged_engine
     # whole requests: (B, Sq, Hq, Hkv, D, kv_dtype, topk_form)
-    assert eng(4, 1, 64, 8, 128, 1, 0) == 1         # FP8, 8 rows per KV head
-    assert eng(4, 2, 32, 8, 128, 1, 0) == 1         # 4 x 2 rows
-    assert eng(4, 1, 128, 16, 128, 1, 0) == 1       # two blocks of 8 KV heads
+    assert eng(4, 1, 32, 8, 128, 1, 0) == 1         # FP8, 4 rows per KV head
+    assert eng(4, 2, 16, 8, 128, 1, 0) == 1         # 2 x 2 rows
+    assert eng(4, 1, 64, 16, 128, 1, 0) == 1        # two blocks of 8 KV heads
     assert eng(4, 1, 8, 8, 128, 1, 0) == 1          # one row per KV head
+    assert eng(4, 1, 64, 8, 128, 1, 0) == 0         # 8 rows per KV head
     assert eng(4, 2, 64, 8, 128, 1, 0) == 0         # 16 rows per KV head
     assert eng(4, 1, 32, 4, 128, 1, 0) == 0         # 4 KV heads
     assert eng(4, 1, 96, 12, 128, 1, 0) == 0        # 12 KV heads
@@ -130,16 +131,16 @@ def test_paged_engine_choice(lib):
     # top-K form (FP8, Sq = 1; kv_dtype ignored)
     assert eng(256, 1, 32, 8, 128, 0, 1) == 1
     assert eng(256, 1, 32, 4, 128, 0, 1) == 0
-    assert eng(256, 1, 128, 8, 128, 0, 1) == 0      # 16 rows per KV head
+    assert eng(256, 1, 64, 8, 128, 0, 1) == 0       # 8 rows per KV head
     assert eng(4, 1, 6, 4, 128, 1, 0) == -1         # Hq % Hkv != 0
     assert eng(4, 1, 64, 8, 96, 1, 0) == -2         # unsupported head size
     lib.gqa_debug_set_paged_engine(1)
     try:
-        assert eng(4, 1, 64, 8, 128, 1, 0) == 0
+        assert eng(4, 1, 32, 8, 128, 1, 0) == 0
         assert eng(256, 1, 32, 8, 128, 0, 1) == 0
     finally:
         lib.gqa_debug_set_paged_engine(0)
-    assert eng(4, 1, 64, 8, 128, 1, 0) == 1
+    assert eng(4, 1, 32, 8, 128, 1, 0) == 1
 
 
 def test_engine_names_match_header():

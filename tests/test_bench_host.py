@@ -75,7 +75,7 @@ def test_workload_kernel_names_the_engine():
     assert bench.workload_kernel(c["dense_b8_h32x2_d256_sq8_kv128k"]) == "gqa_dense_umma_kernel"
     assert bench.workload_kernel(c["dense_b1_h64x8_d192x128_sq2_kv128k"]) == "gqa_dense_split_kernel"
     assert bench.workload_kernel(c["paged_fp8_b256_h32x8_d128_top512_ps16"]) == "gqa_paged_umma_kernel"
-    assert bench.workload_kernel(c["paged_fp8_b32_h64x8_d128_kv32k_ps16"]) == "gqa_paged_umma_kernel"
+    assert bench.workload_kernel(c["paged_fp8_b32_h64x8_d128_kv32k_ps16"]) == "gqa_paged_kernel"  # 8 rows per KV head
     assert bench.workload_kernel(c["paged_bf16_b32_h64x8_d128_kv32k_ps16"]) == "gqa_paged_kernel"
     assert bench.workload_kernel(c["paged_int8_b32_h64x8_d128_kv32k_ps16"]) == "gqa_paged_kernel"
     assert bench.workload_kv_bytes(c["dense_b1_h64x8_d128_sq8_kv128k"]) == 512 << 20

@@ -1,5 +1,5 @@
 """GPU parity of the paged decode's tcgen05 engine (FP8 pools, head dim 128,
-KV heads in blocks of 8, up to 8 query rows per KV head), both forms, through
+KV heads in blocks of 8, up to 4 query rows per KV head), both forms, through
 the C ABI, against the fp64 oracle on the same stored codes and scales; and
 against the mma.sync engine on the same inputs."""
 import math
@@ -68,9 +68,9 @@ TOPK = [
     (2, 8, 8, 16, 8, 100, 5),       # one row per KV head, ragged list with padding
     (2, 16, 8, 1, 70, 67, 0),       # page size 1
     (4, 24, 8, 64, 3, 150, 9),      # 3 rows per KV head (one padding row of 4), page size 64
-    (2, 64, 8, 16, 12, 190, 0),     # 8 rows per KV head
-    (1, 40, 8, 16, 20, 300, 1),     # 5 rows per KV head (instance of 8)
-    (2, 128, 16, 16, 8, 128, 0),    # two blocks of 8 KV heads
+    (2, 32, 8, 16, 12, 190, 0),     # 4 rows per KV head, ragged last block
+    (1, 24, 8, 16, 20, 300, 1),     # 3 rows per KV head, padding entry
+    (2, 64, 16, 16, 8, 128, 0),     # two blocks of 8 KV heads
     (5, 32, 8, 16, 4, 1, 0),        # a single selected token
     (2, 32, 8, 16, 8, 128, 128),    # every entry padding: O = 0, LSE = -inf
     (1, 32, 8, 16, 200, 3000, 11),  # a long list (many blocks, lazy rescales)
@@ -93,12 +93,12 @@ def test_topk_vs_oracle(gq, orc, shape):
 # (B, Sq, Hq, Hkv, page_size, pages_per_req, seq_lens)
 WHOLE = [
     (3, 1, 32, 8, 16, 8, (128, 100, 17)),
-    (2, 2, 32, 8, 1, 90, (90, 33)),          # 8 rows per KV head with the causal mask, page size 1
-    (2, 4, 16, 8, 64, 3, (192, 5)),          # 4 decode rows, a request of 5 tokens
-    (3, 3, 16, 8, 16, 6, (96, 2, 0)),        # 6 rows (instance of 8); shorter than Sq; empty
-    (1, 1, 64, 8, 16, 300, (4800,)),         # long request, 8 rows per KV head
+    (2, 2, 16, 8, 1, 90, (90, 33)),          # 4 rows per KV head with the causal mask, page size 1
+    (2, 4, 8, 8, 64, 3, (192, 5)),           # 4 decode rows, a request of 5 tokens
+    (3, 3, 8, 8, 16, 6, (96, 2, 0)),         # 3 rows (instance of 4); shorter than Sq; empty
+    (1, 1, 32, 8, 16, 300, (4800,)),         # long request, 4 rows per KV head
     (2, 1, 8, 8, 32, 4, (111, 64)),          # one row per KV head
-    (1, 2, 64, 16, 16, 40, (600,)),          # two blocks of 8 KV heads, 8 rows each
+    (1, 2, 32, 16, 16, 40, (600,)),          # two blocks of 8 KV heads, 4 rows each
 ]
 
 
@@ -116,6 +116,14 @@ def test_whole_request_vs_oracle(gq, orc, shape, splits):
     _check_rows(out, lse, ref_o, ref_l, f"whole {shape} splits={splits}")
 
 
+def test_eight_rows_per_head_run_on_mma_sync(gq):
+    """Shapes with 5-8 query rows per KV head stay on the mma.sync engine."""
+    assert gq.gqa_decode_paged_engine(4, 1, 64, 8, 128, 1) == "mma.sync"
+    assert gq.gqa_decode_paged_engine(4, 2, 32, 8, 128, 1) == "mma.sync"
+    assert gq.gqa_decode_paged_engine(256, 1, 64, 8, 128, 1, topk_form=True) == "mma.sync"
+    assert gq.gqa_decode_paged_engine(4, 1, 32, 8, 128, 1) == "tcgen05"
+
+
 def test_engines_agree_and_repeat_bitwise(gq):
     """The tcgen05 and mma.sync engines give the same results within rounding
     on the same inputs; a tcgen05 call repeated is bit for bit the same."""
@@ -131,7 +139,7 @@ def test_engines_agree_and_repeat_bitwise(gq):
         gq.gqa_debug_set_paged_engine(0)
     assert torch.allclose(a1.float(), b1.float(), atol=1e-2, rtol=1e-2)
     assert torch.allclose(l1, m1, atol=1e-3, rtol=0)
-    w = gqa_inputs.paged_kv_inputs(3, 2, 32, 8, 128, 16, 20, 70, seed=92, kv_dtype="fp8", seq_lens=[300, 17, 2])
+    w = gqa_inputs.paged_kv_inputs(3, 2, 16, 8, 128, 16, 20, 70, seed=92, kv_dtype="fp8", seq_lens=[300, 17, 2])
     c1, n1 = _whole(gq, w, num_splits=5)
     gq.gqa_debug_set_paged_engine(1)
     try:
