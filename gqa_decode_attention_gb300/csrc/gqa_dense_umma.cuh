@@ -17,12 +17,14 @@
 //   warp 3      allocates TMEM; lane 0 issues every MMA:
 //                 S(j) = Q K(j)^T   M=128 rows, N=64 keys, K=D  -> TMEM S[j%2]
 //                 O   += P(j) V(j)  M=128 rows, N=D,  K=64 keys -> TMEM O
-//               in the order QK(0), QK(1), PV(0), QK(2), PV(1), ... so the
-//               tensor core computes the next scores while the softmax runs.
+//               so the tensor core computes the next scores while the softmax
+//               runs: at D = 128, QK(0), QK(1), then QK(j+2), PV(j) once P(j)
+//               is out; at D = 256, PV(j) once P(j) is out and QK(j+1) as soon
+//               as its tile lands.
 //   warps 4..7  one thread per query row (TMEM lane): load the S row, take
 //               the maximum, causal mask, online softmax in the log2 domain,
-//               write P as bf16 to shared memory (the A operand of PV), and
-//               the epilogue.
+//               write P(j) as bf16 to shared-memory buffer j % NP (the A
+//               operand of PV), and the epilogue.
 // The online softmax keeps a per-row reference maximum and rescales O (in
 // TMEM) only when a row's maximum grows by more than 2^8; in between, the
 // weights are exp2(s - reference) <= 2^8, which changes rounding only.  Every
@@ -58,16 +60,33 @@ struct UmmaCfg {
     static constexpr int CHUNKS = D / 64;
     static constexpr int TILE_BYTES = BN * D * 2;  // K or V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int P_BYTES = BM * 128;  // P rows use one 128-byte swizzle row (BN <= 64 keys)
+    // Order of the two products once P(j) is out.  A score product is a
+    // chain of D / 16 dependent MMAs (about 150 clocks a step on GB300,
+    // whatever N is), and S(j+2) is what the softmax waits for next, so at
+    // D = 128 QK(j+2) is issued ahead of PV(j) and runs first in the tensor
+    // pipe.  P(j+2) then no longer waits for PV(j) through the score commit,
+    // so P gets a third buffer; and P lives in TMEM (the A operand of PV read
+    // from tensor memory), which takes its writes and reads off the shared
+    // memory the tiles stream through.  At D = 256 TMEM is full (scores,
+    // output and queries) and the tile's bytes dominate: P stays in shared
+    // memory, PV(j) goes first, then QK(j+1) as soon as its tile lands.
+#ifndef GQA_UMMA_QK_FIRST
+#define GQA_UMMA_QK_FIRST (D == 128)
+#endif
+    static constexpr bool QK_FIRST = GQA_UMMA_QK_FIRST;
+    static constexpr bool P_TMEM = QK_FIRST;         // P in tensor memory
+    static constexpr int NP = QK_FIRST ? 3 : 2;      // P buffers
+    static constexpr int P_BYTES = BM * 128;  // a shared-memory P buffer: one 128-byte swizzle row a row (BN <= 64)
+    static constexpr int NP_SMEM = P_TMEM ? 0 : NP;
     static constexpr int BUDGET = 227 * 1024 - 1024 - 256;
-    static constexpr int STAGES_FIT = (BUDGET - 2 * P_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES_FIT = (BUDGET - NP_SMEM * P_BYTES) / STAGE_BYTES;
 #ifndef GQA_UMMA_MAX_STAGES
-#define GQA_UMMA_MAX_STAGES 4
+#define GQA_UMMA_MAX_STAGES 5
 #endif
     static constexpr int STAGES = STAGES_FIT > GQA_UMMA_MAX_STAGES ? GQA_UMMA_MAX_STAGES : STAGES_FIT;
     static constexpr int RING_OFF = 0;
     static constexpr int P_OFF = RING_OFF + STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
+    static constexpr int BAR_OFF = P_OFF + NP_SMEM * P_BYTES;
     static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;
     // Warp roles: 0 TMA producer, 1 and 2 leave at once, 3 allocates TMEM and
     // issues the MMAs, 4..7 softmax (warp w reads TMEM lane quarter w % 4).
@@ -83,13 +102,15 @@ struct UmmaCfg {
     static constexpr uint32_t S_COL = 0;            // two BN-column score buffers
     static constexpr uint32_t O_COL = 2 * BN;       // D columns of fp32 output
     static constexpr uint32_t Q_COL = O_COL + D;    // the CTA's queries, D/2 columns (A operand of QK)
-    static constexpr uint32_t TMEM_COLS = (Q_COL + D / 2) <= 256 ? 256 : 512;
-    static_assert(Q_COL + D / 2 <= 512, "TMEM budget");
+    static constexpr uint32_t P_COL = Q_COL + D / 2;  // P buffers in TMEM, BN/2 columns each (A operand of PV)
+    static constexpr uint32_t COLS_USED = P_COL + (P_TMEM ? NP * BN / 2 : 0);
+    static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256 : 512;
+    static_assert(COLS_USED <= 512, "TMEM budget");
 #ifndef GQA_UMMA_RESCALE_LOG2
 #define GQA_UMMA_RESCALE_LOG2 8.f
 #endif
     static constexpr float kRescaleLog2 = GQA_UMMA_RESCALE_LOG2;
-    static_assert(STAGES >= 2, "ring needs two stages");
+    static_assert(STAGES >= 3, "QK(j+2) and PV(j) need their tiles in the ring together");
     static_assert(BN == 32 || BN == 64, "tile keys");
     static_assert(D % 64 == 0 && D <= 256, "head dim");
 };
@@ -107,8 +128,8 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
     uint64_t *empty = full + C::STAGES;
     uint64_t *s_full = empty + C::STAGES;  // [2]
     uint64_t *p_ready = s_full + 2;        // [2]
-    uint64_t *o_done = p_ready + 2;        // [1]
-    uint64_t *fin = o_done + 1;            // [1]
+    uint64_t *o_done = p_ready + 2;        // [2]: PV(j) completes phase j / 2 of o_done[j % 2]
+    uint64_t *fin = o_done + 2;            // [1]
     uint64_t *q_ready = fin + 1;           // [1]
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(q_ready + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_s + 1);
@@ -131,8 +152,8 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&s_full[s], 1);
             mbar_init(&p_ready[s], 128);
+            mbar_init(&o_done[s], 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(fin, 1);
         mbar_init(q_ready, 128);
         *abort_flag = 0;
@@ -197,8 +218,8 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
             const uint32_t ring_addr = smem_u32(ring);
             const uint32_t p_addr = smem_u32(ps);
             bool ok = true;
-            // QK(j): the tile must have landed; S[j % 2] is free because the
-            // row threads released it (p_ready) before QK(j - 2)'s successor.
+            // QK(j): the tile must have landed, and S[j % 2] is free once the row
+            // threads have released P(j - 2) (they read S(j - 2) first).
             auto issue_qk = [&](int j) {
                 const int st = j % C::STAGES;
                 tc_fence_after_sync();
@@ -220,7 +241,60 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                     qk_issued = 1;
                 }
             }
+            if (C::QK_FIRST && ok && n_it > 1) {
+                ok = mbar_wait_bounded(&full[1], 0, a.wait_limit_ns, abort_flag);
+                if (ok) {
+                    issue_qk(1);
+                    qk_issued = 2;
+                }
+            }
             for (int j = 0; ok && j < n_it; ++j) {
+                if (C::QK_FIRST) {
+                    // Wait for P(j) (suspended in the barrier instruction), then QK(j+2)
+                    // into the score buffer P(j) released -- ahead of PV(j) when its
+                    // tile is in, right after it otherwise.
+                    const uint64_t t0 = globaltimer_ns();
+                    for (uint32_t spin = 1;; ++spin) {
+                        if (mbar_try_wait(&p_ready[j & 1], (j >> 1) & 1)) break;
+                        if ((spin & 63u) == 0u && (*abort_flag || globaltimer_ns() - t0 > a.wait_limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const int nx = j + 2;
+                    if (nx < n_it && mbar_test_wait(&full[nx % C::STAGES], (nx / C::STAGES) & 1)) {
+                        issue_qk(nx);
+                        qk_issued = nx + 1;
+                    }
+                    const int st = j % C::STAGES;
+                    const uint32_t vaddr = ring_addr + st * C::STAGE_BYTES + C::TILE_BYTES;
+                    const uint32_t pcol = C::P_COL + (j % C::NP) * (C::BN / 2);
+#pragma unroll
+                    for (int kg = 0; kg < C::BN / 16; ++kg) {
+                        const uint64_t bd = smem_desc_sw128(vaddr + kg * 2048, C::BN * 128, 1024);
+                        if constexpr (C::P_TMEM) {
+                            umma_bf16_ta(tbase + C::O_COL, tbase + pcol + kg * 8, bd, idesc_pv, (j > 0 || kg > 0) ? 1u : 0u);
+                        } else {
+                            const uint64_t ad =
+                                smem_desc_sw128(p_addr + (j % C::NP) * C::P_BYTES + kg * 32, 16, 1024);
+                            umma_bf16(tbase + C::O_COL, ad, bd, idesc_pv, (j > 0 || kg > 0) ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(&o_done[j & 1]);
+                    umma_commit(&empty[st]);
+                    if (nx < n_it && qk_issued == nx) {
+                        if (!mbar_wait_bounded(&full[nx % C::STAGES], (nx / C::STAGES) & 1, a.wait_limit_ns,
+                                               abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        issue_qk(nx);
+                        qk_issued = nx + 1;
+                    }
+                    continue;
+                }
                 // Wait for P(j) while issuing QK(j+1) the moment its tile lands,
                 // so PV(j) never waits on the next tile's copy.  The wait on P(j)
                 // suspends the thread in the barrier instruction instead of
@@ -254,7 +328,7 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                     const uint64_t bd = smem_desc_sw128(vaddr + kg * 2048, C::BN * 128, 1024);
                     umma_bf16(tbase + C::O_COL, ad, bd, idesc_pv, (j > 0 || kg > 0) ? 1u : 0u);
                 }
-                umma_commit(o_done);
+                umma_commit(&o_done[j & 1]);
                 umma_commit(&empty[st]);
                 if (qk_issued == j + 1 && j + 1 < n_it) {
                     // the next tile was not in yet while P(j) was produced
@@ -352,10 +426,13 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                 const bool renew = mx > m_ref + C::kRescaleLog2;
                 const bool rescale = renew && l > 0.f;
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // PV(j-1) must have finished writing O.  Unambiguous: S(j) was
-                    // committed after QK(j), which was issued after PV(j-2), so at
-                    // least j-1 PV phases are complete when this thread gets here.
-                    const bool od = mbar_wait_bounded(o_done, (j - 1) & 1, a.wait_limit_ns, abort_flag);
+                    // PV(j-1) must have finished writing O: phase (j-1) / 2 of
+                    // o_done[(j-1) % 2].  Unambiguous: S(j) was committed after QK(j),
+                    // which was issued after PV(j-3) (after PV(j-2) when PV goes
+                    // first), so that barrier's previous phase is complete, and its
+                    // next one (PV(j+1)) needs a P this thread has not written yet.
+                    const bool od = mbar_wait_bounded(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.wait_limit_ns,
+                                                      abort_flag);
                     if (!__all_sync(0xffffffffu, od)) {
                         failed = true;
                         break;
@@ -377,24 +454,47 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                 if (renew) m_ref = mx;
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
                 // P = exp2(scale * s - reference) as bf16, straight into the swizzled P tile
-                uint8_t *prow = prow_base + sb * C::P_BYTES;
+                // P(j) goes to buffer j % NP, last read by PV(j - NP), which is
+                // complete: S(j)'s commit followed QK(j), issued after PV(j - NP).
                 float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (C::P_TMEM) {
+                    // one TMEM row of BN/2 columns: keys 2c and 2c+1 in column c
+                    uint32_t pk[C::BN / 2];
 #pragma unroll
-                for (int u = 0; u < C::BN / 8; ++u) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = u * 8 + e * 2;
+                    for (int c2 = 0; c2 < C::BN / 2; ++c2) {
+                        const int c = 2 * c2;
                         const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.alpha, -m_use));
                         const float p1 =
                             fast_exp2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), a.alpha, -m_use));
-                        ps4[e] += p0 + p1;
-                        w[e] = pack_bf16x2(p0, p1);
+                        ps4[c2 & 3] += p0 + p1;
+                        pk[c2] = pack_bf16x2(p0, p1);
                     }
-                    *reinterpret_cast<uint4 *>(prow + ((u ^ (lr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    const uint32_t pt = lane_base + C::P_COL + (j % C::NP) * (C::BN / 2);
+                    if constexpr (C::BN / 2 == 32) {
+                        tmem_st32(pt, pk);
+                    } else {
+                        tmem_st16(pt, pk);
+                    }
+                    tmem_wait_st();
+                } else {
+                    uint8_t *prow = prow_base + (j % C::NP) * C::P_BYTES;
+#pragma unroll
+                    for (int u = 0; u < C::BN / 8; ++u) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = u * 8 + e * 2;
+                            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.alpha, -m_use));
+                            const float p1 =
+                                fast_exp2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), a.alpha, -m_use));
+                            ps4[e] += p0 + p1;
+                            w[e] = pack_bf16x2(p0, p1);
+                        }
+                        *reinterpret_cast<uint4 *>(prow + ((u ^ (lr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async_shared();
                 }
                 l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-                fence_proxy_async_shared();
                 tc_fence_before_sync();
             }
             mbar_arrive(&p_ready[sb]);

@@ -74,6 +74,24 @@ def test_d128_tcgen05_vs_oracle(gq, orc, shape, splits):
     assert_lse_close(lse, ref_l, f"LSE {shape} splits {splits}")
 
 
+# More than 128 rows per KV head: 256 (64 query heads on 8 KV heads, 32
+# decode rows; two row groups per request, KV head and split) and 640 (five).
+MANY_ROWS128 = [(2, 32, 3001, 64, 8, 128), (1, 40, 1500, 16, 1, 128)]
+
+
+@pytest.mark.parametrize("shape", MANY_ROWS128, ids=lambda s: "b{}_sq{}_kv{}_h{}x{}_d{}".format(*s))
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_d128_many_row_groups_vs_oracle(gq, orc, shape, splits):
+    B, Sq, Skv, Hq, Hkv, D = shape
+    assert gq.gqa_decode_dense_engine(B, Sq, Skv, Hq, Hkv, D) == "tcgen05"
+    q, k, v = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=Sq * 1000 + Skv + splits)
+    out, lse = _run(gq, q, k, v, num_splits=splits)
+    assert gq.gqa_device_status() == 0
+    ref_o, ref_l = orc.gqa_decode(q, k, v, 1.0 / math.sqrt(D))
+    assert_o_close(out, ref_o, f"O {shape} splits {splits}")
+    assert_lse_close(lse, ref_l, f"LSE {shape} splits {splits}")
+
+
 def test_d128_engine_boundary(gq, orc):
     """Sq = 7 (mma.sync) and Sq = 8 (tcgen05) on the same cache agree with the
     oracle and with each other on the rows they share (the last 7 rows of the
@@ -120,7 +138,7 @@ def test_same_splits_bitwise_repeatable(gq):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 4), (8, 2), (4, 2), (16, 4), (8, 1), (64, 8), (32, 2)])
-@pytest.mark.parametrize("Sq", [1, 2, 8])
+@pytest.mark.parametrize("Sq", [1, 2, 8, 32])
 @pytest.mark.parametrize("D", [128, 256])
 def test_gqa_bitwise_equals_expanded_mha(gq, Hq, Hkv, Sq, D):
     """Native GQA == the same kernel on K/V pre-expanded to Hq heads, bit for bit
