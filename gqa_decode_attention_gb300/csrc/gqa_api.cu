@@ -37,7 +37,7 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // ------------------------------------------------------------ device facts
 std::mutex g_mu;
 int g_sm_count[kMaxDevices];
-int g_occ[kMaxDevices][4][kDenseCfgs + 1];  // + the tcgen05 engine
+int g_occ[kMaxDevices][4][kLaneCfg + kLaneCfgs];  // mma.sync configurations, tcgen05, key lanes
 
 bool current_device(int *dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return false;
@@ -226,6 +226,25 @@ size_t workspace_bytes(const DenseShape &s, int splits) {
 // key blocks per split as the kernel sees it for a split count
 int blocks_per_split(const DenseShape &s, int splits) { return (s.n_blocks + splits - 1) / splits; }
 
+// What one call launches: the split count (as realised by blocks_per_split),
+// key blocks per split, and the kernel configuration.  A small cache that the
+// automatic choice would split runs instead on the key-lane instance: one CTA
+// per unit, the split done by its warps, no combine pass.  An explicit split
+// count is always honoured as given.  (The key-lane CTA fills an SM, so the
+// units must fit one wave.)
+struct DensePlan {
+    int splits, tps, cfg;
+};
+DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
+    const int splits = choose_splits(s, requested, dev);
+    if (requested == 0 && splits > 1 && s.D == s.Dv && (s.D == 64 || s.D == 128) && s.cfg < kLaneCfgs &&
+        long(s.Skv) * s.D * 4 <= long(GQA_LANE_MAX_UNIT_BYTES) &&
+        long(s.B) * s.Hkv * s.row_groups <= long(sm_count(dev)))
+        return {1, s.n_blocks, kLaneCfg + s.cfg};
+    const int tps = blocks_per_split(s, splits);
+    return {(s.n_blocks + tps - 1) / tps, tps, s.cfg};
+}
+
 gqa_status run_dense(const void *q, const void *k, const void *v, void *out, float *lse, const DenseShape &s,
                      float scale, int requested_splits, void *workspace, size_t workspace_size,
                      cudaStream_t stream) {
@@ -236,10 +255,10 @@ gqa_status run_dense(const void *q, const void *k, const void *v, void *out, flo
     // shared-memory limit there (a per-device attribute); made here so that a
     // call with an explicit split count on a second device is covered too.
     dense_occupancy(dev, s.D, s.cfg);
-    int splits = choose_splits(s, requested_splits, dev);
-    // Equalise: the split count actually realised by blocks_per_split.
-    const int tps = blocks_per_split(s, splits);
-    splits = (s.n_blocks + tps - 1) / tps;
+    const DensePlan plan = plan_dense(s, requested_splits, dev);
+    if (plan.cfg != s.cfg) dense_occupancy(dev, s.D, plan.cfg);  // raises that kernel's limit too
+    const int splits = plan.splits;
+    const int tps = plan.tps;
     const size_t need = workspace_bytes(s, splits);
     void *ws = workspace;
     bool owned = false;
@@ -284,7 +303,7 @@ gqa_status run_dense(const void *q, const void *k, const void *v, void *out, flo
     L.k = k;
     L.v = v;
     L.D = s.D;
-    L.cfg = s.cfg;
+    L.cfg = plan.cfg;
     L.stream = stream;
     L.ev_before = g_ev_before.load();
     L.ev_after = g_ev_after.load();
@@ -515,9 +534,7 @@ size_t gqa_decode_dv_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, in
     if (check_dense_dv(B, Sq, Skv, Hq, Hkv, Dqk, Dv, &s) != GQA_OK || num_splits < 0) return 0;
     int dev = 0;
     if (num_splits == 0 && !current_device(&dev)) return 0;
-    const int splits = choose_splits(s, num_splits, dev);
-    const int tps = blocks_per_split(s, splits);
-    return workspace_bytes(s, (s.n_blocks + tps - 1) / tps);
+    return workspace_bytes(s, plan_dense(s, num_splits, dev).splits);
 }
 
 gqa_status gqa_decode(const void *q, const void *k, const void *v, void *out, float *lse, int B, int Sq, int Skv,
@@ -535,9 +552,7 @@ int gqa_decode_dv_num_splits(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, i
     if (st != GQA_OK) return -int(st);
     int dev = 0;
     if (!current_device(&dev)) return -int(GQA_ERR_CUDA);
-    const int splits = choose_splits(s, 0, dev);
-    const int tps = blocks_per_split(s, splits);
-    return (s.n_blocks + tps - 1) / tps;
+    return plan_dense(s, 0, dev).splits;
 }
 
 int gqa_decode_dense_engine(int B, int Sq, int Skv, int Hq, int Hkv, int Dqk, int Dv) {
@@ -552,9 +567,7 @@ size_t gqa_decode_workspace_bytes(int B, int Sq, int Skv, int Hq, int Hkv, int D
     if (check_dense(B, Sq, Skv, Hq, Hkv, D, &s) != GQA_OK || num_splits < 0) return 0;
     int dev = 0;
     if (num_splits == 0 && !current_device(&dev)) return 0;
-    const int splits = choose_splits(s, num_splits, dev);
-    const int tps = blocks_per_split(s, splits);
-    return workspace_bytes(s, (s.n_blocks + tps - 1) / tps);
+    return workspace_bytes(s, plan_dense(s, num_splits, dev).splits);
 }
 
 gqa_status gqa_decode_host(const void *q_host, const void *k_host, const void *v_host, void *out_host,

@@ -21,9 +21,21 @@ struct DenseInst {
 // The launches below rely on the kernel's dynamic shared-memory limit having
 // been raised on the current device: the front end's occupancy query (once
 // per device and kernel, under its lock) does that before any call launches.
+// Key-lane instance for small caches: CFG 0 or 1 (16 or 32 rows), 8 consumer
+// warps as 8 / RB key lanes.
 template <int D, int DV, int CFG>
+struct DenseLaneInst {
+    static constexpr int RB = 1 << CFG;
+    static constexpr int KS = kLaneWarps / RB;
+    static constexpr int T = dense_lane_tile_keys(D);
+    static constexpr int S = dense_lane_stages(D);
+    using C = DenseCfg<D, DV, RB, T, S, KS>;
+    static constexpr auto kernel() { return gqa_dense_split_kernel<D, DV, RB, T, S, KS>; }
+};
+
+template <int D, int DV, int CFG, template <int, int, int> class Inst = DenseInst>
 static cudaError_t launch_split_cfg(const DenseLaunch &L) {
-    using I = DenseInst<D, DV, CFG>;
+    using I = Inst<D, DV, CFG>;
     using C = typename I::C;
     auto kern = I::kernel();
     CUtensorMap tk, tv;
@@ -38,9 +50,9 @@ static cudaError_t launch_split_cfg(const DenseLaunch &L) {
     return cudaGetLastError();
 }
 
-template <int D, int DV, int CFG>
+template <int D, int DV, int CFG, template <int, int, int> class Inst = DenseInst>
 static int occupancy_cfg() {
-    using I = DenseInst<D, DV, CFG>;
+    using I = Inst<D, DV, CFG>;
     using C = typename I::C;
     auto kern = I::kernel();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
@@ -105,7 +117,15 @@ static cudaError_t launch_dense(const DenseLaunch &L) {
         case 0: e = launch_split_cfg<D, DV, 0>(L); break;
         case 1: e = launch_split_cfg<D, DV, 1>(L); break;
         case 2: e = launch_split_cfg<D, DV, 2>(L); break;
-        default: e = launch_split_cfg<D, DV, 3>(L); break;
+        case 3: e = launch_split_cfg<D, DV, 3>(L); break;
+        default:
+            if constexpr (D == DV && (D == 64 || D == 128)) {
+                e = L.cfg == kLaneCfg ? launch_split_cfg<D, DV, 0, DenseLaneInst>(L)
+                                      : launch_split_cfg<D, DV, 1, DenseLaneInst>(L);
+            } else {
+                e = cudaErrorInvalidValue;
+            }
+            break;
     }
     if (e != cudaSuccess || L.args.num_splits == 1) return e;
     return launch_combine<DV>(L);
@@ -117,7 +137,14 @@ static int dense_occupancy(int cfg) {
         case 0: return occupancy_cfg<D, DV, 0>();
         case 1: return occupancy_cfg<D, DV, 1>();
         case 2: return occupancy_cfg<D, DV, 2>();
-        default: return occupancy_cfg<D, DV, 3>();
+        case 3: return occupancy_cfg<D, DV, 3>();
+        default:
+            if constexpr (D == DV && (D == 64 || D == 128)) {
+                return cfg == kLaneCfg ? occupancy_cfg<D, DV, 0, DenseLaneInst>()
+                                       : occupancy_cfg<D, DV, 1, DenseLaneInst>();
+            } else {
+                return 0;
+            }
     }
 }
 

@@ -21,6 +21,14 @@
 // the combine kernel.  D is the score head size (q, K) and DV the value head
 // size (V, O, partials); they differ only in the d192x128 instance.
 //
+// Small caches (key lanes, KS > 1): the CTA takes the whole cache of its
+// (b, g) -- one split -- and its consumer warps form KS key lanes of RB row
+// blocks; lane k walks the tiles k, k + KS, k + 2 KS, ... of the same ring
+// with its own online-softmax state, and at the end the lanes' (maximum, sum,
+// unnormalised O) are merged in shared memory by lane 0, which writes the
+// result.  One launch and no combine pass: the flash-decoding split of the
+// KV walk, done inside one CTA.
+//
 // Every mbarrier wait is bounded in wall time; on expiry the CTA flags the
 // device error word, waits (bounded) for its own loads still in flight, and
 // returns.
@@ -34,12 +42,12 @@ namespace gqa {
 // Keys per online-softmax step (one m16n8k16 k-group of keys).
 constexpr int kStepKeys = 16;
 
-// Shape of one kernel instance: RB consumer warps (16 rows each), TMA tiles of
-// T keys, STAGES ring slots.  Chosen per (head dim, row count) so small-group
-// CTAs are small and many fit on an SM.
-template <int D, int DV, int RB, int T, int STAGES_>
+// Shape of one kernel instance: RB consumer warps (16 rows each) per key
+// lane, KS key lanes, TMA tiles of T keys, STAGES ring slots.  Chosen per
+// (head dim, row count) so small-group CTAs are small and many fit on an SM.
+template <int D, int DV, int RB, int T, int STAGES_, int KS = 1>
 struct DenseCfg {
-    static constexpr int NC = RB;
+    static constexpr int NC = RB * KS;
     static constexpr int THREADS = 32 * (NC + 1);
     static constexpr int STAGES = STAGES_;
     static constexpr int K_CHUNKS = D / 64;   // 128-byte swizzle atoms per K row (D = score head size)
@@ -55,13 +63,18 @@ struct DenseCfg {
     static constexpr int MIN_BLOCKS_RAW = (227 * 1024) / SMEM_BYTES;
     static constexpr int MIN_BLOCKS = MIN_BLOCKS_RAW < 1 ? 1 : (MIN_BLOCKS_RAW > 8 ? 8 : MIN_BLOCKS_RAW);
     static_assert(kSplitKeys % T == 0 && T % kStepKeys == 0, "tile must divide the split granule");
+    // key-lane merge: per lane of every consumer warp, its O fragment (DV / 2
+    // floats) and two (maximum, sum) pairs, laid over the drained ring
+    static constexpr int MERGE_FLOATS = DV / 2 + 4;
+    static_assert(KS == 1 || NC * 32 * MERGE_FLOATS * 4 <= RING_BYTES, "merge area fits the ring");
 };
 
-template <int D, int DV, int RB, int T, int STAGES_>
-__global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, DenseCfg<D, DV, RB, T, STAGES_>::MIN_BLOCKS)
+template <int D, int DV, int RB, int T, int STAGES_, int KS = 1>
+__global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_, KS>::THREADS,
+                                  DenseCfg<D, DV, RB, T, STAGES_, KS>::MIN_BLOCKS)
     gqa_dense_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            const DenseArgs a) {
-    using C = DenseCfg<D, DV, RB, T, STAGES_>;
+    using C = DenseCfg<D, DV, RB, T, STAGES_, KS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem;
@@ -85,7 +98,7 @@ __global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, Dens
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], C::NC);
+            mbar_init(&empty[s], RB);  // the row blocks of the tile's key lane
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -137,7 +150,8 @@ __global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, Dens
     }
 
     // ---------------------------------------------------------------- consumers
-    const int rb = warp - 1;  // row block of this warp
+    const int rb = (warp - 1) % RB;  // row block of this warp
+    const int ks = (warp - 1) / RB;  // key lane: tiles ks, ks + KS, ...
     const int cthreads = C::NC * 32;
     const int ctid = threadIdx.x - 32;
 
@@ -178,7 +192,7 @@ __global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, Dens
     const uint32_t ring_base = smem_u32(ring);
     bool failed = false;
 
-    for (int it = 0; it < n_it; ++it) {
+    for (int it = ks; it < n_it; it += KS) {
         const int st = it % C::STAGES;
         // ldmatrix / mma.sync are warp-collective: the whole warp leaves together.
         const bool got = mbar_wait_bounded(&full[st], (it / C::STAGES) & 1, a.wait_limit_ns, abort_flag);
@@ -284,13 +298,69 @@ __global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_>::THREADS, Dens
         *abort_flag = 1;
     }
     pdl_launch_dependents();
-    if (failed || *abort_flag) return;
+    if constexpr (KS == 1) {
+        if (failed || *abort_flag) return;
+    }
 
     // ---- row sums across the 4 lanes that share a row
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
         l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 1);
         l_run[hr] += __shfl_xor_sync(0xffffffffu, l_run[hr], 2);
+    }
+
+    if constexpr (KS > 1) {
+        // Every consumer warp gets here (a failed one too), so the barriers below
+        // always complete; the decision to write anything is taken after the
+        // first one, from the shared abort flag.  Past it every tile has been
+        // consumed, so every copy has landed and the ring is free.
+        asm volatile("bar.sync 1, %0;" ::"r"(cthreads) : "memory");
+        if (*abort_flag) return;
+        float *mx = reinterpret_cast<float *>(ring) + size_t((warp - 1) * 32 + lane) * C::MERGE_FLOATS;
+#pragma unroll
+        for (int nt = 0; nt < DV / 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx[nt * 4 + e] = o[nt][e];
+        mx[DV / 2 + 0] = m_run[0];
+        mx[DV / 2 + 1] = m_run[1];
+        mx[DV / 2 + 2] = l_run[0];
+        mx[DV / 2 + 3] = l_run[1];
+        asm volatile("bar.sync 1, %0;" ::"r"(cthreads) : "memory");
+        if (ks != 0) return;
+        // lane 0 merges lanes 0 .. KS-1 of its row block, in lane order:
+        // M = max m_k, O = sum 2^(m_k - M) O_k, L = sum 2^(m_k - M) l_k
+        const float *base = reinterpret_cast<const float *>(ring);
+        float mk[KS][2];
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            const float *src = base + size_t((k * RB + rb) * 32 + lane) * C::MERGE_FLOATS;
+            mk[k][0] = src[DV / 2 + 0];
+            mk[k][1] = src[DV / 2 + 1];
+        }
+        float wk[KS][2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            float M = mk[0][hr];
+#pragma unroll
+            for (int k = 1; k < KS; ++k) M = fmaxf(M, mk[k][hr]);
+            const float M_use = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) wk[k][hr] = (mk[k][hr] == -INFINITY) ? 0.f : fast_exp2(mk[k][hr] - M_use);
+            m_run[hr] = M;
+            l_run[hr] = 0.f;
+        }
+#pragma unroll
+        for (int nt = 0; nt < DV / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+#pragma unroll
+        for (int k = 0; k < KS; ++k) {
+            const float *src = base + size_t((k * RB + rb) * 32 + lane) * C::MERGE_FLOATS;
+            l_run[0] += wk[k][0] * src[DV / 2 + 2];
+            l_run[1] += wk[k][1] * src[DV / 2 + 3];
+#pragma unroll
+            for (int nt = 0; nt < DV / 8; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[nt][e] += wk[k][e >> 1] * src[nt * 4 + e];
+        }
     }
 
     // ---- epilogue

@@ -32,10 +32,33 @@ constexpr int kUmmaCfg = kDenseCfgs;
 inline bool dense_uses_umma(int D, int Dv, int Sq) {
     return D == 256 || (D == 128 && Dv == 128 && Sq >= GQA_D128_UMMA_MIN_SQ);
 }
+// Key-lane instances of the mma.sync kernel for small caches (cfg kLaneCfg +
+// c for the c-th row configuration, c = 0 or 1: 16 or 32 rows): one CTA per
+// (batch row, KV head, row group) takes the whole cache, its 8 consumer warps
+// forming 8 / RB key lanes that split the walk inside the CTA and merge in
+// shared memory -- one launch, no combine pass.  Used when the automatic split
+// count would need several splits and a unit's K and V take at most
+// GQA_LANE_MAX_UNIT_BYTES (head dims 64 and 128).  Measured on GB300 (device
+// time per call, L2 flushed): 1K keys at d64 or 512 at d128 (256 KiB a unit)
+// went from 13.0-16.1 us to 10.9-13.0 us; at 512 KiB a unit the one-CTA walk
+// was already 1-2 us slower than splits + combine.
+constexpr int kLaneCfg = kUmmaCfg + 1;
+constexpr int kLaneCfgs = 2;
+constexpr int kLaneWarps = 8;
+#ifndef GQA_LANE_MAX_UNIT_BYTES
+#define GQA_LANE_MAX_UNIT_BYTES (256 * 1024)
+#endif
+inline bool dense_is_lane_cfg(int cfg) { return cfg >= kLaneCfg && cfg < kLaneCfg + kLaneCfgs; }
 // Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM
 // lanes); the mma.sync engine holds the group's rows rounded up to 16, at
-// most 128.
-inline int dense_rows_per_cta(int cfg) { return cfg == kUmmaCfg ? 128 : dense_cfg_rows(cfg); }
+// most 128 (16 or 32 in a key-lane instance).
+inline int dense_rows_per_cta(int cfg) {
+    return cfg == kUmmaCfg ? 128 : dense_is_lane_cfg(cfg) ? dense_cfg_rows(cfg - kLaneCfg) : dense_cfg_rows(cfg);
+}
+// Tile keys and ring depth of the key-lane instances: 16 KiB stages, twelve of
+// them in flight (one SM then keeps about 192 KiB of loads outstanding).
+constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
+constexpr int dense_lane_stages(int) { return 12; }
 // Tile keys and ring depth of the 16-row instance at D = 128 (the decode
 // shape with the most traffic); compile-time knobs for tuning builds.
 #ifndef GQA_D128_R16_TILE

@@ -103,7 +103,13 @@ const char *gqa_version(void);
  * (Hq/Hkv)*Sq query rows, up to 128 of them, so each K/V byte is read from
  * HBM once per 128 query rows of a group (once for groups of up to 128
  * rows).  When more than one split is used, an LSE-weighted combine kernel
- * produces out / lse.  Two kernel engines serve the dense calls (see
+ * produces out / lse.  A small cache that the automatic choice would split
+ * (head dim 64 or 128, up to 32 query rows per CTA, at most 256 KiB of K and
+ * V per (b, g), B * Hkv * row groups at most the SM count) runs instead as
+ * one CTA per (b, g, row group) whose warps
+ * split the walk among themselves and merge in shared memory: one launch,
+ * no combine, no workspace (the split-count query then reports 1); an
+ * explicit split count is always used as given.  Two kernel engines serve the dense calls (see
  * gqa_decode_dense_engine): mma.sync, and tcgen05 for head dim 256 and for
  * head dim 128 from Sq >= 8.
  *

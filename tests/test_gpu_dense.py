@@ -92,6 +92,39 @@ def test_d128_many_row_groups_vs_oracle(gq, orc, shape, splits):
     assert_lse_close(lse, ref_l, f"LSE {shape} splits {splits}")
 
 
+# Small caches that the automatic choice would split run as one CTA per
+# (b, g, row group) whose warps split the walk (key lanes) and merge in shared
+# memory: 8 lanes of 16 rows or 4 lanes of 32; ragged tails, lanes with no
+# tile (200 keys: 7 tiles of 32 for 8 lanes; 130 and 150 keys: 3 tiles of 64),
+# causal rows, the 256 KiB bound.
+LANES = [(1, 1, 1000, 8, 1, 64), (1, 1, 512, 8, 1, 128), (2, 2, 500, 32, 8, 128), (1, 4, 1024, 16, 2, 64),
+         (1, 1, 200, 8, 1, 128), (1, 4, 150, 8, 1, 64), (1, 2, 480, 16, 1, 128), (1, 1, 130, 4, 1, 64)]
+
+
+@pytest.mark.parametrize("shape", LANES, ids=lambda s: "b{}_sq{}_kv{}_h{}x{}_d{}".format(*s))
+def test_key_lanes_vs_oracle(gq, orc, shape):
+    B, Sq, Skv, Hq, Hkv, D = shape
+    assert gq.gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D) == 1
+    assert gq.gqa_decode_workspace_bytes(B, Sq, Skv, Hq, Hkv, D, 0) == 0
+    q, k, v = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=Skv * 10 + Sq)
+    out, lse = _run(gq, q, k, v)
+    ref_o, ref_l = orc.gqa_decode(q, k, v, 1.0 / math.sqrt(D))
+    assert_o_close(out, ref_o, f"O {shape}")
+    assert_lse_close(lse, ref_l, f"LSE {shape}")
+    # an explicit split count takes the split + combine path: same values within rounding
+    o2, l2 = _run(gq, q, k, v, num_splits=2)
+    assert_o_close(o2, out.double(), f"O {shape} vs 2 splits")
+    assert torch.allclose(l2, lse, atol=1e-4, rtol=0)
+
+
+def test_key_lanes_bound(gq):
+    """Past 256 KiB of K and V per (b, g) the automatic choice splits across CTAs."""
+    assert gq.gqa_decode_num_splits(1, 1, 1024, 8, 1, 64) == 1       # exactly 256 KiB
+    assert gq.gqa_decode_num_splits(1, 1, 1088, 8, 1, 64) > 1        # just above
+    assert gq.gqa_decode_num_splits(1, 1, 1000, 8, 1, 256) > 1       # head dim 256: split kernel
+    assert gq.gqa_decode_num_splits(1, 8, 1000, 64, 8, 128) > 1      # 64 rows per CTA
+
+
 def test_d128_engine_boundary(gq, orc):
     """Sq = 7 (mma.sync) and Sq = 8 (tcgen05) on the same cache agree with the
     oracle and with each other on the rows they share (the last 7 rows of the
