@@ -146,6 +146,9 @@ struct PagedUmmaCfg {
     static constexpr int Q_BYTES = N * 128;       // one E4M3 piece of Q' (N rows of 128 codes)
     static constexpr int P_BYTES = 128 * N;       // one E4M3 piece of P'^T (128 rows x N bytes)
     static constexpr int P_BUFS = R <= 4 ? 2 : 1;
+    static constexpr int OUT_PIECES = N * D / 8;   // 16-byte pieces of the output rows (bf16)
+    static_assert(N * D * 4 <= P_BUFS * 2 * P_BYTES, "the epilogue stages O (fp32) over the P buffers");
+    static_assert(OUT_PIECES % 128 == 0, "whole rounds of output pieces");
     static constexpr int P_NBLK = 2048;           // P'^T: byte distance between 16-column blocks
     static constexpr float kPExp = 6.f;           // p = 2^kPExp exp2(x - m)
     static constexpr float kLazy = 2.75f;         // rescale once x exceeds m by more than this
@@ -845,22 +848,22 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
             // behind that block's work.  (Loading them at the segment's start, to
             // hold them in registers through every block, measured 12 us slower on
             // the 256-request workload.)
-            uint32_t graw[RANGE ? 1 : C::N / 2];
+            // the gate in the epilogue's layout: 16-byte pieces x = m + 128 i of the
+            // segment's output rows (row n = x / 16 holds column n of O^T)
+            uint4 graw[RANGE ? 1 : C::OUT_PIECES / 128];
             if constexpr (!RANGE) {
 #pragma unroll
-                for (int n = 0; n < C::N / 2; ++n) graw[n] = 0u;
+                for (int i = 0; i < C::OUT_PIECES / 128; ++i) graw[i] = make_uint4(0u, 0u, 0u, 0u);
             }
             auto load_gate = [&]() {
                 if constexpr (!RANGE) {
                     const __nv_bfloat16 *__restrict__ gatep = a.gate;
                     if (gatep != nullptr && w.complete && !failed) {
 #pragma unroll
-                        for (int n = 0; n < C::N; n += 2) {
-                            const long long r0 = col_base[n], r1 = col_base[n + 1];
-                            const int d = 16 * ((m >> 4) ^ (n / R)) + (m & 15);  // columns n, n + 1: same head
-                            const uint32_t g0 = r0 >= 0 ? __bfloat16_as_ushort(gatep[r0 * C::D + d]) : 0u;
-                            const uint32_t g1 = r1 >= 0 ? __bfloat16_as_ushort(gatep[r1 * C::D + d]) : 0u;
-                            graw[n / 2] = g0 | (g1 << 16);
+                        for (int i = 0; i < C::OUT_PIECES / 128; ++i) {
+                            const int x = m + 128 * i, n = x / (C::D / 8), u = x % (C::D / 8);
+                            const long long rb = col_base[n];
+                            if (rb >= 0) graw[i] = __ldg(reinterpret_cast<const uint4 *>(gatep + rb * C::D) + u);
                         }
                     }
                 }
@@ -1093,10 +1096,12 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
                 col_f[m] = f;
             }
             softmax_bar();
-            // lane m holds output dimension d = 16 ((m / 16) ^ g') + m % 16 of head g'
-            // in every column (g', r) of O^T
-            __nv_bfloat16 *__restrict__ outp = a.out;
-            float *__restrict__ opart = a.o_part;
+            // O is staged in fp32, in natural dimension order, over the P buffers
+            // (the segment's last PV has completed, and the next P is written by
+            // these threads after the epilogue): lane m holds output dimension
+            // d = 16 ((m / 16) ^ g') + m % 16 of head g' in every column (g', r) of
+            // O^T.  Then every thread writes whole 16-byte pieces of output rows.
+            float *__restrict__ stg = reinterpret_cast<float *>(smem + C::P_OFF);
 #pragma unroll
             for (int c0 = 0; c0 < C::N; c0 += 16) {
                 uint32_t oh[16], ol[16];
@@ -1111,25 +1116,48 @@ __global__ void __launch_bounds__(PagedUmmaCfg<R>::THREADS, PagedUmmaCfg<R>::MIN
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int n = c0 + e;
+                    const int d = 16 * ((m >> 4) ^ (n / R)) + (m & 15);
+                    stg[n * C::D + d] = (__uint_as_float(oh[e]) + 0.0625f * __uint_as_float(ol[e])) * col_f[n];
+                }
+            }
+            softmax_bar();
+            if (!dead) {
+                __nv_bfloat16 *__restrict__ outp = a.out;
+                float *__restrict__ opart = a.o_part;
+#pragma unroll
+                for (int i = 0; i < C::OUT_PIECES / 128; ++i) {
+                    const int x = m + 128 * i, n = x / (C::D / 8), u = x % (C::D / 8);
                     const long long rb = col_base[n];
                     if (rb < 0) continue;
-                    const int d = 16 * ((m >> 4) ^ (n / R)) + (m & 15);
-                    const float o = (__uint_as_float(oh[e]) + 0.0625f * __uint_as_float(ol[e])) * col_f[n];
+                    const float4 v0 = *reinterpret_cast<const float4 *>(stg + n * C::D + 8 * u);
+                    const float4 v1 = *reinterpret_cast<const float4 *>(stg + n * C::D + 8 * u + 4);
+                    float o[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
                     if (w.complete) {
-                        float gsig = 1.f;
                         if constexpr (!RANGE) {
                             if (gated) {
-                                const uint32_t gw = graw[n / 2];
-                                const float gv = __uint_as_float((n & 1) ? (gw & 0xffff0000u) : (gw << 16));
-                                gsig = __fdividef(1.f, 1.f + __expf(-gv));
+                                const uint32_t gw[4] = {graw[i].x, graw[i].y, graw[i].z, graw[i].w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float gv = __uint_as_float((e & 1) ? (gw[e / 2] & 0xffff0000u) : (gw[e / 2] << 16));
+                                    o[e] *= __fdividef(1.f, 1.f + __expf(-gv));
+                                }
                             }
                         }
-                        outp[rb * C::D + d] = __float2bfloat16_rn(o * gsig);
+                        const uint4 pk = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                                                    pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+                        *reinterpret_cast<uint4 *>(outp + rb * C::D + 8 * u) = pk;
                     } else {
-                        opart[rb * C::D + d] = o;
+                        *reinterpret_cast<float4 *>(opart + rb * C::D + 8 * u) = v0;
+                        *reinterpret_cast<float4 *>(opart + rb * C::D + 8 * u + 4) = v1;
                     }
                 }
             }
+            softmax_bar();
+            // P'^T's off-diagonal blocks are never written by the softmax: put back
+            // the zeros the staging overwrote (before the next block's P is
+            // published to the tensor core, which fences the async proxy)
+            for (int i = m; i < C::P_BUFS * 2 * C::P_BYTES / 16; i += 128)
+                reinterpret_cast<uint4 *>(smem + C::P_OFF)[i] = make_uint4(0u, 0u, 0u, 0u);
             if (nonempty && !failed) {
                 tc_fence_before_sync();
                 __syncwarp();
