@@ -39,7 +39,8 @@ import gqa_inputs  # noqa: E402
 METRIC = "GQA decode µs/call and KV-cache HBM GB/s (% of measured GB300 peak)"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gqa_dense_kernel.cuh", "gqa_dense_umma.cuh", "gqa_umma.cuh", "gqa_paged_kernel.cuh",
-                  "gqa_common.cuh", "gqa_params.h", "gqa_dense_impl.cuh", "gqa_paged_impl.cuh"]
+                  "gqa_paged_umma.cuh", "gqa_paged_umma.cu", "gqa_common.cuh", "gqa_params.h", "gqa_launch.h",
+                  "gqa_dense_impl.cuh", "gqa_paged_impl.cuh"]
 
 
 # ---------------------------------------------------------------------------

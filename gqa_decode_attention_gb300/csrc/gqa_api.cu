@@ -433,7 +433,10 @@ int choose_paged_workers(const PagedShape &s, int requested, int dev) {
         const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
         const long occ = paged_occupancy(dev, s) > 0 ? paged_occupancy(dev, s) : 1;
         W = nsm * occ / nhb;
-        if (s.topk_form && 2 * long(s.B) * nhb >= nsm * occ) W = s.B;
+#ifndef GQA_PAGED_TOPK_ONE_PER_REQUEST
+#define GQA_PAGED_TOPK_ONE_PER_REQUEST 1
+#endif
+        if (GQA_PAGED_TOPK_ONE_PER_REQUEST && s.topk_form && 2 * long(s.B) * nhb >= nsm * occ) W = s.B;
     }
     if (W > 65535) W = 65535;
     return W < 1 ? 1 : int(W);

@@ -42,13 +42,18 @@
 // row's reference maximum are dropped.  The normaliser sums the unrounded
 // fp32 weights.
 //
-// Roles (9 warps):
+// Roles (8 warps):
 //   warps 0-3   softmax: thread = TMEM lane m = 8 t + g (token t of the 16,
-//               head g of the 8); the epilogue maps the same lanes to output
-//               dimensions.
-//   warp 4      allocates TMEM; lane 0 issues every MMA, in the order
-//               QK(0), QK(1), PV(0), QK(2), PV(1), ...
-//   warps 5-6   producers (bulk copies, index map of the next stage).
+//               head g of the 8); the epilogue stages O through shared
+//               memory and writes whole 16-byte pieces of output rows.
+//   warp 4      allocates TMEM; lane 0 issues every MMA as its inputs become
+//               ready, the output product of the oldest block first, then the
+//               next score product (two S buffers in TMEM).
+//   warp 5      copies K and warp 6 copies V into separate rings: one bulk
+//               copy per token row piece, or one per block when its 16 rows
+//               are consecutive pool rows.
+//   warp 7      index map: the pool rows and token masks of the coming blocks,
+//               four blocks per round (two memory latencies a round).
 // Every wait is bounded in wall time; on expiry the CTA flags the device
 // error word, stops, drains its own copies and MMAs, frees TMEM and returns.
 #pragma once
