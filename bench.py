@@ -885,6 +885,8 @@ def main(argv=None) -> int:
     p.add_argument("--config", default=gqa_inputs.HEADLINE, choices=sorted(gqa_inputs.CONFIGS))
     p.add_argument("--skv", type=int, default=0,
                    help="override the KV length of a dense configuration (smaller cases for profiling)")
+    p.add_argument("--sq", type=int, default=0,
+                   help="override the decode rows per query head of a dense configuration (row-count sweeps)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -892,13 +894,13 @@ def main(argv=None) -> int:
                    help="small-cache latency sweep (eager and CUDA graph) instead of the benchmark line")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 untimed warm-up steps
-    if args.skv:
+    if args.skv or args.sq:
         import dataclasses
         cfg = gqa_inputs.CONFIGS[args.config]
         if not isinstance(cfg, gqa_inputs.DenseConfig):
-            p.error("--skv applies to dense configurations only")
-        name = f"{cfg.name}@skv{args.skv}"
-        gqa_inputs.CONFIGS[name] = dataclasses.replace(cfg, name=name, Skv=args.skv)
+            p.error("--skv and --sq apply to dense configurations only")
+        name = cfg.name + (f"@skv{args.skv}" if args.skv else "") + (f"@sq{args.sq}" if args.sq else "")
+        gqa_inputs.CONFIGS[name] = dataclasses.replace(cfg, name=name, Skv=args.skv or cfg.Skv, Sq=args.sq or cfg.Sq)
         args.config = name
     if args.impl == "reference":
         return run_reference(args)

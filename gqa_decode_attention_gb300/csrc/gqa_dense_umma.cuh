@@ -48,6 +48,12 @@ namespace gqa {
 #endif
 constexpr uint32_t kIssuerPollNs = GQA_UMMA_ISSUER_POLL_NS;
 
+// Whether the producer waits for Q in TMEM after requesting tile 0 (1) or
+// requests the whole ring at once (0); a compile-time knob for tuning builds.
+#ifndef GQA_UMMA_Q_BEFORE_RING
+#define GQA_UMMA_Q_BEFORE_RING 1
+#endif
+
 // Keys per tile of the tcgen05 engine; a compile-time knob for tuning builds.
 #ifndef GQA_UMMA_TILE_KEYS
 #define GQA_UMMA_TILE_KEYS 64
@@ -175,6 +181,15 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
             for (int it = 0; it < n_it; ++it) {
                 const int st = it % C::STAGES;
                 const int round = it / C::STAGES;
+                // Tile 0 first, then the query rows: every SM starts by asking for
+                // its whole ring at once, and the row threads' plain loads of Q
+                // would queue behind all of it, delaying the first scores by
+                // microseconds; the rest of the ring is requested once Q is in TMEM.
+                if (GQA_UMMA_Q_BEFORE_RING && it == 1 &&
+                    !mbar_wait_bounded(q_ready, 0, a.wait_limit_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 if (round > 0 && !mbar_wait_bounded(&empty[st], (round - 1) & 1, a.wait_limit_ns, abort_flag)) {
                     ok = false;
                     break;
