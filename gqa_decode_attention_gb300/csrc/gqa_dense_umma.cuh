@@ -424,17 +424,21 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                 // Scores stay raw; the scale (log2 domain) enters through the
                 // maximum (exact: the scale is positive) and one fma per weight.
                 const int key0 = key_begin + j * C::BN;
-                const bool need_mask = key0 + C::BN - 1 > mask_from;
+                if (key0 + C::BN - 1 > mask_from) {  // the tile reaches past some row's last visible key
+#pragma unroll
+                    for (int h = 0; h < C::BN / 32; ++h)
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (key0 + h * 32 + c > kmax) sr[h][c] = __float_as_uint(-INFINITY);
+                }
+                // the maximum over four independent chains of three-input maxima (exact)
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int h = 0; h < C::BN / 32; ++h)
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        float t = __uint_as_float(sr[h][c]);
-                        if (need_mask && key0 + h * 32 + c > kmax) t = -INFINITY;
-                        sr[h][c] = __float_as_uint(t);
-                        m4[c & 3] = fmaxf(m4[c & 3], t);
-                    }
+                    for (int c = 0; c < 32; c += 2)
+                        m4[(c >> 1) & 3] =
+                            fmax3(m4[(c >> 1) & 3], __uint_as_float(sr[h][c]), __uint_as_float(sr[h][c + 1]));
                 const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.alpha;
                 // A row whose maximum grew by more than 2^8 takes it as the new
                 // reference; if it had accumulated anything, its O row is rescaled.
@@ -460,7 +464,12 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                         tmem_ld32(lane_base + C::O_COL + c * 32, ov);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * corr);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 o2 = mul2(make_float2(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])),
+                                                   make_float2(corr, corr));
+                            ov[e] = __float_as_uint(o2.x);
+                            ov[e + 1] = __float_as_uint(o2.y);
+                        }
                         tmem_st32(lane_base + C::O_COL + c * 32, ov);
                     }
                     tmem_wait_st();
@@ -471,18 +480,22 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
                 // P = exp2(scale * s - reference) as bf16, straight into the swizzled P tile
                 // P(j) goes to buffer j % NP, last read by PV(j - NP), which is
                 // complete: S(j)'s commit followed QK(j), issued after PV(j - NP).
-                float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+                // weights exp2(scale * s - reference) for two keys at a time (the
+                // two-lane fma rounds each lane as fmaf), summed in two two-lane chains
+                const float2 al2 = make_float2(a.alpha, a.alpha), nm2 = make_float2(-m_use, -m_use);
+                float2 ps2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                 if constexpr (C::P_TMEM) {
                     // one TMEM row of BN/2 columns: keys 2c and 2c+1 in column c
                     uint32_t pk[C::BN / 2];
 #pragma unroll
                     for (int c2 = 0; c2 < C::BN / 2; ++c2) {
                         const int c = 2 * c2;
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.alpha, -m_use));
-                        const float p1 =
-                            fast_exp2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), a.alpha, -m_use));
-                        ps4[c2 & 3] += p0 + p1;
-                        pk[c2] = pack_bf16x2(p0, p1);
+                        const float2 x = fma2(make_float2(__uint_as_float(sr[c >> 5][c & 31]),
+                                                          __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31])),
+                                              al2, nm2);
+                        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                        ps2[c2 & 1] = add2(ps2[c2 & 1], p);
+                        pk[c2] = pack_bf16x2(p.x, p.y);
                     }
                     const uint32_t pt = lane_base + C::P_COL + (j % C::NP) * (C::BN / 2);
                     if constexpr (C::BN / 2 == 32) {
@@ -499,17 +512,18 @@ __global__ void __launch_bounds__(UmmaCfg<D>::THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int c = u * 8 + e * 2;
-                            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), a.alpha, -m_use));
-                            const float p1 =
-                                fast_exp2(fmaf(__uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31]), a.alpha, -m_use));
-                            ps4[e] += p0 + p1;
-                            w[e] = pack_bf16x2(p0, p1);
+                            const float2 x = fma2(make_float2(__uint_as_float(sr[c >> 5][c & 31]),
+                                                              __uint_as_float(sr[(c + 1) >> 5][(c + 1) & 31])),
+                                                  al2, nm2);
+                            const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                            ps2[e & 1] = add2(ps2[e & 1], p);
+                            w[e] = pack_bf16x2(p.x, p.y);
                         }
                         *reinterpret_cast<uint4 *>(prow + ((u ^ (lr & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                     fence_proxy_async_shared();
                 }
-                l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+                l += (ps2[0].x + ps2[1].x) + (ps2[0].y + ps2[1].y);
                 tc_fence_before_sync();
             }
             mbar_arrive(&p_ready[sb]);
