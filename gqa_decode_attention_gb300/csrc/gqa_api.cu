@@ -227,20 +227,41 @@ size_t workspace_bytes(const DenseShape &s, int splits) {
 int blocks_per_split(const DenseShape &s, int splits) { return (s.n_blocks + splits - 1) / splits; }
 
 // What one call launches: the split count (as realised by blocks_per_split),
-// key blocks per split, and the kernel configuration.  A small cache that the
-// automatic choice would split runs instead on the key-lane instance: one CTA
-// per unit, the split done by its warps, no combine pass.  An explicit split
-// count is always honoured as given.  (The key-lane CTA fills an SM, so the
-// units must fit one wave.)
+// key blocks per split, and the kernel configuration.  An explicit split count
+// is always honoured as given.  Otherwise, where the automatic choice would
+// split the cache and the units (batch row, KV head, row group) are few, the
+// key-lane instance takes over: its CTA fills an SM and its warps split the
+// walk, so
+//  - a cache of at most GQA_LANE_MAX_UNIT_BYTES per unit runs as one CTA per
+//    unit (one launch, no combine pass), as long as the units fit one wave;
+//  - a longer cache with at most a quarter as many units as SMs is split
+//    across one wave of key-lane CTAs (SMs / units splits) and combined.
+// Measured on GB300 (device time per call, L2 flushed): batch 1 with 8 KV
+// heads and 1K-8K keys went from 16-18 us to 14 us, and the 128K-key
+// two-row decode from 92 to 87 us; with 64 units (batch 8) the one-wave
+// plan was 1 us slower at 1K keys and 1-4 us faster from 4K, so it is left
+// to the general split choice there.
 struct DensePlan {
     int splits, tps, cfg;
 };
+#ifndef GQA_LANE_MIN_SPLITS
+#define GQA_LANE_MIN_SPLITS 4
+#endif
 DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     const int splits = choose_splits(s, requested, dev);
-    if (requested == 0 && splits > 1 && s.D == s.Dv && (s.D == 64 || s.D == 128) && s.cfg < kLaneCfgs &&
-        long(s.Skv) * s.D * 4 <= long(GQA_LANE_MAX_UNIT_BYTES) &&
-        long(s.B) * s.Hkv * s.row_groups <= long(sm_count(dev)))
-        return {1, s.n_blocks, kLaneCfg + s.cfg};
+    const long units = long(s.B) * s.Hkv * s.row_groups;
+    const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
+    const bool lanes_fit = requested == 0 && splits > 1 && s.D == s.Dv && (s.D == 64 || s.D == 128) &&
+                           s.cfg < 2 && units <= nsm;
+    if (lanes_fit && long(s.Skv) * s.D * 4 <= long(GQA_LANE_MAX_UNIT_BYTES))
+        return {1, s.n_blocks, kLaneCfg + (s.cfg == 0 ? 2 : 1)};
+    if (lanes_fit && nsm / units >= GQA_LANE_MIN_SPLITS) {
+        long ls = nsm / units;
+        if (ls > kMaxSplits) ls = kMaxSplits;
+        if (ls > s.n_blocks) ls = s.n_blocks;
+        const int ltps = blocks_per_split(s, int(ls));
+        return {(s.n_blocks + ltps - 1) / ltps, ltps, kLaneCfg + s.cfg};
+    }
     const int tps = blocks_per_split(s, splits);
     return {(s.n_blocks + tps - 1) / tps, tps, s.cfg};
 }

@@ -21,14 +21,13 @@ struct DenseInst {
 // The launches below rely on the kernel's dynamic shared-memory limit having
 // been raised on the current device: the front end's occupancy query (once
 // per device and kernel, under its lock) does that before any call launches.
-// Key-lane instance for small caches: CFG 0 or 1 (16 or 32 rows), 8 consumer
-// warps as 8 / RB key lanes.
+// Key-lane instance CFG (0, 1 or 2): 8 consumer warps as 8 / RB key lanes.
 template <int D, int DV, int CFG>
 struct DenseLaneInst {
-    static constexpr int RB = 1 << CFG;
+    static constexpr int RB = 1 << dense_lane_rows_cfg(CFG);
     static constexpr int KS = kLaneWarps / RB;
     static constexpr int T = dense_lane_tile_keys(D);
-    static constexpr int S = dense_lane_stages(D);
+    static constexpr int S = dense_lane_stages(CFG);
     using C = DenseCfg<D, DV, RB, T, S, KS>;
     static constexpr auto kernel() { return gqa_dense_split_kernel<D, DV, RB, T, S, KS>; }
 };
@@ -120,8 +119,9 @@ static cudaError_t launch_dense(const DenseLaunch &L) {
         case 3: e = launch_split_cfg<D, DV, 3>(L); break;
         default:
             if constexpr (D == DV && (D == 64 || D == 128)) {
-                e = L.cfg == kLaneCfg ? launch_split_cfg<D, DV, 0, DenseLaneInst>(L)
-                                      : launch_split_cfg<D, DV, 1, DenseLaneInst>(L);
+                e = L.cfg == kLaneCfg       ? launch_split_cfg<D, DV, 0, DenseLaneInst>(L)
+                    : L.cfg == kLaneCfg + 1 ? launch_split_cfg<D, DV, 1, DenseLaneInst>(L)
+                                            : launch_split_cfg<D, DV, 2, DenseLaneInst>(L);
             } else {
                 e = cudaErrorInvalidValue;
             }
@@ -140,8 +140,9 @@ static int dense_occupancy(int cfg) {
         case 3: return occupancy_cfg<D, DV, 3>();
         default:
             if constexpr (D == DV && (D == 64 || D == 128)) {
-                return cfg == kLaneCfg ? occupancy_cfg<D, DV, 0, DenseLaneInst>()
-                                       : occupancy_cfg<D, DV, 1, DenseLaneInst>();
+                return cfg == kLaneCfg       ? occupancy_cfg<D, DV, 0, DenseLaneInst>()
+                       : cfg == kLaneCfg + 1 ? occupancy_cfg<D, DV, 1, DenseLaneInst>()
+                                             : occupancy_cfg<D, DV, 2, DenseLaneInst>();
             } else {
                 return 0;
             }

@@ -67,6 +67,19 @@ struct DenseCfg {
     // floats) and two (maximum, sum) pairs, laid over the drained ring
     static constexpr int MERGE_FLOATS = DV / 2 + 4;
     static_assert(KS == 1 || NC * 32 * MERGE_FLOATS * 4 <= RING_BYTES, "merge area fits the ring");
+    // A consumer waits for tile `it` on its stage's full barrier by phase
+    // parity, which is unambiguous only if that stage's previous tile
+    // (it - STAGES) has landed.  With STAGES a multiple of KS that tile belongs
+    // to the same key lane, which consumed it before.  Otherwise a lane running
+    // ahead of another could see a phase two back as complete (parity alone
+    // cannot tell "tile it - STAGES not landed" from "tile it landed").  So it
+    // first waits on the stage's empty barrier for tile it - STAGES to have
+    // been consumed (hence landed).  That wait is unambiguous: the producer
+    // fills stages in order, so once a lane has consumed tile it - KS every
+    // tile up to it - KS - STAGES has been consumed -- with STAGES >= KS that
+    // includes it - 2 STAGES -- and tile it has not.
+    static constexpr bool TWO_STEP_WAIT = KS > 1 && STAGES % KS != 0;
+    static_assert(STAGES >= KS, "ring at least as deep as the key lanes");
 };
 
 template <int D, int DV, int RB, int T, int STAGES_, int KS = 1>
@@ -195,7 +208,11 @@ __global__ void __launch_bounds__(DenseCfg<D, DV, RB, T, STAGES_, KS>::THREADS,
     for (int it = ks; it < n_it; it += KS) {
         const int st = it % C::STAGES;
         // ldmatrix / mma.sync are warp-collective: the whole warp leaves together.
-        const bool got = mbar_wait_bounded(&full[st], (it / C::STAGES) & 1, a.wait_limit_ns, abort_flag);
+        bool got = true;
+        if constexpr (C::TWO_STEP_WAIT) {
+            if (it >= C::STAGES) got = mbar_wait_bounded(&empty[st], (it / C::STAGES - 1) & 1, a.wait_limit_ns, abort_flag);
+        }
+        got = got && mbar_wait_bounded(&full[st], (it / C::STAGES) & 1, a.wait_limit_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
             failed = true;
             break;

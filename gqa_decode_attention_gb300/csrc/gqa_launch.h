@@ -32,33 +32,43 @@ constexpr int kUmmaCfg = kDenseCfgs;
 inline bool dense_uses_umma(int D, int Dv, int Sq) {
     return D == 256 || (D == 128 && Dv == 128 && Sq >= GQA_D128_UMMA_MIN_SQ);
 }
-// Key-lane instances of the mma.sync kernel for small caches (cfg kLaneCfg +
-// c for the c-th row configuration, c = 0 or 1: 16 or 32 rows): one CTA per
-// (batch row, KV head, row group) takes the whole cache, its 8 consumer warps
-// forming 8 / RB key lanes that split the walk inside the CTA and merge in
-// shared memory -- one launch, no combine pass.  Used when the automatic split
-// count would need several splits and a unit's K and V take at most
-// GQA_LANE_MAX_UNIT_BYTES (head dims 64 and 128).  Measured on GB300 (device
-// time per call, L2 flushed): 1K keys at d64 or 512 at d128 (256 KiB a unit)
-// went from 13.0-16.1 us to 10.9-13.0 us; at 512 KiB a unit the one-CTA walk
-// was already 1-2 us slower than splits + combine.
+// Key-lane instances of the mma.sync kernel (cfg kLaneCfg + c): a CTA whose 8
+// consumer warps form 8 / RB key lanes that split its walk and merge in
+// shared memory.  c = 0: 16 rows, 8 lanes, 8-stage ring (a long walk, as one
+// of several splits); c = 1: 32 rows, 4 lanes, 12 stages; c = 2: 16 rows, 8
+// lanes, 12 stages (a whole small cache in one CTA).  Head dims 64 and 128,
+// tiles of 16 KiB (64 keys at d64, 32 at d128).
+//  - A small cache (K and V of a (batch row, KV head, row group) unit within
+//    GQA_LANE_MAX_UNIT_BYTES) that the automatic split count would split runs
+//    as one CTA per unit: one launch, no combine pass.  Measured on GB300
+//    (device time per call, L2 flushed): 1K keys at d64 or 512 at d128 went
+//    from 13.0-16.1 us to 10.9-13.0 us; at 512 KiB a unit the one-CTA walk was
+//    already 1-2 us slower than splits + combine.
+//  - Past that, few units split across one wave of key-lane CTAs (the plan
+//    is in the front end).
+// Ring depth: 12 stages (192 KiB of loads outstanding on the SM) took the
+// 1K-key d64 cache from 11.8 to 10.9 us against 8 stages, while 8 stages were
+// 4 % faster on a 128K-key walk split 19 ways; halving the tile to keep 16 or
+// 24 stages cost 2 us on the small cache and up to 50 % on long walks.
 constexpr int kLaneCfg = kUmmaCfg + 1;
-constexpr int kLaneCfgs = 2;
+constexpr int kLaneCfgs = 3;
 constexpr int kLaneWarps = 8;
 #ifndef GQA_LANE_MAX_UNIT_BYTES
 #define GQA_LANE_MAX_UNIT_BYTES (256 * 1024)
 #endif
 inline bool dense_is_lane_cfg(int cfg) { return cfg >= kLaneCfg && cfg < kLaneCfg + kLaneCfgs; }
+// mma.sync row configuration (0: 16 rows, 1: 32) of key-lane instance c
+constexpr int dense_lane_rows_cfg(int c) { return c == 1 ? 1 : 0; }
+constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
+constexpr int dense_lane_stages(int c) { return c == 0 ? 8 : 12; }
 // Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM
 // lanes); the mma.sync engine holds the group's rows rounded up to 16, at
 // most 128 (16 or 32 in a key-lane instance).
 inline int dense_rows_per_cta(int cfg) {
-    return cfg == kUmmaCfg ? 128 : dense_is_lane_cfg(cfg) ? dense_cfg_rows(cfg - kLaneCfg) : dense_cfg_rows(cfg);
+    return cfg == kUmmaCfg                ? 128
+           : dense_is_lane_cfg(cfg) ? dense_cfg_rows(dense_lane_rows_cfg(cfg - kLaneCfg))
+                                          : dense_cfg_rows(cfg);
 }
-// Tile keys and ring depth of the key-lane instances: 16 KiB stages, twelve of
-// them in flight (one SM then keeps about 192 KiB of loads outstanding).
-constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
-constexpr int dense_lane_stages(int) { return 12; }
 // Tile keys and ring depth of the 16-row instance at D = 128 (the decode
 // shape with the most traffic); compile-time knobs for tuning builds.
 #ifndef GQA_D128_R16_TILE

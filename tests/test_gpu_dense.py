@@ -117,6 +117,36 @@ def test_key_lanes_vs_oracle(gq, orc, shape):
     assert torch.allclose(l2, lse, atol=1e-4, rtol=0)
 
 
+# Longer caches over few (batch row, KV head) units: one wave of key-lane CTAs,
+# SMs // units splits (at least 4), then the combine.  Tiles per lane from
+# under one to past the ring depth, ragged last splits, both lane layouts.
+LANE_SPLITS = [(1, 2, 5000, 16, 2, 128), (2, 1, 3001, 32, 8, 128), (1, 4, 4100, 16, 2, 64),
+               (4, 1, 2500, 32, 8, 64), (1, 1, 20000, 8, 1, 64), (1, 2, 40000, 16, 2, 128),
+               (1, 1, 60000, 8, 1, 128)]
+
+
+def _lane_plan_splits(B, Sq, Skv, Hq, Hkv, D):
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    units = B * Hkv  # Sq * G <= 32 rows: one row group
+    n_blocks = -(-Skv // 64)
+    ls = min(nsm // units, n_blocks)
+    tps = -(-n_blocks // ls)
+    return nsm // units, -(-n_blocks // tps)
+
+
+@pytest.mark.parametrize("shape", LANE_SPLITS, ids=lambda s: "b{}_sq{}_kv{}_h{}x{}_d{}".format(*s))
+def test_key_lane_splits_vs_oracle(gq, orc, shape):
+    B, Sq, Skv, Hq, Hkv, D = shape
+    per_sm, want = _lane_plan_splits(*shape)
+    assert per_sm >= 4
+    assert gq.gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D) == want
+    q, k, v = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=Skv + Sq)
+    out, lse = _run(gq, q, k, v)
+    ref_o, ref_l = orc.gqa_decode(q, k, v, 1.0 / math.sqrt(D))
+    assert_o_close(out, ref_o, f"O {shape}")
+    assert_lse_close(lse, ref_l, f"LSE {shape}")
+
+
 def test_key_lanes_bound(gq):
     """Past 256 KiB of K and V per (b, g) the automatic choice splits across CTAs."""
     assert gq.gqa_decode_num_splits(1, 1, 1024, 8, 1, 64) == 1       # exactly 256 KiB

@@ -5,8 +5,8 @@ they decode (a memory budget fixed at start-up, real-time loops, hosts that
 hand the library only its inputs and outputs): it keeps the split partials in
 a fixed scratch array inside the library.  Each case below is checked against
 the fp64 oracle at the method's tolerances, and bit for bit against the
-allocating entry point with the same split count (the same kernels run, only
-the partials live elsewhere).  The cases run back to back on different
+allocating entry point given the same split argument (0 = the automatic plan;
+the same kernels run, only the partials live elsewhere).  The cases run back to back on different
 shapes, so every call after the first starts on the previous call's leftover
 scratch; they cover both kernel engines (mma.sync and tcgen05).  A shape
 needing more scratch than exists is refused.  This file is collected last so
@@ -52,7 +52,6 @@ def test_noalloc_matches_oracle_and_allocating_entry_point(gq, orc):
         engines.add(gq.gqa_decode_dense_engine(B, Sq, Skv, Hq, Hkv, D))
         qc, kc, vc = gqa_inputs.dense_inputs(B, Sq, Skv, Hq, Hkv, D, seed=seed)
         q, k, v = qc.cuda(), kc.cuda(), vc.cuda()
-        n_splits = splits if splits > 0 else gq.gqa_decode_num_splits(B, Sq, Skv, Hq, Hkv, D)
         out = torch.full_like(q, float("nan"))
         lse = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device="cuda")
         gq.gqa_decode_noalloc(q, k, v, out, lse, num_splits=splits)
@@ -61,7 +60,7 @@ def test_noalloc_matches_oracle_and_allocating_entry_point(gq, orc):
         ref_o, ref_l = orc.gqa_decode(qc, kc, vc, 1.0 / math.sqrt(D))
         assert_o_close(out.cpu(), ref_o, f"noalloc O {shape} vs oracle")
         assert_lse_close(lse.cpu(), ref_l, f"noalloc LSE {shape} vs oracle")
-        ex_o, ex_l = gq.gqa_decode_ex(q, k, v, num_splits=n_splits)
+        ex_o, ex_l = gq.gqa_decode_ex(q, k, v, num_splits=splits)
         torch.cuda.synchronize()
         assert gq.gqa_device_status() == 0
         assert torch.equal(out, ex_o), f"noalloc O {shape} differs from gqa_decode_ex"
