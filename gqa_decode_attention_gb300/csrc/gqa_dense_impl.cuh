@@ -104,9 +104,8 @@ static int umma_occupancy() {
     auto kern = gqa_dense_umma_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return 0;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM_BYTES) != cudaSuccess) return 0;
-    return n;
+    return tmem_kernel_ctas_per_sm(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, C::THREADS,
+                                   int(C::TMEM_COLS));
 }
 
 template <int D, int DV = D>

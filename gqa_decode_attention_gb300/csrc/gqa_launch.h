@@ -121,6 +121,29 @@ int dense_ctas_per_sm_d256(int cfg);
 // most the number whose row pieces fit 1 KiB per token (8 heads of 128 with
 // 8-bit codes, 4 bf16 heads of 128), and at most 4 when a consumer holds two
 // n-tiles.
+// CTAs of a TMEM-allocating kernel that fit on one SM: the least of what its
+// shared memory, registers, threads and TMEM columns allow.  (The CUDA
+// occupancy query answers 1 for every kernel that allocates TMEM.)  The
+// kernel's dynamic shared-memory limit must have been raised already.
+inline int tmem_kernel_ctas_per_sm(const void *kern, int smem_bytes, int threads, int tmem_cols) {
+    int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, threads_sm = 0;
+    cudaFuncAttributes fa;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
+        return 0;
+    const int by_smem = smem_sm / (smem_bytes + int(fa.sharedSizeBytes) + smem_rsv);
+    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocation unit: 256 per warp
+    const int by_regs = regs_sm / (regs_warp * (threads / 32));
+    const int by_threads = threads_sm / threads;
+    const int by_tmem = 512 / tmem_cols;
+    int n = by_smem < by_regs ? by_smem : by_regs;
+    n = n < by_threads ? n : by_threads;
+    return n < by_tmem ? n : by_tmem;
+}
 inline int paged_heads_per_cta(int D, bool kv8, int Mq, int Hkv) {
     int cap = 1024 / (D * (kv8 ? 1 : 2));
     if (cap > 8) cap = 8;

@@ -39,24 +39,8 @@ int occupancy_inst() {
     auto kern = gqa_paged_umma_kernel<R, RANGE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
         return 0;
-    int dev = 0, smem_sm = 0, smem_rsv = 0, regs_sm = 0, threads_sm = 0;
-    cudaFuncAttributes fa;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess ||
-        cudaFuncGetAttributes(&fa, kern) != cudaSuccess)
-        return 0;
-    const int by_smem = smem_sm / (C::SMEM_BYTES + int(fa.sharedSizeBytes) + smem_rsv);
-    const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocation unit: 256 per warp
-    const int by_regs = regs_sm / (regs_warp * (C::THREADS / 32));
-    const int by_threads = threads_sm / C::THREADS;
-    const int by_tmem = 512 / int(C::TMEM_COLS);
-    int n = by_smem < by_regs ? by_smem : by_regs;
-    n = n < by_threads ? n : by_threads;
-    n = n < by_tmem ? n : by_tmem;
-    return n;
+    return tmem_kernel_ctas_per_sm(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, C::THREADS,
+                                   int(C::TMEM_COLS));
 }
 
 }  // namespace
