@@ -38,9 +38,11 @@ import gqa_inputs  # noqa: E402
 
 METRIC = "GQA decode µs/call and KV-cache HBM GB/s (% of measured GB300 peak)"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["gqa_dense_kernel.cuh", "gqa_dense_umma.cuh", "gqa_umma.cuh", "gqa_paged_kernel.cuh",
-                  "gqa_paged_umma.cuh", "gqa_paged_umma.cu", "gqa_common.cuh", "gqa_params.h", "gqa_launch.h",
-                  "gqa_dense_impl.cuh", "gqa_paged_impl.cuh"]
+# Every source of the library: the kernels, and the host code that picks the
+# kernel, its grid and its split count for a shape (all of which set the DRAM
+# traffic a recorded capture stands for).
+KERNEL_SOURCES = sorted(n for n in os.listdir(os.path.join(ROOT, "gqa_decode_attention_gb300", "csrc"))
+                        if n.endswith((".cu", ".cuh", ".h")))
 
 
 # ---------------------------------------------------------------------------
