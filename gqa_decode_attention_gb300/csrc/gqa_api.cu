@@ -251,9 +251,9 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     const int splits = choose_splits(s, requested, dev);
     const long units = long(s.B) * s.Hkv * s.row_groups;
     const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
-    const bool lanes_fit = requested == 0 && splits > 1 && s.D == s.Dv && (s.D == 64 || s.D == 128) &&
+    const bool lanes_fit = requested == 0 && splits > 1 && dense_has_lanes(s.D, s.Dv) &&
                            s.cfg < 2 && units <= nsm;
-    if (lanes_fit && long(s.Skv) * s.D * 4 <= long(GQA_LANE_MAX_UNIT_BYTES))
+    if (lanes_fit && long(s.Skv) * (s.D + s.Dv) * 2 <= long(GQA_LANE_MAX_UNIT_BYTES))
         return {1, s.n_blocks, kLaneCfg + (s.cfg == 0 ? 2 : 1)};
     if (lanes_fit && nsm / units >= GQA_LANE_MIN_SPLITS) {
         long ls = nsm / units;

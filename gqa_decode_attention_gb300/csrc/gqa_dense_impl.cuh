@@ -27,7 +27,7 @@ struct DenseLaneInst {
     static constexpr int RB = 1 << dense_lane_rows_cfg(CFG);
     static constexpr int KS = kLaneWarps / RB;
     static constexpr int T = dense_lane_tile_keys(D);
-    static constexpr int S = dense_lane_stages(CFG);
+    static constexpr int S = dense_lane_stages(D, DV, CFG);
     using C = DenseCfg<D, DV, RB, T, S, KS>;
     static constexpr auto kernel() { return gqa_dense_split_kernel<D, DV, RB, T, S, KS>; }
 };
@@ -117,7 +117,7 @@ static cudaError_t launch_dense(const DenseLaunch &L) {
         case 2: e = launch_split_cfg<D, DV, 2>(L); break;
         case 3: e = launch_split_cfg<D, DV, 3>(L); break;
         default:
-            if constexpr (D == DV && (D == 64 || D == 128)) {
+            if constexpr (dense_has_lanes(D, DV)) {
                 e = L.cfg == kLaneCfg       ? launch_split_cfg<D, DV, 0, DenseLaneInst>(L)
                     : L.cfg == kLaneCfg + 1 ? launch_split_cfg<D, DV, 1, DenseLaneInst>(L)
                                             : launch_split_cfg<D, DV, 2, DenseLaneInst>(L);
@@ -138,7 +138,7 @@ static int dense_occupancy(int cfg) {
         case 2: return occupancy_cfg<D, DV, 2>();
         case 3: return occupancy_cfg<D, DV, 3>();
         default:
-            if constexpr (D == DV && (D == 64 || D == 128)) {
+            if constexpr (dense_has_lanes(D, DV)) {
                 return cfg == kLaneCfg       ? occupancy_cfg<D, DV, 0, DenseLaneInst>()
                        : cfg == kLaneCfg + 1 ? occupancy_cfg<D, DV, 1, DenseLaneInst>()
                                              : occupancy_cfg<D, DV, 2, DenseLaneInst>();

@@ -37,7 +37,8 @@ inline bool dense_uses_umma(int D, int Dv, int Sq) {
 // shared memory.  c = 0: 16 rows, 8 lanes, 8-stage ring (a long walk, as one
 // of several splits); c = 1: 32 rows, 4 lanes, 12 stages; c = 2: 16 rows, 8
 // lanes, 12 stages (a whole small cache in one CTA).  Head dims 64 and 128,
-// tiles of 16 KiB (64 keys at d64, 32 at d128).
+// tiles of 16 KiB (64 keys at d64, 32 at d128); the d192x128 flavour, 32-key
+// tiles of 20 KiB and 8 stages in every instance.
 //  - A small cache (K and V of a (batch row, KV head, row group) unit within
 //    GQA_LANE_MAX_UNIT_BYTES) that the automatic split count would split runs
 //    as one CTA per unit: one launch, no combine pass.  Measured on GB300
@@ -60,7 +61,10 @@ inline bool dense_is_lane_cfg(int cfg) { return cfg >= kLaneCfg && cfg < kLaneCf
 // mma.sync row configuration (0: 16 rows, 1: 32) of key-lane instance c
 constexpr int dense_lane_rows_cfg(int c) { return c == 1 ? 1 : 0; }
 constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
-constexpr int dense_lane_stages(int c) { return c == 0 ? 8 : 12; }
+// (The d192x128 flavour's 20 KiB stages take 8 in every instance.)
+constexpr int dense_lane_stages(int D, int DV, int c) { return c == 0 || D + DV > 256 ? 8 : 12; }
+// Head sizes with key-lane instances: 64 and 128 (D == Dv), and d192x128.
+constexpr bool dense_has_lanes(int D, int DV) { return (D == DV && (D == 64 || D == 128)) || (D == 192 && DV == 128); }
 // Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM
 // lanes); the mma.sync engine holds the group's rows rounded up to 16, at
 // most 128 (16 or 32 in a key-lane instance).

@@ -58,6 +58,43 @@ def test_dv_small_vs_oracle(gq, orc, shape, splits):
     assert_lse_close(lse, ref_l, f"LSE {shape} splits={splits}")
 
 
+# Key lanes: caches of at most 256 KiB of K and V per (b, g) (409 keys at
+# 640 bytes a key) in one CTA, and longer caches over few units split across
+# one wave of key-lane CTAs (SMs // units splits); both lane layouts (16 and
+# 32 rows), ragged tails, causal rows.
+DV_LANES_ONE = [(1, 1, 409, 8, 1), (1, 2, 300, 16, 2), (1, 4, 350, 16, 2), (2, 1, 200, 32, 8)]
+DV_LANE_SPLITS = [(1, 2, 5000, 64, 8), (2, 1, 3001, 32, 8), (1, 1, 20000, 8, 1), (1, 4, 4100, 16, 2)]
+
+
+@pytest.mark.parametrize("shape", DV_LANES_ONE, ids=lambda s: "b{}_sq{}_kv{}_h{}x{}".format(*s))
+def test_dv_key_lanes_one_cta_vs_oracle(gq, orc, shape):
+    B, Sq, Skv, Hq, Hkv = shape
+    assert gq.gqa_decode_dv_num_splits(B, Sq, Skv, Hq, Hkv, DQK, DV) == 1
+    assert gq.gqa_decode_dv_workspace_bytes(B, Sq, Skv, Hq, Hkv, DQK, DV, 0) == 0
+    q, k, v = _inputs(B, Sq, Skv, Hq, Hkv, seed=Skv * 7 + Sq)
+    out, lse = _run(gq, q, k, v)
+    ref_o, ref_l = orc.gqa_decode_dv(q, k, v, 1.0 / math.sqrt(DQK))
+    assert_o_close(out, ref_o, f"O {shape}")
+    assert_lse_close(lse, ref_l, f"LSE {shape}")
+
+
+@pytest.mark.parametrize("shape", DV_LANE_SPLITS, ids=lambda s: "b{}_sq{}_kv{}_h{}x{}".format(*s))
+def test_dv_key_lane_splits_vs_oracle(gq, orc, shape):
+    B, Sq, Skv, Hq, Hkv = shape
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    units = B * Hkv  # Sq * G <= 32 rows: one row group
+    n_blocks = -(-Skv // 64)
+    ls = min(nsm // units, n_blocks)
+    tps = -(-n_blocks // ls)
+    assert nsm // units >= 4
+    assert gq.gqa_decode_dv_num_splits(B, Sq, Skv, Hq, Hkv, DQK, DV) == -(-n_blocks // tps)
+    q, k, v = _inputs(B, Sq, Skv, Hq, Hkv, seed=Skv * 3 + Sq)
+    out, lse = _run(gq, q, k, v)
+    ref_o, ref_l = orc.gqa_decode_dv(q, k, v, 1.0 / math.sqrt(DQK))
+    assert_o_close(out, ref_o, f"O {shape}")
+    assert_lse_close(lse, ref_l, f"LSE {shape}")
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(8, 4), (8, 2), (16, 4), (64, 8)])
 def test_dv_gqa_bitwise_equals_expanded_mha(gq, Hq, Hkv):
     q, k, v = _inputs(2, 2, 700, Hq, Hkv, seed=Hq * 10 + Hkv)
