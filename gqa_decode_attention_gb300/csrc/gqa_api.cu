@@ -234,18 +234,24 @@ int blocks_per_split(const DenseShape &s, int splits) { return (s.n_blocks + spl
 // walk, so
 //  - a cache of at most GQA_LANE_MAX_UNIT_BYTES per unit runs as one CTA per
 //    unit (one launch, no combine pass), as long as the units fit one wave;
-//  - a longer cache with at most a quarter as many units as SMs is split
-//    across one wave of key-lane CTAs (SMs / units splits) and combined.
+//  - a longer cache is split across one wave of key-lane CTAs (SMs / units
+//    splits) and combined, when the units are at most a quarter of the SMs,
+//    or when that wave still fills at least 80 % of the SMs with splits of at
+//    least GQA_LANE_MIN_SPLIT_KEYS keys.
 // Measured on GB300 (device time per call, L2 flushed): batch 1 with 8 KV
 // heads and 1K-8K keys went from 16-18 us to 14 us, and the 128K-key
-// two-row decode from 92 to 87 us; with 64 units (batch 8) the one-wave
-// plan was 1 us slower at 1K keys and 1-4 us faster from 4K, so it is left
-// to the general split choice there.
+// two-row decode from 92 to 87 us; with 64-72 units (batch 8-9, two splits a
+// unit) splits of 2K keys and more were 2-7 % faster than the general choice
+// and shorter ones up to 1 us slower, and a wave of 120 CTAs (batch 5, three
+// splits) was 2 us slower at 8K-16K keys.
 struct DensePlan {
     int splits, tps, cfg;
 };
 #ifndef GQA_LANE_MIN_SPLITS
 #define GQA_LANE_MIN_SPLITS 4
+#endif
+#ifndef GQA_LANE_MIN_SPLIT_KEYS
+#define GQA_LANE_MIN_SPLIT_KEYS 2048
 #endif
 DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     const int splits = choose_splits(s, requested, dev);
@@ -255,8 +261,12 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
                            s.cfg < 2 && units <= nsm;
     if (lanes_fit && long(s.Skv) * (s.D + s.Dv) * 2 <= long(GQA_LANE_MAX_UNIT_BYTES))
         return {1, s.n_blocks, kLaneCfg + (s.cfg == 0 ? 2 : 1)};
-    if (lanes_fit && nsm / units >= GQA_LANE_MIN_SPLITS) {
-        long ls = nsm / units;
+    const long per_sm = nsm / units;  // key-lane splits a unit gets in one wave
+    const bool one_wave_lanes =
+        per_sm >= GQA_LANE_MIN_SPLITS ||
+        (per_sm >= 2 && 5 * units * per_sm >= 4 * nsm && long(s.Skv) / per_sm >= GQA_LANE_MIN_SPLIT_KEYS);
+    if (lanes_fit && one_wave_lanes) {
+        long ls = per_sm;
         if (ls > kMaxSplits) ls = kMaxSplits;
         if (ls > s.n_blocks) ls = s.n_blocks;
         const int ltps = blocks_per_split(s, int(ls));
