@@ -235,15 +235,17 @@ int blocks_per_split(const DenseShape &s, int splits) { return (s.n_blocks + spl
 //  - a cache of at most GQA_LANE_MAX_UNIT_BYTES per unit runs as one CTA per
 //    unit (one launch, no combine pass), as long as the units fit one wave;
 //  - a longer cache is split across one wave of key-lane CTAs (SMs / units
-//    splits) and combined, when the units are at most a quarter of the SMs,
-//    or when that wave still fills at least 80 % of the SMs with splits of at
-//    least GQA_LANE_MIN_SPLIT_KEYS keys.
+//    splits, combined when there are several), when the units are at most a
+//    quarter of the SMs, or when that wave still fills at least 80 % of the
+//    SMs with splits of at least GQA_LANE_MIN_SPLIT_KEYS keys (down to one
+//    key-lane CTA per unit and no combine pass).
 // Measured on GB300 (device time per call, L2 flushed): batch 1 with 8 KV
 // heads and 1K-8K keys went from 16-18 us to 14 us, and the 128K-key
 // two-row decode from 92 to 87 us; with 64-72 units (batch 8-9, two splits a
 // unit) splits of 2K keys and more were 2-7 % faster than the general choice
 // and shorter ones up to 1 us slower, and a wave of 120 CTAs (batch 5, three
-// splits) was 2 us slower at 8K-16K keys.
+// splits) was 2 us slower at 8K-16K keys; with 128-152 units (batch 16-19,
+// one key-lane CTA a unit) 2K-32K keys were 4-21 % faster.
 struct DensePlan {
     int splits, tps, cfg;
 };
@@ -253,6 +255,7 @@ struct DensePlan {
 #ifndef GQA_LANE_MIN_SPLIT_KEYS
 #define GQA_LANE_MIN_SPLIT_KEYS 2048
 #endif
+
 DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     const int splits = choose_splits(s, requested, dev);
     const long units = long(s.B) * s.Hkv * s.row_groups;
@@ -264,7 +267,7 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     const long per_sm = nsm / units;  // key-lane splits a unit gets in one wave
     const bool one_wave_lanes =
         per_sm >= GQA_LANE_MIN_SPLITS ||
-        (per_sm >= 2 && 5 * units * per_sm >= 4 * nsm && long(s.Skv) / per_sm >= GQA_LANE_MIN_SPLIT_KEYS);
+        (5 * units * per_sm >= 4 * nsm && long(s.Skv) / per_sm >= GQA_LANE_MIN_SPLIT_KEYS);
     if (lanes_fit && one_wave_lanes) {
         long ls = per_sm;
         if (ls > kMaxSplits) ls = kMaxSplits;
