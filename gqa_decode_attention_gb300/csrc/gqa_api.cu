@@ -235,17 +235,20 @@ int blocks_per_split(const DenseShape &s, int splits) { return (s.n_blocks + spl
 //  - a cache of at most GQA_LANE_MAX_UNIT_BYTES per unit runs as one CTA per
 //    unit (one launch, no combine pass), as long as the units fit one wave;
 //  - a longer cache is split across one wave of key-lane CTAs (SMs / units
-//    splits, combined when there are several), when the units are at most a
-//    quarter of the SMs, or when that wave still fills at least 80 % of the
-//    SMs with splits of at least GQA_LANE_MIN_SPLIT_KEYS keys (down to one
-//    key-lane CTA per unit and no combine pass).
+//    splits, combined when there are several) when the units are at most a
+//    quarter of the SMs; when that wave fills at least 80 % of the SMs with
+//    one CTA per unit (no combine pass), or with several whose splits hold at
+//    least GQA_LANE_MIN_SPLIT_KEYS keys; or when one CTA per unit fills 60 %
+//    of the SMs with caches of at most that many keys.
 // Measured on GB300 (device time per call, L2 flushed): batch 1 with 8 KV
 // heads and 1K-8K keys went from 16-18 us to 14 us, and the 128K-key
 // two-row decode from 92 to 87 us; with 64-72 units (batch 8-9, two splits a
 // unit) splits of 2K keys and more were 2-7 % faster than the general choice
 // and shorter ones up to 1 us slower, and a wave of 120 CTAs (batch 5, three
 // splits) was 2 us slower at 8K-16K keys; with 128-152 units (batch 16-19,
-// one key-lane CTA a unit) 2K-32K keys were 4-21 % faster.
+// one key-lane CTA a unit) 600-32K keys were 4-26 % faster; with 96-112 units
+// (63-74 % of the SMs) 1K-2K keys were 4-14 % faster and 4K keys and more
+// 7-50 % slower (one SM then pulls a whole unit).
 struct DensePlan {
     int splits, tps, cfg;
 };
@@ -265,9 +268,11 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     if (lanes_fit && long(s.Skv) * (s.D + s.Dv) * 2 <= long(GQA_LANE_MAX_UNIT_BYTES))
         return {1, s.n_blocks, kLaneCfg + (s.cfg == 0 ? 2 : 1)};
     const long per_sm = nsm / units;  // key-lane splits a unit gets in one wave
+    const long fill_pct = 100 * units * per_sm / nsm;  // SMs the wave occupies
     const bool one_wave_lanes =
         per_sm >= GQA_LANE_MIN_SPLITS ||
-        (5 * units * per_sm >= 4 * nsm && long(s.Skv) / per_sm >= GQA_LANE_MIN_SPLIT_KEYS);
+        (fill_pct >= 80 && (per_sm == 1 || long(s.Skv) / per_sm >= GQA_LANE_MIN_SPLIT_KEYS)) ||
+        (per_sm == 1 && fill_pct >= 60 && s.Skv <= GQA_LANE_MIN_SPLIT_KEYS);
     if (lanes_fit && one_wave_lanes) {
         long ls = per_sm;
         if (ls > kMaxSplits) ls = kMaxSplits;

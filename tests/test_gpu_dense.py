@@ -118,15 +118,16 @@ def test_key_lanes_vs_oracle(gq, orc, shape):
 
 
 # Longer caches over few (batch row, KV head) units: one wave of key-lane CTAs,
-# SMs // units splits, then the combine -- at least 4 splits a unit, or 1-3
-# when the wave fills 80 % of the SMs with splits of 2K keys or more (one
-# split: no combine).  Tiles
+# SMs // units splits, then the combine -- at least 4 splits a unit; one (no
+# combine) when that fills 80 % of the SMs, or 60 % with at most 2K keys; 2-3
+# when the wave fills 80 % of the SMs with splits of 2K keys or more.  Tiles
 # per lane from under one to past the ring depth, ragged last splits, both
 # lane layouts.
 LANE_SPLITS = [(1, 2, 5000, 16, 2, 128), (2, 1, 3001, 32, 8, 128), (1, 4, 4100, 16, 2, 64),
                (4, 1, 2500, 32, 8, 64), (1, 1, 20000, 8, 1, 64), (1, 2, 40000, 16, 2, 128),
                (1, 1, 60000, 8, 1, 128), (8, 1, 8200, 32, 8, 128), (9, 2, 5000, 16, 8, 64),
-               (16, 1, 2100, 32, 8, 128), (19, 2, 2500, 16, 8, 64), (128, 1, 2048, 8, 1, 128)]
+               (16, 1, 2100, 32, 8, 128), (19, 2, 2500, 16, 8, 64), (128, 1, 2048, 8, 1, 128),
+               (16, 1, 600, 32, 8, 128), (12, 2, 1024, 16, 8, 128)]
 
 
 def _lane_plan_splits(B, Sq, Skv, Hq, Hkv, D):
@@ -161,9 +162,14 @@ def test_key_lanes_bound(gq):
     nsm = torch.cuda.get_device_properties(0).multi_processor_count
     if 5 * 40 * (nsm // 40) < 4 * nsm:
         assert gq.gqa_decode_num_splits(5, 1, 8192, 32, 8, 128) != nsm // 40
-    # 96 units, one CTA each, would leave a third of the SMs idle: general choice
-    if 5 * 96 * (nsm // 96) < 4 * nsm:
+    # 96 units, one CTA each, would leave a third of the SMs idle: general
+    # choice unless the caches are short; 80 units: general choice
+    if nsm // 96 == 1 and 100 * 96 // nsm < 80:
         assert gq.gqa_decode_num_splits(12, 1, 8192, 32, 8, 128) > 1
+        if 100 * 96 // nsm >= 60:
+            assert gq.gqa_decode_num_splits(12, 1, 2048, 32, 8, 128) == 1
+    if nsm // 80 == 1 and 100 * 80 // nsm < 60:
+        assert gq.gqa_decode_num_splits(10, 1, 2048, 32, 8, 128) > 1
     # two-split waves need splits of 2K keys or more
     if nsm // 64 == 2 and 5 * 64 * 2 >= 4 * nsm:
         assert gq.gqa_decode_num_splits(8, 1, 2048, 32, 8, 128) != 2
