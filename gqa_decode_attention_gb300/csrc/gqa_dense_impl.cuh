@@ -25,7 +25,7 @@ struct DenseInst {
 template <int D, int DV, int CFG>
 struct DenseLaneInst {
     static constexpr int RB = 1 << dense_lane_rows_cfg(CFG);
-    static constexpr int KS = kLaneWarps / RB;
+    static constexpr int KS = dense_lane_lanes(CFG);
     static constexpr int T = dense_lane_tile_keys(D);
     static constexpr int S = dense_lane_stages(D, DV, CFG);
     using C = DenseCfg<D, DV, RB, T, S, KS>;

@@ -32,13 +32,14 @@ constexpr int kUmmaCfg = kDenseCfgs;
 inline bool dense_uses_umma(int D, int Dv, int Sq) {
     return D == 256 || (D == 128 && Dv == 128 && Sq >= GQA_D128_UMMA_MIN_SQ);
 }
-// Key-lane instances of the mma.sync kernel (cfg kLaneCfg + c): a CTA whose 8
-// consumer warps form 8 / RB key lanes that split its walk and merge in
-// shared memory.  c = 0: 16 rows, 8 lanes, 8-stage ring (a long walk, as one
-// of several splits); c = 1: 32 rows, 4 lanes, 12 stages; c = 2: 16 rows, 8
-// lanes, 12 stages (a whole small cache in one CTA).  Head dims 64 and 128,
-// tiles of 16 KiB (64 keys at d64, 32 at d128); the d192x128 flavour, 32-key
-// tiles of 20 KiB and 8 stages in every instance.
+// Key-lane instances of the mma.sync kernel (cfg kLaneCfg + c): a CTA whose
+// consumer warps form key lanes of RB warps (16 rows each) that split its
+// walk and merge in shared memory.  c = 0: 16 rows, 4 lanes, 8-stage ring
+// (one split of a long walk: two stages a lane, so each lane's next tile
+// loads while it computes); c = 1: 32 rows, 4 lanes, 12 stages; c = 2: 16
+// rows, 8 lanes, 12 stages (a whole small cache in one CTA).  Head dims 64
+// and 128, tiles of 16 KiB (64 keys at d64, 32 at d128); the d192x128
+// flavour, 32-key tiles of 20 KiB and 8 stages in every instance.
 //  - A small cache (K and V of a (batch row, KV head, row group) unit within
 //    GQA_LANE_MAX_UNIT_BYTES) that the automatic split count would split runs
 //    as one CTA per unit: one launch, no combine pass.  Measured on GB300
@@ -49,11 +50,15 @@ inline bool dense_uses_umma(int D, int Dv, int Sq) {
 //    is in the front end).
 // Ring depth: 12 stages (192 KiB of loads outstanding on the SM) took the
 // 1K-key d64 cache from 11.8 to 10.9 us against 8 stages, while 8 stages were
-// 4 % faster on a 128K-key walk split 19 ways; halving the tile to keep 16 or
-// 24 stages cost 2 us on the small cache and up to 50 % on long walks.
+// 4 % faster on a 128K-key walk split 19 ways, and 12 stages up to 6 % slower
+// when split walks fill every SM; halving the tile to keep 16 or 24 stages
+// cost 2 us on the small cache and up to 50 % on long walks.  For split walks
+// 4 lanes with two stages each beat 8 lanes with one (the 128K-key two-row
+// decode 87.0 -> 85.1 us, batch 1 with 4K keys 15.4 -> 13.4 us, no shape
+// slower); 6 lanes with 12 stages gained more on some shapes but lost 6 % at
+// 152 CTAs.
 constexpr int kLaneCfg = kUmmaCfg + 1;
 constexpr int kLaneCfgs = 3;
-constexpr int kLaneWarps = 8;
 #ifndef GQA_LANE_MAX_UNIT_BYTES
 #define GQA_LANE_MAX_UNIT_BYTES (256 * 1024)
 #endif
@@ -63,6 +68,7 @@ constexpr int dense_lane_rows_cfg(int c) { return c == 1 ? 1 : 0; }
 constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
 // (The d192x128 flavour's 20 KiB stages take 8 in every instance.)
 constexpr int dense_lane_stages(int D, int DV, int c) { return c == 0 || D + DV > 256 ? 8 : 12; }
+constexpr int dense_lane_lanes(int c) { return c == 2 ? 8 : 4; }
 // Head sizes with key-lane instances: 64 and 128 (D == Dv), and d192x128.
 constexpr bool dense_has_lanes(int D, int DV) { return (D == DV && (D == 64 || D == 128)) || (D == 192 && DV == 128); }
 // Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM
