@@ -37,7 +37,7 @@ inline bool dense_uses_umma(int D, int Dv, int Sq) {
 // walk and merge in shared memory.  c = 0: 16 rows, 4 lanes, 8-stage ring
 // (one split of a long walk: two stages a lane, so each lane's next tile
 // loads while it computes); c = 1: 32 rows, 4 lanes, 12 stages; c = 2: 16
-// rows, 8 lanes, 12 stages (a whole small cache in one CTA).  Head dims 64
+// rows, 6 lanes, 12 stages (a whole small cache in one CTA).  Head dims 64
 // and 128, tiles of 16 KiB (64 keys at d64, 32 at d128); the d192x128
 // flavour, 32-key tiles of 20 KiB and 8 stages in every instance.
 //  - A small cache (K and V of a (batch row, KV head, row group) unit within
@@ -56,7 +56,9 @@ inline bool dense_uses_umma(int D, int Dv, int Sq) {
 // 4 lanes with two stages each beat 8 lanes with one (the 128K-key two-row
 // decode 87.0 -> 85.1 us, batch 1 with 4K keys 15.4 -> 13.4 us, no shape
 // slower); 6 lanes with 12 stages gained more on some shapes but lost 6 % at
-// 152 CTAs.
+// 152 CTAs.  For a whole small cache 6 lanes over 12 stages matched or beat 8
+// (batch 4 with 400 keys 12.3 -> 10.3 us) and 4 lanes lost 1.3 us on the
+// 1K-key d64 cache.
 constexpr int kLaneCfg = kUmmaCfg + 1;
 constexpr int kLaneCfgs = 3;
 #ifndef GQA_LANE_MAX_UNIT_BYTES
@@ -68,7 +70,7 @@ constexpr int dense_lane_rows_cfg(int c) { return c == 1 ? 1 : 0; }
 constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
 // (The d192x128 flavour's 20 KiB stages take 8 in every instance.)
 constexpr int dense_lane_stages(int D, int DV, int c) { return c == 0 || D + DV > 256 ? 8 : 12; }
-constexpr int dense_lane_lanes(int c) { return c == 2 ? 8 : 4; }
+constexpr int dense_lane_lanes(int c) { return c == 2 ? 6 : 4; }
 // Head sizes with key-lane instances: 64 and 128 (D == Dv), and d192x128.
 constexpr bool dense_has_lanes(int D, int DV) { return (D == DV && (D == 64 || D == 128)) || (D == 192 && DV == 128); }
 // Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM
