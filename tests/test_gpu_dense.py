@@ -220,6 +220,17 @@ def test_same_splits_bitwise_repeatable(gq):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 5000, 64, 8, 128), (1, 1, 1000, 8, 1, 64), (16, 1, 2100, 32, 8, 128)],
+                         ids=["lane_splits", "lane_one_cta_small", "lane_one_cta_per_unit"])
+def test_key_lanes_bitwise_repeatable(gq, shape):
+    """The key-lane merge runs in lane order: repeated calls give the same bits."""
+    q, k, v = gqa_inputs.dense_inputs(*shape, seed=8)
+    a = _run(gq, q, k, v)
+    for _ in range(3):
+        b = _run(gq, q, k, v)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(8, 4), (8, 2), (4, 2), (16, 4), (8, 1), (64, 8), (32, 2)])
 @pytest.mark.parametrize("Sq", [1, 2, 8, 32])
 @pytest.mark.parametrize("D", [128, 256])
@@ -352,6 +363,27 @@ def test_wait_timeout_is_reported_not_hung(gq, D, Sq):
         gq.gqa_debug_set_fault_mode(0)
         gq.gqa_set_wait_limit_ns(0)
     out, lse = gq.gqa_decode_ex(q, k, v, num_splits=2)
+    assert gq.gqa_device_status() == 0
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1000, 8, 1, 64), (1, 2, 5000, 64, 8, 128), (1, 4, 1024, 16, 2, 64)],
+                         ids=["lanes_whole_cache", "lane_splits", "lanes_32_rows"])
+def test_key_lanes_wait_timeout_is_reported_not_hung(gq, shape):
+    """The key-lane instances under the same forced timeout (automatic plan): the
+    lane whose tile never lands gives up, the others stop at the abort flag,
+    every consumer warp still reaches the merge barriers, and the context stays
+    usable."""
+    q, k, v = (t.cuda() for t in gqa_inputs.dense_inputs(*shape, seed=19))
+    gq.gqa_set_wait_limit_ns(50_000_000)
+    gq.gqa_debug_set_fault_mode(1)
+    try:
+        gq.gqa_decode_ex(q, k, v, num_splits=0)
+        assert gq.gqa_device_status() == 6
+    finally:
+        gq.gqa_debug_set_fault_mode(0)
+        gq.gqa_set_wait_limit_ns(0)
+    out, lse = gq.gqa_decode_ex(q, k, v, num_splits=0)
     assert gq.gqa_device_status() == 0
     assert torch.isfinite(out.float()).all()
 

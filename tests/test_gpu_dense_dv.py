@@ -185,6 +185,25 @@ def test_dv_wait_timeout_is_reported_not_hung(gq):
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 409, 8, 1), (1, 2, 5000, 64, 8)], ids=["lanes_whole_cache", "lane_splits"])
+def test_dv_key_lanes_wait_timeout_is_reported_not_hung(gq, shape):
+    """Forced timeout on the d192x128 key-lane instances (automatic plan); the
+    whole-cache one has 6 lanes over 8 stages, so its lanes also take the
+    empty-barrier wait for a stage's previous tile."""
+    q, k, v = (t.cuda() for t in _inputs(*shape, seed=27))
+    gq.gqa_set_wait_limit_ns(50_000_000)
+    gq.gqa_debug_set_fault_mode(1)
+    try:
+        gq.gqa_decode_dv(q, k, v, num_splits=0)
+        assert gq.gqa_device_status() == 6
+    finally:
+        gq.gqa_debug_set_fault_mode(0)
+        gq.gqa_set_wait_limit_ns(0)
+    out, lse = gq.gqa_decode_dv(q, k, v, num_splits=0)
+    assert gq.gqa_device_status() == 0
+    assert torch.isfinite(out.float()).all()
+
+
 FULL = [c for c in gqa_inputs.CONFIGS.values() if isinstance(c, gqa_inputs.DenseConfig) and c.dv != c.D]
 
 
