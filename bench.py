@@ -809,7 +809,7 @@ def run_reference(args) -> int:
 
 def run_latency_grid(args) -> int:
     """Small-cache decode latency over the grid the portability study measured
-    (32/8 heads, d 128, bf16, Sq 1; batch 1 .. 32 x KV length 512 .. 16384):
+    (32/8 heads, d 128, bf16, Sq 1; batch 1 .. 64 x KV length 512 .. 16384):
     per cell the automatic split count, device time per call (CUDA events,
     L2 flushed, median of 20), and host time per call back to back, eager
     and replayed from a captured CUDA graph.  One JSON line per cell."""
@@ -849,8 +849,8 @@ def run_latency_grid(args) -> int:
         return (time.perf_counter() - t0) / n * 1e6
 
     Hq, Hkv, D = 32, 8, 128
-    for B in (1, 8, 32):
-        for N in (512, 2048, 16384):
+    for B in (1, 4, 8, 16, 32, 64):
+        for N in (512, 2048, 8192, 16384):
             q, k, v = gqa_inputs.dense_inputs(B, 1, N, Hq, Hkv, D, 7, device=dev)
             out = torch.empty_like(q)
             lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)

@@ -169,7 +169,10 @@ gqa_status check_dense(int B, int Sq, int Skv, int Hq, int Hkv, int D, DenseShap
 
 // Split count.  The kernel is HBM-bound once about kCtasPerSmTarget CTAs are
 // resident on every SM (enough loads in flight), so:
-//  - units (batch x KV head x row group) already giving that many CTAs: 1 split;
+//  - units (batch x KV head x row group) already giving that many CTAs: 1
+//    split; with small CTAs (kCtasPerSmTarget or more resident) already at
+//    three quarters of that many (measured on GB300 at 512 units against 608:
+//    1 split 3-6 % faster than 2, which leave a partial second wave);
 //  - otherwise the fewest splits that reach the target while the whole grid
 //    stays one wave of resident CTAs;
 //  - when occupancy is too low for that (large CTAs), the split count that
@@ -188,7 +191,7 @@ int choose_splits(const DenseShape &s, int requested, int dev) {
         const long slots = nsm * occ;
         const long target = nsm * (occ < kCtasPerSmTarget ? occ : kCtasPerSmTarget);
         const long max_s = (s.n_blocks + kMinBlocksPerSplit - 1) / kMinBlocksPerSplit;
-        if (units >= target) {
+        if (units >= target || (occ >= kCtasPerSmTarget && 4 * units >= 3 * target)) {
             S = 1;
         } else {
             const long s_min = (target + units - 1) / units;
