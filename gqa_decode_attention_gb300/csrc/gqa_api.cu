@@ -258,6 +258,9 @@ struct DensePlan {
 #ifndef GQA_LANE_MIN_SPLITS
 #define GQA_LANE_MIN_SPLITS 4
 #endif
+#ifndef GQA_LANE_ONE_WAVE
+#define GQA_LANE_ONE_WAVE 1  // 0: small caches only (tuning builds)
+#endif
 #ifndef GQA_LANE_MIN_SPLIT_KEYS
 #define GQA_LANE_MIN_SPLIT_KEYS 2048
 #endif
@@ -272,10 +275,10 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
         return {1, s.n_blocks, kLaneCfg + (s.cfg == 0 ? 2 : 1)};
     const long per_sm = nsm / units;  // key-lane splits a unit gets in one wave
     const long fill_pct = 100 * units * per_sm / nsm;  // SMs the wave occupies
-    const bool one_wave_lanes =
+    const bool one_wave_lanes = GQA_LANE_ONE_WAVE && (
         per_sm >= GQA_LANE_MIN_SPLITS ||
         (fill_pct >= 80 && (per_sm == 1 || long(s.Skv) / per_sm >= GQA_LANE_MIN_SPLIT_KEYS)) ||
-        (per_sm == 1 && fill_pct >= 60 && s.Skv <= GQA_LANE_MIN_SPLIT_KEYS);
+        (per_sm == 1 && fill_pct >= 60 && s.Skv <= GQA_LANE_MIN_SPLIT_KEYS));
     if (lanes_fit && one_wave_lanes) {
         long ls = per_sm;
         if (ls > kMaxSplits) ls = kMaxSplits;
