@@ -103,13 +103,16 @@ const char *gqa_version(void);
  * (Hq/Hkv)*Sq query rows, up to 128 of them, so each K/V byte is read from
  * HBM once per 128 query rows of a group (once for groups of up to 128
  * rows).  When more than one split is used, an LSE-weighted combine kernel
- * produces out / lse.  A small cache that the automatic choice would split
- * (head dim 64 or 128, up to 32 query rows per CTA, at most 256 KiB of K and
- * V per (b, g), B * Hkv * row groups at most the SM count) runs instead as
- * one CTA per (b, g, row group) whose warps
- * split the walk among themselves and merge in shared memory: one launch,
- * no combine, no workspace (the split-count query then reports 1); an
- * explicit split count is always used as given.  Two kernel engines serve the dense calls (see
+ * produces out / lse.  Where the automatic choice would split the walk and
+ * the (b, g, row group) units fit one wave of SMs (head dims 64, 128 and
+ * 192x128, up to 32 query rows per CTA), key-lane CTAs can take over: CTAs
+ * whose warps split their walk among themselves and merge in shared memory.
+ * A small cache (at most 256 KiB of K and V per unit) then runs as one such
+ * CTA per unit -- one launch, no combine, no workspace (the split-count
+ * query reports 1) -- and a longer one as SMs / units such CTAs per unit
+ * (one wave; a single one, again without combine or workspace, when that
+ * fills most SMs).  An explicit split count is always used as given and
+ * never takes key lanes.  Two kernel engines serve the dense calls (see
  * gqa_decode_dense_engine): mma.sync, and tcgen05 for head dim 256 and for
  * head dim 128 from Sq >= 8.
  *
