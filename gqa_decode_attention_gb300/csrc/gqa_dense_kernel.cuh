@@ -21,13 +21,13 @@
 // the combine kernel.  D is the score head size (q, K) and DV the value head
 // size (V, O, partials); they differ only in the d192x128 instance.
 //
-// Small caches (key lanes, KS > 1): the CTA takes the whole cache of its
-// (b, g) -- one split -- and its consumer warps form KS key lanes of RB row
-// blocks; lane k walks the tiles k, k + KS, k + 2 KS, ... of the same ring
-// with its own online-softmax state, and at the end the lanes' (maximum, sum,
-// unnormalised O) are merged in shared memory by lane 0, which writes the
-// result.  One launch and no combine pass: the flash-decoding split of the
-// KV walk, done inside one CTA.
+// Key lanes (KS > 1): the consumer warps form KS key lanes of RB row blocks;
+// lane k walks the tiles k, k + KS, k + 2 KS, ... of the CTA's split through
+// the same ring with its own online-softmax state, and at the end the lanes'
+// (maximum, sum, unnormalised O) are merged in shared memory by lane 0, which
+// writes the result (one split: a small cache, or a unit whose CTA fills an
+// SM, in one launch without a combine pass) or the split's partials.  The
+// flash-decoding split of the KV walk, done inside one CTA.
 //
 // Every mbarrier wait is bounded in wall time; on expiry the CTA flags the
 // device error word, waits (bounded) for its own loads still in flight, and
