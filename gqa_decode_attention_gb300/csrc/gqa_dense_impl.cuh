@@ -21,7 +21,7 @@ struct DenseInst {
 // The launches below rely on the kernel's dynamic shared-memory limit having
 // been raised on the current device: the front end's occupancy query (once
 // per device and kernel, under its lock) does that before any call launches.
-// Key-lane instance CFG (0, 1 or 2): 8 consumer warps as 8 / RB key lanes.
+// Key-lane instance CFG (0, 1 or 2): dense_lane_lanes(CFG) key lanes of RB warps.
 template <int D, int DV, int CFG>
 struct DenseLaneInst {
     static constexpr int RB = 1 << dense_lane_rows_cfg(CFG);

@@ -94,8 +94,8 @@ def test_d128_many_row_groups_vs_oracle(gq, orc, shape, splits):
 
 # Small caches that the automatic choice would split run as one CTA per
 # (b, g, row group) whose warps split the walk (key lanes) and merge in shared
-# memory: 8 lanes of 16 rows or 4 lanes of 32; ragged tails, lanes with no
-# tile (200 keys: 7 tiles of 32 for 8 lanes; 130 and 150 keys: 3 tiles of 64),
+# memory: 6 lanes of 16 rows or 4 lanes of 32; ragged tails, lanes with no
+# tile (200 keys: 7 tiles of 32 for 6 lanes; 130 and 150 keys: 3 tiles of 64),
 # causal rows, the 256 KiB bound.
 LANES = [(1, 1, 1000, 8, 1, 64), (1, 1, 512, 8, 1, 128), (2, 2, 500, 32, 8, 128), (1, 4, 1024, 16, 2, 64),
          (1, 1, 200, 8, 1, 128), (1, 4, 150, 8, 1, 64), (1, 2, 480, 16, 1, 128), (1, 1, 130, 4, 1, 64)]
