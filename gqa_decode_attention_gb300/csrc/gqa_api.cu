@@ -270,9 +270,9 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
     const long units = long(s.B) * s.Hkv * s.row_groups;
     const long nsm = sm_count(dev) > 0 ? sm_count(dev) : 1;
     const bool lanes_fit = requested == 0 && splits > 1 && dense_has_lanes(s.D, s.Dv) &&
-                           s.cfg < 2 && units <= nsm;
+                           s.cfg < dense_lane_row_cfgs(s.D, s.Dv) && units <= nsm;
     if (lanes_fit && long(s.Skv) * (s.D + s.Dv) * 2 <= long(GQA_LANE_MAX_UNIT_BYTES))
-        return {1, s.n_blocks, kLaneCfg + (s.cfg == 0 ? 2 : 1)};
+        return {1, s.n_blocks, dense_lane_cfg_for(s.cfg, true)};
     const long per_sm = nsm / units;  // key-lane splits a unit gets in one wave
     const long fill_pct = 100 * units * per_sm / nsm;  // SMs the wave occupies
     const bool one_wave_lanes = GQA_LANE_ONE_WAVE && (
@@ -284,7 +284,7 @@ DensePlan plan_dense(const DenseShape &s, int requested, int dev) {
         if (ls > kMaxSplits) ls = kMaxSplits;
         if (ls > s.n_blocks) ls = s.n_blocks;
         const int ltps = blocks_per_split(s, int(ls));
-        return {(s.n_blocks + ltps - 1) / ltps, ltps, kLaneCfg + s.cfg};
+        return {(s.n_blocks + ltps - 1) / ltps, ltps, dense_lane_cfg_for(s.cfg, false)};
     }
     const int tps = blocks_per_split(s, splits);
     return {(s.n_blocks + tps - 1) / tps, tps, s.cfg};

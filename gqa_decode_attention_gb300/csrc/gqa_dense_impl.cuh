@@ -21,7 +21,7 @@ struct DenseInst {
 // The launches below rely on the kernel's dynamic shared-memory limit having
 // been raised on the current device: the front end's occupancy query (once
 // per device and kernel, under its lock) does that before any call launches.
-// Key-lane instance CFG (0, 1 or 2): dense_lane_lanes(CFG) key lanes of RB warps.
+// Key-lane instance CFG (0-3): dense_lane_lanes(CFG) key lanes of RB warps.
 template <int D, int DV, int CFG>
 struct DenseLaneInst {
     static constexpr int RB = 1 << dense_lane_rows_cfg(CFG);
@@ -120,7 +120,8 @@ static cudaError_t launch_dense(const DenseLaunch &L) {
             if constexpr (dense_has_lanes(D, DV)) {
                 e = L.cfg == kLaneCfg       ? launch_split_cfg<D, DV, 0, DenseLaneInst>(L)
                     : L.cfg == kLaneCfg + 1 ? launch_split_cfg<D, DV, 1, DenseLaneInst>(L)
-                                            : launch_split_cfg<D, DV, 2, DenseLaneInst>(L);
+                    : L.cfg == kLaneCfg + 2 ? launch_split_cfg<D, DV, 2, DenseLaneInst>(L)
+                                            : launch_split_cfg<D, DV, 3, DenseLaneInst>(L);
             } else {
                 e = cudaErrorInvalidValue;
             }
@@ -141,7 +142,8 @@ static int dense_occupancy(int cfg) {
             if constexpr (dense_has_lanes(D, DV)) {
                 return cfg == kLaneCfg       ? occupancy_cfg<D, DV, 0, DenseLaneInst>()
                        : cfg == kLaneCfg + 1 ? occupancy_cfg<D, DV, 1, DenseLaneInst>()
-                                             : occupancy_cfg<D, DV, 2, DenseLaneInst>();
+                       : cfg == kLaneCfg + 2 ? occupancy_cfg<D, DV, 2, DenseLaneInst>()
+                                             : occupancy_cfg<D, DV, 3, DenseLaneInst>();
             } else {
                 return 0;
             }

@@ -37,7 +37,8 @@ inline bool dense_uses_umma(int D, int Dv, int Sq) {
 // walk and merge in shared memory.  c = 0: 16 rows, 4 lanes, 8-stage ring
 // (one split of a long walk: two stages a lane, so each lane's next tile
 // loads while it computes); c = 1: 32 rows, 4 lanes, 12 stages; c = 2: 16
-// rows, 6 lanes, 12 stages (a whole small cache in one CTA).  Head dims 64
+// rows, 6 lanes, 12 stages (a whole small cache in one CTA); c = 3: 64 rows,
+// 2 lanes of 4 warps, 12 stages (both uses; d128 only).  Head dims 64
 // and 128, tiles of 16 KiB (64 keys at d64, 32 at d128); the d192x128
 // flavour, 32-key tiles of 20 KiB and 8 stages in every instance.
 //  - A small cache (K and V of a (batch row, KV head, row group) unit within
@@ -60,17 +61,26 @@ inline bool dense_uses_umma(int D, int Dv, int Sq) {
 // (batch 4 with 400 keys 12.3 -> 10.3 us) and 4 lanes lost 1.3 us on the
 // 1K-key d64 cache.
 constexpr int kLaneCfg = kUmmaCfg + 1;
-constexpr int kLaneCfgs = 3;
+constexpr int kLaneCfgs = 4;
 #ifndef GQA_LANE_MAX_UNIT_BYTES
 #define GQA_LANE_MAX_UNIT_BYTES (256 * 1024)
 #endif
 inline bool dense_is_lane_cfg(int cfg) { return cfg >= kLaneCfg && cfg < kLaneCfg + kLaneCfgs; }
-// mma.sync row configuration (0: 16 rows, 1: 32) of key-lane instance c
-constexpr int dense_lane_rows_cfg(int c) { return c == 1 ? 1 : 0; }
+// mma.sync row configuration (0: 16 rows, 1: 32, 2: 64) of key-lane instance c
+// Key-lane instance for a CTA of mma.sync row configuration rc (0-2): a
+// whole small cache (whole) or one split of a longer walk.
+inline int dense_lane_cfg_for(int rc, bool whole) { return kLaneCfg + (rc == 2 ? 3 : rc == 1 ? 1 : whole ? 2 : 0); }
+// Row configurations with key-lane instances in use: 16 and 32 rows, and 64
+// rows at d128 (measured on GB300 with 64 rows a CTA: 64/4 heads at Sq 4 over
+// 128K keys 94.3 -> 76.8 us, 128/8 heads at Sq 4, batch 2, 32K keys 101.4 ->
+// 80.9 us; at d64 64/8 heads at Sq 8 over 64K keys went 48.2 -> 52.3 us, so
+// d64 keeps the general choice there).
+inline int dense_lane_row_cfgs(int D, int Dv) { return D == 128 && Dv == 128 ? 3 : 2; }
+constexpr int dense_lane_rows_cfg(int c) { return c == 1 ? 1 : c == 3 ? 2 : 0; }
 constexpr int dense_lane_tile_keys(int D) { return D == 64 ? 64 : 32; }
 // (The d192x128 flavour's 20 KiB stages take 8 in every instance.)
 constexpr int dense_lane_stages(int D, int DV, int c) { return c == 0 || D + DV > 256 ? 8 : 12; }
-constexpr int dense_lane_lanes(int c) { return c == 2 ? 6 : 4; }
+constexpr int dense_lane_lanes(int c) { return c == 2 ? 6 : c == 3 ? 2 : 4; }
 // Head sizes with key-lane instances: 64 and 128 (D == Dv), and d192x128.
 constexpr bool dense_has_lanes(int D, int DV) { return (D == DV && (D == 64 || D == 128)) || (D == 192 && DV == 128); }
 // Query rows per CTA: the tcgen05 engine always holds 128 rows (its TMEM

@@ -105,7 +105,8 @@ const char *gqa_version(void);
  * rows).  When more than one split is used, an LSE-weighted combine kernel
  * produces out / lse.  Where the automatic choice would split the walk and
  * the (b, g, row group) units fit one wave of SMs (head dims 64, 128 and
- * 192x128, up to 32 query rows per CTA), key-lane CTAs can take over: CTAs
+ * 192x128, up to 32 query rows per CTA, 64 at head dim 128), key-lane CTAs
+ * can take over: CTAs
  * whose warps split their walk among themselves and merge in shared memory.
  * A small cache (at most 256 KiB of K and V per unit) then runs as one such
  * CTA per unit -- one launch, no combine, no workspace (the split-count

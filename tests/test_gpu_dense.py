@@ -98,6 +98,7 @@ def test_d128_many_row_groups_vs_oracle(gq, orc, shape, splits):
 # tile (200 keys: 7 tiles of 32 for 6 lanes; 130 and 150 keys: 3 tiles of 64),
 # causal rows, the 256 KiB bound.
 LANES = [(1, 1, 1000, 8, 1, 64), (1, 1, 512, 8, 1, 128), (2, 2, 500, 32, 8, 128), (1, 4, 1024, 16, 2, 64),
+         (1, 4, 400, 64, 4, 128), (2, 3, 300, 64, 4, 128),
          (1, 1, 200, 8, 1, 128), (1, 4, 150, 8, 1, 64), (1, 2, 480, 16, 1, 128), (1, 1, 130, 4, 1, 64)]
 
 
@@ -127,7 +128,8 @@ LANE_SPLITS = [(1, 2, 5000, 16, 2, 128), (2, 1, 3001, 32, 8, 128), (1, 4, 4100, 
                (4, 1, 2500, 32, 8, 64), (1, 1, 20000, 8, 1, 64), (1, 2, 40000, 16, 2, 128),
                (1, 1, 60000, 8, 1, 128), (8, 1, 8200, 32, 8, 128), (9, 2, 5000, 16, 8, 64),
                (16, 1, 2100, 32, 8, 128), (19, 2, 2500, 16, 8, 64), (128, 1, 2048, 8, 1, 128),
-               (16, 1, 600, 32, 8, 128), (12, 2, 1024, 16, 8, 128)]
+               (16, 1, 600, 32, 8, 128), (12, 2, 1024, 16, 8, 128),
+               (1, 4, 5000, 64, 4, 128), (2, 4, 3001, 128, 8, 128)]  # the last two: 64 rows a CTA
 
 
 def _lane_plan_splits(B, Sq, Skv, Hq, Hkv, D):
