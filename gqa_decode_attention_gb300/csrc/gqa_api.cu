@@ -28,6 +28,16 @@ std::atomic<cudaEvent_t> g_ev_after{nullptr};
 
 constexpr int kMaxDevices = 64;
 constexpr int kMinBlocksPerSplit = 2;
+// Fixed cost of a wave of tcgen05 split CTAs, in 64-key blocks of walk.
+// Fitted on GB300 to eight shapes (d128 Sq 8-16 and d256 Sq 8, 1-64 units,
+// explicit split counts): any value from 13 to 16 picks the fastest count
+// measured for each; without it the choice took 2-4 waves of short splits
+// where one wave was 3-14 % faster (batch 8, 32/2 heads, d256, 128K keys:
+// 333.8 -> 323.6 us; batch 8, 64/8 heads, d128 Sq 8, 8K keys: 75.8 -> 65.5 us).
+#ifndef GQA_UMMA_WAVE_FIXED_BLOCKS
+#define GQA_UMMA_WAVE_FIXED_BLOCKS 14
+#endif
+constexpr long kUmmaWaveFixedBlocks = GQA_UMMA_WAVE_FIXED_BLOCKS;
 constexpr long kCtasPerSmTarget = 4;
 constexpr int kMaxSplits = 4096;
 constexpr long kMaxGroupRows = 4096;
@@ -199,10 +209,13 @@ int choose_splits(const DenseShape &s, int requested, int dev) {
             if (s_min <= s_one_wave) {
                 S = int(s_min);
             } else {
+                // a wave of tcgen05 CTAs also pays a fixed start and finish
+                // (TMEM, queries, the first tiles, the epilogue)
+                const long fixed = s.cfg == kUmmaCfg ? kUmmaWaveFixedBlocks : 0;
                 long best = 1, best_cost = -1;
                 for (long c = 1; c <= 4 * s_one_wave + 4 && c <= max_s; ++c) {
                     const long waves = (units * c + slots - 1) / slots;
-                    const long cost = waves * ((s.n_blocks + c - 1) / c);
+                    const long cost = waves * ((s.n_blocks + c - 1) / c + fixed);
                     if (best_cost < 0 || cost < best_cost) {
                         best_cost = cost;
                         best = c;
