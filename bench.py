@@ -889,6 +889,9 @@ def main(argv=None) -> int:
                    help="override the KV length of a dense configuration (smaller cases for profiling)")
     p.add_argument("--sq", type=int, default=0,
                    help="override the decode rows per query head of a dense configuration (row-count sweeps)")
+    p.add_argument("--pages-per-req", type=int, default=0,
+                   help="override the page-table length of a whole-request paged configuration (smaller pools "
+                        "for profiling)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -903,6 +906,14 @@ def main(argv=None) -> int:
             p.error("--skv and --sq apply to dense configurations only")
         name = cfg.name + (f"@skv{args.skv}" if args.skv else "") + (f"@sq{args.sq}" if args.sq else "")
         gqa_inputs.CONFIGS[name] = dataclasses.replace(cfg, name=name, Skv=args.skv or cfg.Skv, Sq=args.sq or cfg.Sq)
+        args.config = name
+    if args.pages_per_req:
+        import dataclasses
+        cfg = gqa_inputs.CONFIGS[args.config]
+        if not isinstance(cfg, gqa_inputs.PagedKVConfig):
+            p.error("--pages-per-req applies to whole-request paged configurations only")
+        name = f"{cfg.name}@ppr{args.pages_per_req}"
+        gqa_inputs.CONFIGS[name] = dataclasses.replace(cfg, name=name, pages_per_req=args.pages_per_req)
         args.config = name
     if args.impl == "reference":
         return run_reference(args)
