@@ -145,3 +145,14 @@ def test_cpu_model_and_single_thread_baseline(orc):
     r = bench._single_thread_baseline(orc, cfg, {"q": q, "k": k, "v": v}, seconds=0.05)
     assert r["cores"] == 1 and r["value"] > 0 and r["unit"] == "GB/s"
     assert orc.num_threads() == threads
+
+
+def test_size_overrides_reject_the_wrong_form():
+    """--skv / --sq shrink dense workloads and --pages-per-req whole-request
+    paged ones; each refuses the other form before any device work."""
+    with pytest.raises(SystemExit):
+        bench.main(["--config", "paged_fp8_b32_h64x8_d128_kv32k_ps16", "--skv", "4096"])
+    with pytest.raises(SystemExit):
+        bench.main(["--config", "dense_b1_h64x8_d128_sq2_kv128k", "--pages-per-req", "512"])
+    with pytest.raises(SystemExit):
+        bench.main(["--config", "paged_fp8_b256_h32x8_d128_top512_ps16", "--pages-per-req", "512"])
